@@ -1,0 +1,98 @@
+/*
+ * lp_oracle.h -- plain CPU oracle for the generation-logprob and greedy
+ * speculative-acceptance epilogue.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may include, link or
+ * call this file; only the tests, the smoke check and the benchmark's CPU
+ * baseline leg use it.  It shares no code, header, table or constant with the
+ * CUDA library: every constant below is restated here on purpose.
+ *
+ * What it computes (sources: "logprobs-design.md", the generation-logprob
+ * contract, and "mtp-design.md", section "A speculative round is a state
+ * transaction", steps 2-3):
+ *
+ *   - lse   = log(sum_v exp(x_v)) over the V unpadded lanes, in FP64, then
+ *             rounded to FP32 (round to nearest even).
+ *   - lp_v  = fl32(x_v - lse), an FP32 subtraction; a -0 result is reported
+ *             as +0 ("signed zero is normalized").
+ *   - natural alternatives: all v sorted by (lp_v descending, v ascending),
+ *             the first min(K, V) reported.
+ *   - explicit IDs: lp of each caller ID, in caller order.
+ *   - greedy acceptance: a = number of leading drafts equal to their row's
+ *             argmax over raw logits (smallest ID among equal maxima, -0 and
+ *             +0 equal); the group emits rows 0..a.
+ *   - record: int32[258] = chosen id, chosen lp bits, then (id, lp bits)
+ *             pairs; unused pairs are (-1, 0x7FC00000).
+ *
+ * Logits are passed as FP32 (BF16 inputs are widened exactly by the caller).
+ * Inputs must be finite; the oracle is not defined for NaN or infinities.
+ */
+#ifndef LP_ORACLE_H
+#define LP_ORACLE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Record geometry: chosen pair + 128 alternative pairs = 258 int32 words. */
+#define ORC_RECORD_WORDS 258
+#define ORC_MAX_PAIRS 128
+#define ORC_NAN_BITS 0x7FC00000u
+
+/* Status bits (same meaning as the library's device status word). */
+#define ORC_STATUS_BAD_ID 0x1u
+#define ORC_STATUS_BAD_TOKEN 0x2u
+#define ORC_STATUS_BAD_COUNT 0x4u
+#define ORC_STATUS_BAD_GROUP 0x8u
+
+/* log-sum-exp of x[0..V) computed in double, rounded to float. V >= 1. */
+float orc_lse(const float* x, int64_t V);
+
+/* Index of the largest x (smallest index among equal maxima). V >= 1. */
+int32_t orc_argmax(const float* x, int64_t V);
+
+/* fl32(x - lse) with -0 reported as +0. */
+float orc_logprob(float x, float lse);
+
+/*
+ * Natural alternatives: sorts all V lanes by (fl32(x - lse) desc, id asc)
+ * with a full stable sort and writes the first n = min(K, V) ids and
+ * logprobs.  Returns n.
+ */
+int32_t orc_topk(const float* x, int64_t V, float lse, int32_t K, int32_t* ids, float* lps);
+
+/* Whole epilogue over one logit block (all pointers are host memory). */
+typedef struct {
+    const float* logits;          /* [rows, Vp]; lanes >= V are ignored */
+    int64_t rows, V, Vp;
+    int32_t groups;
+    const int32_t* group_indptr;   /* [groups+1] */
+    const int32_t* draft_tokens;   /* [rows] */
+    const int32_t* sampled_tokens; /* [groups]; <0 -> argmax */
+    const int32_t* requested;      /* [groups]; nonzero = report */
+    const int32_t* top_k;          /* [groups] */
+    const int32_t* token_ids;      /* [groups, 128] */
+    const int32_t* id_counts;      /* [groups]; 0 -> natural */
+    int32_t k_max;                 /* largest allowed drafts per group */
+    int32_t k_alt_max;             /* largest allowed K (natural alternatives) */
+    int32_t max_ids;               /* largest allowed explicit-ID count */
+    int32_t* records;              /* [rows, 258]; only emitted flagged rows written */
+    int32_t* accepted;             /* [groups] */
+    int32_t* emitted_tokens;       /* [rows]; -1 for rows not emitted */
+    float* lse_out;                /* [rows] or NULL; written for rows whose lse is computed */
+    uint32_t* status;              /* out: status bits */
+    int64_t* rows_read;            /* out (optional): logit rows the path had to read */
+} orc_io;
+
+/* Runs the epilogue; groups are split over `threads` host threads (<=1: one).
+ * Returns 0, or -1 on a NULL required pointer. */
+int orc_epilogue(const orc_io* io, int threads);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif

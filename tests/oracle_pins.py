@@ -1,0 +1,281 @@
+"""Pins for the CPU oracle: checks against what the pages and mathematics fix.
+
+Each pin is a function of an oracle handle (``oracle.load()`` or a mutated
+copy), so the same pins can show that a planted mistake is caught.  Sources:
+
+  * "logprobs-design.md", generation-logprob contract: lp = logit - logsumexp
+    over the full vocabulary (FP32), alternatives by decreasing logprob then
+    increasing id, signed zero normalised, padded lanes excluded, explicit ids
+    in caller order, packed record with -1 for unused ids.
+  * "mtp-design.md", "A speculative round is a state transaction", steps 2-3:
+    a accepted drafts => a+1 emitted tokens.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+
+import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "oracle_cases.json")
+NAN_BITS = 0x7FC00000
+
+
+def _num(v) -> np.float32:
+    return np.float32(float(v))  # "-0.0" strings keep the sign
+
+
+def _golden_row(case) -> np.ndarray:
+    if "x" in case:
+        return np.array([_num(v) for v in case["x"]], np.float32)
+    spec = case["x_spec"]
+    x = np.full(spec["V"], np.float32(spec["fill"]), np.float32)
+    for lo, hi, val in spec["set"]:
+        x[lo:hi + 1] = np.float32(val)
+    return x
+
+
+def f32_ulp(v: np.float32) -> float:
+    v = np.float32(v)
+    return float(np.spacing(np.abs(v)))
+
+
+def bits(v) -> int:
+    return int(np.array([v], np.float32).view(np.uint32)[0])
+
+
+def brute_force_order(lp: np.ndarray) -> np.ndarray:
+    """O(V^2) rank count: rank(v) = #{u: lp_u > lp_v or (lp_u == lp_v and u < v)}."""
+    V = lp.shape[0]
+    ranks = np.empty(V, np.int64)
+    for v in range(V):
+        gt = np.count_nonzero(lp > lp[v])
+        eq_before = np.count_nonzero(lp[:v] == lp[v])
+        ranks[v] = gt + eq_before
+    order = np.empty(V, np.int64)
+    order[ranks] = np.arange(V)
+    return order
+
+
+def independent_lse(x: np.ndarray) -> np.float32:
+    """math.fsum-based logsumexp in double (a different summation than the oracle's)."""
+    xs = [float(v) for v in x]
+    m = max(xs)
+    return np.float32(m + math.log(math.fsum(math.exp(v - m) for v in xs)))
+
+
+# ----------------------------------------------------------------------------- pins
+
+def pin_golden_rows(orc):
+    cases = json.load(open(GOLDEN))["rows"]
+    for c in cases:
+        x = _golden_row(c)
+        want_lse = np.float32(eval(c["lse_expr"], {"math": math}))
+        got_lse = orc.lse(x)
+        assert abs(float(got_lse) - float(want_lse)) <= f32_ulp(want_lse), (c["name"], got_lse, want_lse)
+        assert bits(got_lse) == bits(want_lse) or c["name"] not in ("subtraction_induced_ties", "single_lane_negative_zero"), c["name"]
+        ids, lps = orc.topk(x, c["K"])
+        assert ids.tolist() == c["expected_ids"], (c["name"], ids.tolist())
+        for sid, b in c.get("expected_lp_bits", {}).items():
+            pos = ids.tolist().index(int(sid))
+            assert bits(lps[pos]) == b, (c["name"], sid, hex(bits(lps[pos])), hex(b))
+        assert orc.argmax(x) == c["expected_argmax"], c["name"]
+        # every reported lp is fl32(x - lse) computed here with numpy float32
+        for i, v in zip(ids, lps):
+            want = np.float32(x[i]) - np.float32(got_lse)
+            want = np.float32(0.0) if want == 0 else want
+            assert bits(v) == bits(want), (c["name"], int(i))
+
+
+def pin_golden_groups(orc):
+    for c in json.load(open(GOLDEN))["groups"]:
+        V = c["V"]
+        rows = np.array([[_num(v) for v in r] for r in c["rows"]], np.float32)
+        n = rows.shape[0]
+        w = W.custom(rows, V, [n], drafts=c["drafts"], top_k=[2], k_max=n - 1)
+        sentinel = np.full((n, 258), 0x5A5A5A5A, np.int32)
+        r = orc.epilogue(w.logits_f32(), V, **w.inputs(), k_max=w.k_max, records=sentinel.copy())
+        for j, a in enumerate(c["expected_argmax"]):
+            assert orc.argmax(rows[j]) == a, (c["name"], j)
+        assert int(r["accepted"][0]) == c["expected_accepted"], c["name"]
+        assert r["emitted_tokens"].tolist() == c["expected_emitted"], c["name"]
+        assert r["rows_read"] == c["expected_rows_read"], c["name"]
+        acc = c["expected_accepted"]
+        for j in range(n):
+            if j <= acc:
+                assert r["records"][j, 0] == c["expected_emitted"][j]
+                assert r["records"][j, 2 + 2 * 2] == -1 and r["records"][j, 3 + 2 * 2] == NAN_BITS
+            else:
+                assert (r["records"][j] == 0x5A5A5A5A).all(), (c["name"], j)
+
+
+def _bf_rows(rng):
+    out = []
+    for V in (1, 2, 3, 5, 17, 33, 64, 100):
+        out.append(("random", rng.normal(0, 3, V).astype(np.float32)))
+        out.append(("tied", np.round(rng.normal(0, 1, V) * 2).astype(np.float32) / 2))
+        z = rng.normal(0, 1, V).astype(np.float32)
+        m = rng.random(V) < 0.4
+        z[m] = np.where(rng.random(m.sum()) < 0.5, np.float32(-0.0), np.float32(0.0))
+        out.append(("signed_zero", z))
+    # a row whose subtraction merges distinct logits
+    out.append(("collapse", np.concatenate([[np.float32(3000.0)], rng.uniform(0, 0.01, 60).astype(np.float32)])))
+    return out
+
+
+def pin_brute_force(orc):
+    rng = np.random.default_rng(1234)
+    for kind, x in _bf_rows(rng):
+        lse = orc.lse(x)
+        lp = (x.astype(np.float32) - np.float32(lse)).astype(np.float32)
+        lp[lp == 0] = np.float32(0.0)
+        order = brute_force_order(lp)
+        am = int(np.flatnonzero(x == x.max())[0])
+        assert orc.argmax(x) == am, kind
+        for K in (0, 1, 5, 20, 25):
+            ids, lps = orc.topk(x, K, lse)
+            n = min(K, x.size)
+            assert ids.tolist() == order[:n].tolist(), (kind, x.size, K)
+            assert [bits(v) for v in lps] == [bits(lp[i]) for i in order[:n]], (kind, x.size, K)
+
+
+def pin_lse_independent(orc):
+    import torch
+    rng = np.random.default_rng(99)
+    cases = [rng.normal(0, s, V).astype(np.float32) for s, V in ((1, 7), (3, 1000), (3, 248_320), (4, 20_000))]
+    cases.append(np.full(513, np.float32(-7.25), np.float32))
+    for x in cases:
+        got = orc.lse(x)
+        a = independent_lse(x)
+        b = np.float32((torch.from_numpy(x.astype(np.float64))[0]
+                        - torch.log_softmax(torch.from_numpy(x.astype(np.float64)), 0)[0]).item())
+        for want in (a, b):
+            assert abs(float(got) - float(want)) <= f32_ulp(want), (x.size, got, want)
+
+
+def pin_two_value_closed_form(orc):
+    for a, d in ((0.0, 0.5), (10.0, 3.0), (-4.0, 20.0), (1e3, 1e-3)):
+        x = np.array([a, a - d], np.float32)
+        want = np.float32(float(x[0]) + math.log1p(math.exp(float(x[1]) - float(x[0]))))
+        got = orc.lse(x)
+        assert abs(float(got) - float(want)) <= f32_ulp(want), (a, d, got, want)
+        lp0 = orc.logprob(x[0], got)
+        assert bits(lp0) == bits(np.float32(x[0]) - got), (a, d)
+
+
+def pin_sum_exp_invariant(orc):
+    rng = np.random.default_rng(5)
+    for V, s in ((1000, 2.0), (151_936, 2.5), (262_144, 4.0)):
+        x = rng.normal(0, s, V).astype(np.float32)
+        lse = orc.lse(x)
+        total = float(np.exp(x.astype(np.float64) - np.float64(lse)).sum())
+        assert abs(total - 1.0) <= 1e-5, (V, total)
+
+
+def pin_pad_exclusion(orc):
+    w = W.tiny()
+    base = orc.epilogue(w.logits_f32(), w.V, **w.inputs(), k_max=w.k_max)
+    x = w.logits_f32().copy()
+    x[:, w.V:] = np.float32(-3.0)        # different pad contents
+    alt = orc.epilogue(x, w.V, **w.inputs(), k_max=w.k_max)
+    for key in ("records", "accepted", "emitted_tokens"):
+        assert np.array_equal(base[key], alt[key]), key
+    # and a leak of +1e30 pads would make lse ~1e30
+    assert np.nanmax(base["lse"]) < 100.0
+
+
+def pin_id_passthrough(orc):
+    rng = np.random.default_rng(7)
+    x = rng.normal(0, 2, 300).astype(np.float32)
+    ids = [299, 0, 17, 5, 128, 64]
+    lse = orc.lse(x)
+    nat_ids, nat_lps = orc.topk(x, 300, lse)
+    nat = {int(i): bits(v) for i, v in zip(nat_ids, nat_lps)}
+    w = W.custom(x[None, :], 300, [1], top_k=[20], token_ids=[ids], id_counts=[len(ids)])
+    r = orc.epilogue(w.logits_f32(), 300, **w.inputs())
+    rec = r["records"][0]
+    for i, tid in enumerate(ids):
+        assert rec[2 + 2 * i] == tid
+        assert (int(rec[3 + 2 * i]) & 0xFFFFFFFF) == nat[tid]
+    for i in range(len(ids), 128):
+        assert rec[2 + 2 * i] == -1 and rec[3 + 2 * i] == NAN_BITS
+
+
+def pin_acceptance_prefixes(orc):
+    rng = np.random.default_rng(11)
+    k, V = 5, 64
+    for a in range(k + 1):
+        rows = rng.normal(0, 1, (k + 1, V)).astype(np.float32)
+        am = rng.integers(0, V, k + 1)
+        rows[np.arange(k + 1), am] = 10.0
+        drafts = np.full(k + 1, -1, np.int32)
+        drafts[:k] = am[:k]
+        if a < k:
+            drafts[a] = (am[a] + 1) % V
+        w = W.custom(rows, V, [k + 1], drafts=drafts, top_k=[3], k_max=k)
+        sentinel = np.full((k + 1, 258), 0x33, np.int32)
+        r = orc.epilogue(w.logits_f32(), V, **w.inputs(), k_max=k, records=sentinel.copy())
+        assert int(r["accepted"][0]) == a
+        assert r["rows_read"] == a + 1
+        want = [int(am[j]) for j in range(a + 1)] + [-1] * (k - a)
+        assert r["emitted_tokens"].tolist() == want, (a, r["emitted_tokens"])
+        for j in range(k + 1):
+            if j <= a:
+                assert r["records"][j, 0] == am[j] and r["records"][j, 2] == am[j]
+            else:
+                assert (r["records"][j] == 0x33).all()
+
+
+def pin_tiny_workload(orc):
+    w = W.tiny()
+    sentinel = np.full((w.rows, 258), 0x11, np.int32)
+    r = orc.epilogue(w.logits_f32(), w.V, **w.inputs(), k_max=w.k_max, records=sentinel.copy())
+    assert r["accepted"].tolist() == [2, 0, 0]
+    assert r["rows_read"] == 4                      # rows 0, 1, 2 and 4
+    em = r["emitted_tokens"].tolist()
+    assert em[:3] == [int(w.draft_tokens[0]), int(w.draft_tokens[1]), int(w.planted_argmax[2])]
+    assert em[3] == -1 and em[4] == int(w.sampled_tokens[1]) and em[5] == int(w.sampled_tokens[2])
+    assert (r["records"][3] == 0x11).all() and (r["records"][5] == 0x11).all()
+    rec4 = r["records"][4]
+    assert [int(rec4[2 + 2 * i]) for i in range(15)] == w.token_ids[1, :15].tolist()
+    assert w.token_ids[1, :3].tolist() == [7, 999, 3]
+    assert r["status"] == 0
+
+
+def pin_wide_tie(orc):
+    w = W.wide()
+    r = orc.epilogue(w.logits_f32(), w.V, **w.inputs(), k_max=w.k_max)
+    assert r["accepted"].tolist() == [3]
+    x = w.logits_f32(3)
+    tied = np.flatnonzero(x[:w.V] == np.float32(16.0))
+    assert tied.size == 64
+    rec = r["records"][3]
+    assert [int(rec[2 + 2 * i]) for i in range(20)] == sorted(tied.tolist())[:20]
+    assert rec[0] == tied.min()
+
+
+def pin_status_bits(orc):
+    x = np.arange(10, dtype=np.float32)[None, :].repeat(3, 0)
+    # bad explicit id, bad sampled token, bad count
+    w = W.custom(x, 10, [1, 1, 1], sampled=[-1, 12, -1], requested=[1, 0, 1], top_k=[20, 0, 40],
+                 token_ids=[[3, 10, -2], None, None], id_counts=[3, 0, 0])
+    r = orc.epilogue(w.logits_f32(), 10, **w.inputs())
+    rec = r["records"][0]
+    assert rec[2:8].view(np.uint32).tolist() == [3, bits(np.float32(3) - orc.lse(x[0])), 10, NAN_BITS,
+                                                 0xFFFFFFFE, NAN_BITS]
+    assert r["status"] == (0x1 | 0x2 | 0x4)
+    assert r["emitted_tokens"][1] == 12
+    assert r["rows_read"] == 2          # row 1: unflagged k=0 with a sampled token is not read
+    # malformed groups: nothing written
+    w2 = W.custom(x, 10, [2, 1], k_max=0)
+    r2 = orc.epilogue(w2.logits_f32(), 10, **w2.inputs(), k_max=0)
+    assert r2["status"] == 0x8 and r2["rows_read"] == 0
+    assert (r2["emitted_tokens"] == -7).all()
+
+
+ALL_PINS = [pin_golden_rows, pin_golden_groups, pin_brute_force, pin_lse_independent,
+            pin_two_value_closed_form, pin_sum_exp_invariant, pin_pad_exclusion, pin_id_passthrough,
+            pin_acceptance_prefixes, pin_tiny_workload, pin_status_bits]
