@@ -1,0 +1,201 @@
+/*
+ * lp_epilogue.h -- C ABI of the GB300 (sm_103a) generation-logprob and greedy
+ * speculative-acceptance epilogue.
+ *
+ * The operation (sources: "logprobs-design.md", the generation-logprob
+ * captured-graph contract; "mtp-design.md", section "A speculative round is a
+ * state transaction", steps 2-3):
+ *
+ *   Input is a block of target logits [rows, V_padded] (FP32 or BF16), split
+ *   into verify groups.  Group g owns rows group_indptr[g] .. group_indptr[g+1]-1
+ *   = [p, d0, ..., d(k-1)]: row j holds the target logits that check draft
+ *   draft_tokens[row] (j < k); row k yields the bonus token.
+ *
+ *   1. Greedy acceptance.  a = number of leading rows j < k whose draft equals
+ *      the row's argmax over raw logits (smallest id among equal maxima; -0 and
+ *      +0 are one value).  The group emits rows 0..a: the chosen token of row
+ *      j is its argmax (equal to the draft for j < a; the correction or bonus
+ *      token for j = a).  A k = 0 group emits one row whose chosen token is
+ *      sampled_tokens[g] when that is >= 0, else the argmax.
+ *      ("with a accepted drafts ... produces a+1 newly generated tokens")
+ *   2. For every emitted row of a group whose requested[g] is nonzero:
+ *      lse = log sum_v exp(logits[v]) over the V unpadded lanes, accumulated
+ *      in FP32; lp(v) = fl32(logits[v] - lse), -0 reported as +0.
+ *      ("report logits[t] - logsumexp(logits) over the full vocabulary ...,
+ *      accumulating in FP32")
+ *   3. The record of that row (258 int32 words):
+ *        [0] chosen token id, [1] FP32 bits of its lp,
+ *        [2+2i], [3+2i] = (id, lp bits) of alternative i:
+ *          - id_counts[g] == 0: the top_k[g] (<= k_alt_max) natural
+ *            alternatives, ordered by lp descending then id ascending, ties
+ *            created by the FP32 subtraction included;
+ *          - id_counts[g] = c > 0: token_ids[g][0..c) in caller order;
+ *        every other pair = (-1, 0x7FC00000).
+ *      ("chosen token ID, chosen FP32 logprob bits, then pairs of alternative
+ *      ID and FP32 logprob bits"; "unused alternative IDs are -1")
+ *   4. Rows past a group's emitted prefix are never read; a k = 0 group with
+ *      requested[g] == 0 and sampled_tokens[g] >= 0 reads nothing.  Records of
+ *      rows that are not emitted, or whose group is not requested, are not
+ *      written.  ("A packed request's columns beyond its committed prefix are
+ *      never read"; "A zero request flag bypasses vocabulary reads, sorting,
+ *      and payload writes")
+ *
+ * Lifetime: lp_plan_create allocates all device scratch once; lp_bind records
+ * caller-owned device pointers; lp_run only enqueues kernels on the caller's
+ * stream (no allocation, no host synchronisation; capturable in a CUDA graph).
+ * One plan serves one stream at a time; the plan must outlive queued work.
+ * Binds and runs of one plan are not thread-safe.
+ *
+ * Errors: every function returns LP_OK (0) or a negative LP_E* code and never
+ * aborts.  Conditions only visible on the device are reported in the bound
+ * status word (LP_STATUS_* bits), which each lp_run resets to 0 first.
+ */
+#ifndef LP_EPILOGUE_H
+#define LP_EPILOGUE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define LP_RECORD_WORDS 258          /* chosen pair + 128 alternative pairs */
+#define LP_MAX_IDS 128               /* explicit-id slots per group */
+#define LP_MAX_K_ALT 32              /* largest natural-alternative count a plan accepts */
+#define LP_MAX_DRAFTS 15             /* largest k (drafts per group) a plan accepts */
+#define LP_UNUSED_LP_BITS 0x7FC00000u /* lp bits of an unused pair (a quiet NaN) */
+
+/* Element type of the logit block. */
+typedef enum { LP_F32 = 0, LP_BF16 = 1 } lp_dtype;
+
+/* Host error codes. */
+enum {
+    LP_OK = 0,
+    LP_EINVAL = -1,    /* NULL pointer or nonsensical argument */
+    LP_ESHAPE = -2,    /* sizes inconsistent (V > V_padded, rows > max_rows, ...) */
+    LP_EALIGN = -3,    /* logits not 16-byte aligned, or V_padded * elt not a multiple of 16 */
+    LP_ECAPACITY = -4, /* request beyond the plan's limits (k_max, k_alt_max, max_ids) */
+    LP_EDTYPE = -5,    /* unknown dtype */
+    LP_ECUDA = -6,     /* a CUDA runtime call failed (see lp_last_cuda_error) */
+    LP_ESTATE = -7     /* lp_run before lp_bind, or host staging not enabled */
+};
+
+/* Device status bits (OR-ed into *status by a run). */
+#define LP_STATUS_BAD_ID 0x1u    /* explicit id outside [0, V): pair = (id, 0x7FC00000) */
+#define LP_STATUS_BAD_TOKEN 0x2u /* sampled token >= V: chosen lp bits = 0x7FC00000 */
+#define LP_STATUS_BAD_COUNT 0x4u /* id count outside [0, max_ids] or top_k outside [0, k_alt_max]: clamped */
+#define LP_STATUS_BAD_GROUP 0x8u /* group_indptr malformed: the run reads and writes nothing else */
+#define LP_STATUS_TIMEOUT 0x10u  /* a bounded device wait expired: outputs are incomplete */
+
+/* Plan flags. */
+#define LP_PLAN_HOST_STAGING 0x1u     /* also allocate device staging so lp_run_host can be used */
+#define LP_PLAN_DEBUG_FORCE_TIMEOUT 0x100u /* test hook: every bounded wait runs out (no reads) */
+
+typedef struct {
+    int32_t max_rows;     /* capacity: rows per run (>= 1) */
+    int32_t max_groups;   /* capacity: groups per run (>= 1) */
+    int32_t k_max;        /* largest drafts per group, 0..LP_MAX_DRAFTS */
+    int64_t V;            /* unpadded vocabulary (>= 1) */
+    int64_t V_padded;     /* row stride in elements (>= V) */
+    int32_t dtype;        /* lp_dtype */
+    int32_t k_alt_max;    /* largest top_k, 0..LP_MAX_K_ALT */
+    int32_t max_ids;      /* largest id count, 0..LP_MAX_IDS */
+    int32_t device;       /* CUDA device ordinal the plan lives on */
+    uint32_t flags;       /* LP_PLAN_* */
+    int64_t timeout_ns;   /* limit of every device-side wait, from kernel start; 0 = 1 s */
+} lp_plan_desc;
+
+/* Buffers of one run.  Device pointers for lp_bind, host pointers for
+ * lp_run_host.  Layouts are dense row-major:
+ *   logits         [rows, V_padded] of dtype   (input; lanes >= V are never used)
+ *   group_indptr   int32 [groups + 1]          (0 <= indptr[0] < ... <= rows; sizes 1..k_max+1)
+ *   draft_tokens   int32 [rows]                (row indptr[g]+j carries draft j of group g)
+ *   sampled_tokens int32 [groups]              (k = 0 groups: chosen token; < 0 = argmax)
+ *   requested      int32 [groups]              (nonzero = report logprobs)
+ *   top_k          int32 [groups]              (natural alternatives, 0..k_alt_max)
+ *   token_ids      int32 [groups, 128]         (explicit ids, caller order)
+ *   id_counts      int32 [groups]              (0 = natural alternatives; 1..max_ids = explicit)
+ *   records        int32 [rows, 258]           (output; only emitted rows of requested groups)
+ *   accepted       int32 [groups]              (output: a, the accepted drafts)
+ *   emitted_tokens int32 [rows]                (output: chosen token, -1 past the prefix)
+ *   lse_out        float [rows] or NULL        (output: lse of rows whose record is written)
+ *   status         uint32 [1]                  (output: LP_STATUS_* bits)
+ */
+typedef struct {
+    const void* logits;
+    const int32_t* group_indptr;
+    const int32_t* draft_tokens;
+    const int32_t* sampled_tokens;
+    const int32_t* requested;
+    const int32_t* top_k;
+    const int32_t* token_ids;
+    const int32_t* id_counts;
+    int32_t* records;
+    int32_t* accepted;
+    int32_t* emitted_tokens;
+    float* lse_out;
+    uint32_t* status;
+    int32_t rows;
+    int32_t groups;
+} lp_io;
+
+typedef struct lp_plan_s* lp_plan_t;
+
+/* Creates a plan on desc->device and allocates its device scratch (once).
+ * Errors: LP_EINVAL, LP_ESHAPE, LP_EDTYPE, LP_ECAPACITY, LP_ECUDA. */
+int lp_plan_create(lp_plan_t* out, const lp_plan_desc* desc);
+
+/* Frees the plan's scratch.  The caller must have drained work queued with it. */
+int lp_plan_destroy(lp_plan_t plan);
+
+/* Device bytes lp_plan_create allocates for desc (0 if desc is invalid). */
+size_t lp_plan_scratch_bytes(const lp_plan_desc* desc);
+
+/* Validates and records the device buffers of the next runs.  Checks NULLs,
+ * rows <= max_rows, groups <= max_groups, 16-byte alignment of logits and
+ * 4-byte alignment of the int32 buffers.  Contents are validated on the
+ * device (status bits).  Errors: LP_EINVAL, LP_ESHAPE, LP_EALIGN. */
+int lp_bind(lp_plan_t plan, const lp_io* io);
+
+/* Enqueues the epilogue over the bound buffers on `stream` (a cudaStream_t;
+ * NULL = legacy default stream).  Returns after enqueueing.  Errors:
+ * LP_ESTATE (nothing bound), LP_ECUDA (launch failed). */
+int lp_run(lp_plan_t plan, void* stream);
+
+/* Same operation over HOST buffers (pinned for asynchronous copies): copies the
+ * inputs and the output buffers (so that rows the run does not write keep the
+ * caller's contents) to plan-owned device staging, runs, and copies records,
+ * accepted, emitted_tokens, lse_out (if non-NULL) and status back, all on
+ * `stream`.
+ * Returns after enqueueing; synchronise the stream before reading outputs.
+ * Needs a plan created with LP_PLAN_HOST_STAGING (else LP_ESTATE).
+ * Host buffers must stay valid until the stream reaches the end of the copies. */
+int lp_run_host(lp_plan_t plan, const lp_io* host_io, void* stream);
+
+/* Bytes lp_run_host copies host->device and device->host for host_io. */
+int lp_run_host_bytes(lp_plan_t plan, const lp_io* host_io, int64_t* h2d, int64_t* d2h);
+
+/* Debug: number of vocabulary tiles the last run read for each row (0 = the
+ * row was never read), copied into host_tiles[0..rows).  Synchronises the
+ * plan's last stream.  Tiles hold 8192 elements (the last one of a row fewer). */
+int lp_debug_tiles_read(lp_plan_t plan, int32_t* host_tiles, int32_t rows);
+
+/* Debug: fills the plan's per-tile partial-result scratch with NaN bytes on
+ * `stream` (to show that no result depends on stale scratch). */
+int lp_debug_poison_scratch(lp_plan_t plan, void* stream);
+
+/* Tiles per row for this plan (ceil(V / 8192)). */
+int lp_plan_tiles_per_row(lp_plan_t plan);
+
+/* Message of an LP_E* code. */
+const char* lp_strerror(int code);
+
+/* The last cudaError_t seen by this library in the calling thread (0 = none). */
+int lp_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LP_EPILOGUE_H */

@@ -1,0 +1,266 @@
+"""Python binding of liblp_epilogue.so: the GB300 generation-logprob and greedy
+speculative-acceptance epilogue.
+
+Argument marshalling only: every step of the operation runs in the library's
+CUDA kernels (see ``include/lp_epilogue.h`` for the contract).  PyTorch is used
+for device memory and streams.  There is no fallback: if the library is not
+built, or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "liblp_epilogue.so")
+
+RECORD_WORDS = 258
+MAX_IDS = 128
+UNUSED_LP_BITS = 0x7FC00000
+TILE_ELEMS = 8192
+
+LP_F32, LP_BF16 = 0, 1
+STATUS_BAD_ID = 0x1
+STATUS_BAD_TOKEN = 0x2
+STATUS_BAD_COUNT = 0x4
+STATUS_BAD_GROUP = 0x8
+STATUS_TIMEOUT = 0x10
+PLAN_HOST_STAGING = 0x1
+PLAN_DEBUG_FORCE_TIMEOUT = 0x100
+
+ERRORS = {0: "LP_OK", -1: "LP_EINVAL", -2: "LP_ESHAPE", -3: "LP_EALIGN", -4: "LP_ECAPACITY",
+          -5: "LP_EDTYPE", -6: "LP_ECUDA", -7: "LP_ESTATE"}
+
+# Every symbol include/lp_epilogue.h declares.
+EXPORTS = ("lp_plan_create", "lp_plan_destroy", "lp_plan_scratch_bytes", "lp_bind", "lp_run", "lp_run_host",
+           "lp_run_host_bytes", "lp_debug_tiles_read", "lp_debug_poison_scratch", "lp_plan_tiles_per_row",
+           "lp_strerror", "lp_last_cuda_error")
+
+
+class PlanDesc(ctypes.Structure):
+    _fields_ = [
+        ("max_rows", ctypes.c_int32),
+        ("max_groups", ctypes.c_int32),
+        ("k_max", ctypes.c_int32),
+        ("V", ctypes.c_int64),
+        ("V_padded", ctypes.c_int64),
+        ("dtype", ctypes.c_int32),
+        ("k_alt_max", ctypes.c_int32),
+        ("max_ids", ctypes.c_int32),
+        ("device", ctypes.c_int32),
+        ("flags", ctypes.c_uint32),
+        ("timeout_ns", ctypes.c_int64),
+    ]
+
+
+class IO(ctypes.Structure):
+    _fields_ = [
+        ("logits", ctypes.c_void_p),
+        ("group_indptr", ctypes.c_void_p),
+        ("draft_tokens", ctypes.c_void_p),
+        ("sampled_tokens", ctypes.c_void_p),
+        ("requested", ctypes.c_void_p),
+        ("top_k", ctypes.c_void_p),
+        ("token_ids", ctypes.c_void_p),
+        ("id_counts", ctypes.c_void_p),
+        ("records", ctypes.c_void_p),
+        ("accepted", ctypes.c_void_p),
+        ("emitted_tokens", ctypes.c_void_p),
+        ("lse_out", ctypes.c_void_p),
+        ("status", ctypes.c_void_p),
+        ("rows", ctypes.c_int32),
+        ("groups", ctypes.c_int32),
+    ]
+
+
+_lib = None
+
+
+class LPError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        msg = lib().lp_strerror(code).decode() if _lib is not None else ""
+        cuda = f" (cudaError {lib().lp_last_cuda_error()})" if code == -6 else ""
+        super().__init__(f"{what}: {ERRORS.get(code, code)}: {msg}{cuda}")
+        self.code = code
+
+
+def lib() -> ctypes.CDLL:
+    """Loads the in-tree library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with logprob_epilogue_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        P = ctypes.c_void_p
+        L.lp_plan_create.argtypes = [ctypes.POINTER(P), ctypes.POINTER(PlanDesc)]
+        L.lp_plan_destroy.argtypes = [P]
+        L.lp_plan_scratch_bytes.argtypes = [ctypes.POINTER(PlanDesc)]
+        L.lp_plan_scratch_bytes.restype = ctypes.c_size_t
+        L.lp_bind.argtypes = [P, ctypes.POINTER(IO)]
+        L.lp_run.argtypes = [P, P]
+        L.lp_run_host.argtypes = [P, ctypes.POINTER(IO), P]
+        L.lp_run_host_bytes.argtypes = [P, ctypes.POINTER(IO), ctypes.POINTER(ctypes.c_int64),
+                                        ctypes.POINTER(ctypes.c_int64)]
+        L.lp_debug_tiles_read.argtypes = [P, P, ctypes.c_int32]
+        L.lp_debug_poison_scratch.argtypes = [P, P]
+        L.lp_plan_tiles_per_row.argtypes = [P]
+        L.lp_strerror.argtypes = [ctypes.c_int]
+        L.lp_strerror.restype = ctypes.c_char_p
+        L.lp_last_cuda_error.argtypes = []
+        for name in EXPORTS:
+            if name not in ("lp_plan_scratch_bytes", "lp_strerror"):
+                getattr(L, name).restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != 0:
+        raise LPError(rc, what)
+
+
+def make_desc(*, max_rows, max_groups, k_max, V, V_padded=None, dtype="bf16", k_alt_max=20, max_ids=128,
+              device=0, host_staging=False, timeout_ns=0, debug_force_timeout=False) -> PlanDesc:
+    flags = (PLAN_HOST_STAGING if host_staging else 0) | (PLAN_DEBUG_FORCE_TIMEOUT if debug_force_timeout else 0)
+    return PlanDesc(int(max_rows), int(max_groups), int(k_max), int(V), int(V if V_padded is None else V_padded),
+                    LP_BF16 if dtype == "bf16" else (LP_F32 if dtype == "f32" else 99), int(k_alt_max),
+                    int(max_ids), int(device), flags, int(timeout_ns))
+
+
+def scratch_bytes(**desc_kw) -> int:
+    d = make_desc(**desc_kw)
+    return int(lib().lp_plan_scratch_bytes(ctypes.byref(d)))
+
+
+_IO_NAMES = ("logits", "group_indptr", "draft_tokens", "sampled_tokens", "requested", "top_k", "token_ids",
+             "id_counts", "records", "accepted", "emitted_tokens", "lse_out", "status")
+
+
+class Plan:
+    """One epilogue plan (device scratch allocated once at creation)."""
+
+    def __init__(self, **desc_kw):
+        self.desc = make_desc(**desc_kw)
+        self.dtype = desc_kw.get("dtype", "bf16")
+        self.device = int(desc_kw.get("device", 0))
+        h = ctypes.c_void_p()
+        _check(lib().lp_plan_create(ctypes.byref(h), ctypes.byref(self.desc)), "lp_plan_create")
+        self._h = h
+        self._keep = None
+        self.rows = 0
+        self.groups = 0
+
+    @property
+    def tiles_per_row(self) -> int:
+        return int(lib().lp_plan_tiles_per_row(self._h))
+
+    def close(self) -> None:
+        if getattr(self, "_h", None) is not None and self._h.value:
+            _check(lib().lp_plan_destroy(self._h), "lp_plan_destroy")
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def _io(self, tensors: dict, rows: int, groups: int, ptr) -> IO:
+        vals = [ptr(tensors.get(n)) for n in _IO_NAMES]
+        return IO(*vals, int(rows), int(groups))
+
+    def bind(self, *, logits, group_indptr, draft_tokens, sampled_tokens, requested, top_k, token_ids,
+             id_counts, records, accepted, emitted_tokens, status, lse_out=None) -> None:
+        """Binds CUDA tensors (contiguous; int32 except logits, lse_out and status)."""
+        import torch
+        t = dict(logits=logits, group_indptr=group_indptr, draft_tokens=draft_tokens,
+                 sampled_tokens=sampled_tokens, requested=requested, top_k=top_k, token_ids=token_ids,
+                 id_counts=id_counts, records=records, accepted=accepted, emitted_tokens=emitted_tokens,
+                 status=status, lse_out=lse_out)
+        want_logit = torch.bfloat16 if self.dtype == "bf16" else torch.float32
+        for name, x in t.items():
+            if x is None:
+                continue
+            if not isinstance(x, torch.Tensor) or not x.is_cuda or x.device.index != self.device:
+                raise ValueError(f"{name}: expected a CUDA tensor on device {self.device}")
+            if not x.is_contiguous():
+                raise ValueError(f"{name}: must be contiguous")
+            if name == "logits":
+                if x.dtype != want_logit or x.dim() != 2 or x.shape[1] != self.desc.V_padded:
+                    raise ValueError(f"logits: expected {want_logit} [rows, {self.desc.V_padded}]")
+            elif name == "lse_out":
+                if x.dtype != torch.float32:
+                    raise ValueError("lse_out: expected float32")
+            elif name == "status":
+                if x.element_size() != 4 or x.numel() < 1:
+                    raise ValueError("status: expected one 32-bit word")
+            elif x.dtype != torch.int32:
+                raise ValueError(f"{name}: expected int32")
+        rows = int(logits.shape[0])
+        groups = int(group_indptr.numel()) - 1
+        if records.numel() < rows * RECORD_WORDS or emitted_tokens.numel() < rows or draft_tokens.numel() < rows:
+            raise ValueError("records / emitted_tokens / draft_tokens smaller than rows")
+        for name in ("sampled_tokens", "requested", "top_k", "id_counts", "accepted"):
+            if t[name].numel() < groups:
+                raise ValueError(f"{name} smaller than groups")
+        if token_ids.numel() < groups * MAX_IDS:
+            raise ValueError("token_ids smaller than groups * 128")
+        if lse_out is not None and lse_out.numel() < rows:
+            raise ValueError("lse_out smaller than rows")
+        io = self._io(t, rows, groups, lambda x: None if x is None else x.data_ptr())
+        _check(lib().lp_bind(self._h, ctypes.byref(io)), "lp_bind")
+        self._keep = t
+        self.rows, self.groups = rows, groups
+
+    def run(self, stream=None) -> None:
+        """Enqueues the epilogue on ``stream`` (default: torch's current stream)."""
+        import torch
+        if stream is None:
+            stream = torch.cuda.current_stream(self.device)
+        handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+        _check(lib().lp_run(self._h, ctypes.c_void_p(handle)), "lp_run")
+
+    def host_io(self, arrays: dict) -> IO:
+        rows = int(arrays["logits"].shape[0])
+        groups = int(np.asarray(arrays["group_indptr"]).size) - 1
+
+        def ptr(a):
+            if a is None:
+                return None
+            if hasattr(a, "data_ptr"):
+                return a.data_ptr()
+            return a.ctypes.data
+        return self._io(arrays, rows, groups, ptr)
+
+    def run_host(self, arrays: dict, stream=None) -> None:
+        """Runs over host arrays (numpy or pinned CPU tensors); outputs land in the
+        output arrays once ``stream`` is synchronised."""
+        import torch
+        io = self.host_io(arrays)
+        if stream is None:
+            stream = torch.cuda.current_stream(self.device)
+        handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+        self._keep_host = (arrays, io)
+        _check(lib().lp_run_host(self._h, ctypes.byref(io), ctypes.c_void_p(handle)), "lp_run_host")
+
+    def host_bytes(self, arrays: dict):
+        io = self.host_io(arrays)
+        h2d, d2h = ctypes.c_int64(), ctypes.c_int64()
+        _check(lib().lp_run_host_bytes(self._h, ctypes.byref(io), ctypes.byref(h2d), ctypes.byref(d2h)),
+               "lp_run_host_bytes")
+        return int(h2d.value), int(d2h.value)
+
+    def tiles_read(self, rows: int | None = None) -> np.ndarray:
+        """Tiles the last run read per row (synchronises the last stream)."""
+        rows = self.rows if rows is None else rows
+        out = np.zeros(max(rows, 1), np.int32)
+        _check(lib().lp_debug_tiles_read(self._h, out.ctypes.data, int(rows)), "lp_debug_tiles_read")
+        return out[:rows]
+
+    def poison_scratch(self, stream=None) -> None:
+        import torch
+        if stream is None:
+            stream = torch.cuda.current_stream(self.device)
+        _check(lib().lp_debug_poison_scratch(self._h, ctypes.c_void_p(stream.cuda_stream)), "lp_debug_poison_scratch")

@@ -1,0 +1,435 @@
+// lp_plan.cu -- host side of the C ABI (plan / bind / run).
+//
+// The plan owns one device allocation holding the run's control block, work
+// queue, per-row counters, group descriptors and per-tile partial results, sized
+// once from the plan descriptor.  lp_run only enqueues the two kernels; nothing
+// is allocated or synchronised on the hot path.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <new>
+
+#include "lp_epilogue.h"
+#include "lp_internal.h"
+
+struct lp_plan_s {
+    lp_plan_desc d;
+    int elt;
+    int T;
+    lp::LaunchCfg cfg;
+    unsigned char* scratch;
+    size_t scratch_bytes;
+    lp::Ctrl* ctrl;
+    int* queue;
+    int* ticket;
+    int* done;
+    int4* gdesc;
+    float2* part_ms;
+    unsigned long long* part_keys;
+    size_t part_ms_bytes, part_keys_bytes;
+    bool bound;
+    lp_io io;
+    // optional host staging (LP_PLAN_HOST_STAGING)
+    unsigned char* staging;
+    size_t staging_bytes;
+    lp_io stage_io;
+    cudaStream_t last_stream;
+};
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+constexpr size_t kAlign = 256;
+constexpr int64_t kDefaultTimeoutNs = 1000000000LL;  // 1 s
+
+size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
+
+int cuda_fail(cudaError_t e) {
+    g_last_cuda_error = (int)e;
+    return LP_ECUDA;
+}
+
+int elt_of(int dtype) { return dtype == LP_BF16 ? 2 : (dtype == LP_F32 ? 4 : 0); }
+
+int check_desc(const lp_plan_desc* d) {
+    if (!d) return LP_EINVAL;
+    if (elt_of(d->dtype) == 0) return LP_EDTYPE;
+    if (d->max_rows < 1 || d->max_groups < 1 || d->V < 1 || d->V_padded < d->V) return LP_ESHAPE;
+    if (d->V > (int64_t)0x7FFFFFFF - lp::kTileElems) return LP_ESHAPE;
+    if (d->k_max < 0 || d->k_max > LP_MAX_DRAFTS) return LP_ECAPACITY;
+    if (d->k_alt_max < 0 || d->k_alt_max > LP_MAX_K_ALT) return LP_ECAPACITY;
+    if (d->max_ids < 0 || d->max_ids > LP_MAX_IDS) return LP_ECAPACITY;
+    if (d->max_groups > (1 << 26)) return LP_ECAPACITY;
+    if ((d->V_padded * elt_of(d->dtype)) % 16 != 0) return LP_EALIGN;
+    if (d->timeout_ns < 0) return LP_EINVAL;
+    return LP_OK;
+}
+
+struct Layout {
+    size_t ctrl, queue, ticket, done, gdesc, part_ms, part_keys, total;
+    size_t part_ms_bytes, part_keys_bytes;
+};
+
+Layout layout_of(const lp_plan_desc* d) {
+    Layout L{};
+    const size_t rows = (size_t)d->max_rows;
+    const size_t T = (size_t)((d->V + lp::kTileElems - 1) / lp::kTileElems);
+    size_t off = 0;
+    L.ctrl = off;
+    off = align_up(off + sizeof(lp::Ctrl));
+    L.queue = off;
+    off = align_up(off + rows * sizeof(int));
+    L.ticket = off;
+    off = align_up(off + rows * sizeof(int));
+    L.done = off;
+    off = align_up(off + rows * sizeof(int));
+    L.gdesc = off;
+    off = align_up(off + (size_t)d->max_groups * sizeof(int4));
+    L.part_ms = off;
+    L.part_ms_bytes = rows * T * sizeof(float2);
+    off = align_up(off + L.part_ms_bytes);
+    L.part_keys = off;
+    L.part_keys_bytes = rows * T * lp::kKeysPerTile * sizeof(unsigned long long);
+    off = align_up(off + L.part_keys_bytes);
+    L.total = off;
+    return L;
+}
+
+struct StageLayout {
+    size_t logits, indptr, drafts, sampled, requested, top_k, token_ids, id_counts;
+    size_t records, accepted, emitted, lse, status, total;
+};
+
+StageLayout stage_layout_of(const lp_plan_desc* d) {
+    StageLayout S{};
+    const size_t rows = (size_t)d->max_rows, G = (size_t)d->max_groups;
+    size_t off = 0;
+    S.logits = off;
+    off = align_up(off + rows * (size_t)d->V_padded * (size_t)elt_of(d->dtype));
+    S.indptr = off;
+    off = align_up(off + (G + 1) * 4);
+    S.drafts = off;
+    off = align_up(off + rows * 4);
+    S.sampled = off;
+    off = align_up(off + G * 4);
+    S.requested = off;
+    off = align_up(off + G * 4);
+    S.top_k = off;
+    off = align_up(off + G * 4);
+    S.token_ids = off;
+    off = align_up(off + G * LP_MAX_IDS * 4);
+    S.id_counts = off;
+    off = align_up(off + G * 4);
+    S.records = off;
+    off = align_up(off + rows * LP_RECORD_WORDS * 4);
+    S.accepted = off;
+    off = align_up(off + G * 4);
+    S.emitted = off;
+    off = align_up(off + rows * 4);
+    S.lse = off;
+    off = align_up(off + rows * 4);
+    S.status = off;
+    off = align_up(off + 4);
+    S.total = off;
+    return S;
+}
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+int check_io(const lp_plan_s* plan, const lp_io* io) {
+    if (!io) return LP_EINVAL;
+    if (io->rows < 0 || io->groups < 0) return LP_ESHAPE;
+    if (io->rows > plan->d.max_rows || io->groups > plan->d.max_groups) return LP_ESHAPE;
+    if (!io->logits || !io->group_indptr || !io->draft_tokens || !io->sampled_tokens || !io->requested ||
+        !io->top_k || !io->token_ids || !io->id_counts || !io->records || !io->accepted ||
+        !io->emitted_tokens || !io->status)
+        return LP_EINVAL;
+    if (!aligned(io->logits, 16)) return LP_EALIGN;
+    const void* i32s[] = {io->group_indptr, io->draft_tokens, io->sampled_tokens, io->requested, io->top_k,
+                          io->token_ids,    io->id_counts,    io->records,        io->accepted,  io->emitted_tokens,
+                          io->status};
+    for (const void* q : i32s)
+        if (!aligned(q, 4)) return LP_EALIGN;
+    if (io->lse_out && !aligned(io->lse_out, 4)) return LP_EALIGN;
+    return LP_OK;
+}
+
+lp::Params make_params(const lp_plan_s* plan, const lp_io& io) {
+    lp::Params p{};
+    p.logits = io.logits;
+    p.V = plan->d.V;
+    p.Vp = plan->d.V_padded;
+    p.rows = io.rows;
+    p.G = io.groups;
+    p.T = plan->T;
+    p.k_max = plan->d.k_max;
+    p.k_alt_max = plan->d.k_alt_max;
+    p.max_ids = plan->d.max_ids;
+    p.indptr = io.group_indptr;
+    p.drafts = io.draft_tokens;
+    p.sampled = io.sampled_tokens;
+    p.requested = io.requested;
+    p.top_k = io.top_k;
+    p.token_ids = io.token_ids;
+    p.id_counts = io.id_counts;
+    p.records = io.records;
+    p.accepted = io.accepted;
+    p.emitted = io.emitted_tokens;
+    p.lse_out = io.lse_out;
+    p.status = io.status;
+    p.ctrl = plan->ctrl;
+    p.queue = plan->queue;
+    p.ticket = plan->ticket;
+    p.done = plan->done;
+    p.gdesc = plan->gdesc;
+    p.part_ms = plan->part_ms;
+    p.part_keys = plan->part_keys;
+    p.timeout_ns = (unsigned long long)(plan->d.timeout_ns > 0 ? plan->d.timeout_ns : kDefaultTimeoutNs);
+    p.debug_flags = plan->d.flags & LP_PLAN_DEBUG_FORCE_TIMEOUT;
+    return p;
+}
+
+// Makes the plan's device current for the scope; restores the caller's.
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = true;
+    explicit DeviceGuard(int dev) {
+        if (cudaGetDevice(&prev) != cudaSuccess) {
+            ok = false;
+            return;
+        }
+        if (prev != dev && cudaSetDevice(dev) != cudaSuccess) ok = false;
+    }
+    ~DeviceGuard() {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+}  // namespace
+
+extern "C" {
+
+size_t lp_plan_scratch_bytes(const lp_plan_desc* desc) {
+    if (check_desc(desc) != LP_OK) return 0;
+    size_t total = layout_of(desc).total;
+    if (desc->flags & LP_PLAN_HOST_STAGING) total += stage_layout_of(desc).total;
+    return total;
+}
+
+int lp_plan_create(lp_plan_t* out, const lp_plan_desc* desc) {
+    if (!out) return LP_EINVAL;
+    *out = nullptr;
+    int rc = check_desc(desc);
+    if (rc != LP_OK) return rc;
+    DeviceGuard guard(desc->device);
+    if (!guard.ok) return cuda_fail(cudaGetLastError());
+    lp_plan_s* plan = new (std::nothrow) lp_plan_s();
+    if (!plan) return LP_EINVAL;
+    plan->d = *desc;
+    plan->elt = elt_of(desc->dtype);
+    plan->T = (int)((desc->V + lp::kTileElems - 1) / lp::kTileElems);
+    cudaError_t e = lp::query_launch_cfg(desc->dtype, &plan->cfg);
+    if (e != cudaSuccess) {
+        delete plan;
+        return cuda_fail(e);
+    }
+    const Layout L = layout_of(desc);
+    e = cudaMalloc(&plan->scratch, L.total);
+    if (e != cudaSuccess) {
+        delete plan;
+        return cuda_fail(e);
+    }
+    plan->scratch_bytes = L.total;
+    plan->ctrl = reinterpret_cast<lp::Ctrl*>(plan->scratch + L.ctrl);
+    plan->queue = reinterpret_cast<int*>(plan->scratch + L.queue);
+    plan->ticket = reinterpret_cast<int*>(plan->scratch + L.ticket);
+    plan->done = reinterpret_cast<int*>(plan->scratch + L.done);
+    plan->gdesc = reinterpret_cast<int4*>(plan->scratch + L.gdesc);
+    plan->part_ms = reinterpret_cast<float2*>(plan->scratch + L.part_ms);
+    plan->part_keys = reinterpret_cast<unsigned long long*>(plan->scratch + L.part_keys);
+    plan->part_ms_bytes = L.part_ms_bytes;
+    plan->part_keys_bytes = L.part_keys_bytes;
+    e = cudaMemset(plan->scratch, 0, L.part_ms);  // control block, queue, counters, descriptors
+    if (e == cudaSuccess && (desc->flags & LP_PLAN_HOST_STAGING)) {
+        const StageLayout S = stage_layout_of(desc);
+        e = cudaMalloc(&plan->staging, S.total);
+        if (e == cudaSuccess) {
+            plan->staging_bytes = S.total;
+            lp_io& s = plan->stage_io;
+            s.logits = plan->staging + S.logits;
+            s.group_indptr = reinterpret_cast<const int32_t*>(plan->staging + S.indptr);
+            s.draft_tokens = reinterpret_cast<const int32_t*>(plan->staging + S.drafts);
+            s.sampled_tokens = reinterpret_cast<const int32_t*>(plan->staging + S.sampled);
+            s.requested = reinterpret_cast<const int32_t*>(plan->staging + S.requested);
+            s.top_k = reinterpret_cast<const int32_t*>(plan->staging + S.top_k);
+            s.token_ids = reinterpret_cast<const int32_t*>(plan->staging + S.token_ids);
+            s.id_counts = reinterpret_cast<const int32_t*>(plan->staging + S.id_counts);
+            s.records = reinterpret_cast<int32_t*>(plan->staging + S.records);
+            s.accepted = reinterpret_cast<int32_t*>(plan->staging + S.accepted);
+            s.emitted_tokens = reinterpret_cast<int32_t*>(plan->staging + S.emitted);
+            s.lse_out = reinterpret_cast<float*>(plan->staging + S.lse);
+            s.status = reinterpret_cast<uint32_t*>(plan->staging + S.status);
+        }
+    }
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        if (plan->staging) cudaFree(plan->staging);
+        cudaFree(plan->scratch);
+        delete plan;
+        return cuda_fail(e);
+    }
+    *out = plan;
+    return LP_OK;
+}
+
+int lp_plan_destroy(lp_plan_t plan) {
+    if (!plan) return LP_EINVAL;
+    DeviceGuard guard(plan->d.device);
+    cudaError_t e = cudaSuccess;
+    if (plan->staging) e = cudaFree(plan->staging);
+    cudaError_t e2 = cudaFree(plan->scratch);
+    delete plan;
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (e2 != cudaSuccess) return cuda_fail(e2);
+    return LP_OK;
+}
+
+int lp_bind(lp_plan_t plan, const lp_io* io) {
+    if (!plan) return LP_EINVAL;
+    const int rc = check_io(plan, io);
+    if (rc != LP_OK) return rc;
+    plan->io = *io;
+    plan->bound = true;
+    return LP_OK;
+}
+
+int lp_run(lp_plan_t plan, void* stream) {
+    if (!plan) return LP_EINVAL;
+    if (!plan->bound) return LP_ESTATE;
+    DeviceGuard guard(plan->d.device);
+    if (!guard.ok) return cuda_fail(cudaGetLastError());
+    const lp::Params p = make_params(plan, plan->io);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const cudaError_t e = lp::launch_epilogue(p, plan->d.dtype, plan->cfg, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    plan->last_stream = s;
+    return LP_OK;
+}
+
+int lp_run_host_bytes(lp_plan_t plan, const lp_io* io, int64_t* h2d, int64_t* d2h) {
+    if (!plan || !io || !h2d || !d2h) return LP_EINVAL;
+    const int64_t rows = io->rows, G = io->groups;
+    *h2d = rows * plan->d.V_padded * plan->elt + (G + 1) * 4 + rows * 4 + G * 4 * 4 + G * LP_MAX_IDS * 4 +
+           rows * LP_RECORD_WORDS * 4 + G * 4 + rows * 4 + (io->lse_out ? rows * 4 : 0);
+    *d2h = rows * LP_RECORD_WORDS * 4 + G * 4 + rows * 4 + (io->lse_out ? rows * 4 : 0) + 4;
+    return LP_OK;
+}
+
+int lp_run_host(lp_plan_t plan, const lp_io* h, void* stream) {
+    if (!plan) return LP_EINVAL;
+    if (!plan->staging) return LP_ESTATE;
+    int rc = check_io(plan, h);
+    if (rc != LP_OK && rc != LP_EALIGN) return rc;  // host buffers need no device alignment
+    DeviceGuard guard(plan->d.device);
+    if (!guard.ok) return cuda_fail(cudaGetLastError());
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const lp_io& d = plan->stage_io;
+    const size_t rows = (size_t)h->rows, G = (size_t)h->groups;
+    const cudaMemcpyKind H2D = cudaMemcpyHostToDevice, D2H = cudaMemcpyDeviceToHost;
+    struct Cp {
+        void* dst;
+        const void* src;
+        size_t n;
+        cudaMemcpyKind k;
+    };
+    const Cp in[] = {
+        {(void*)d.logits, h->logits, rows * (size_t)plan->d.V_padded * plan->elt, H2D},
+        {(void*)d.group_indptr, h->group_indptr, (G + 1) * 4, H2D},
+        {(void*)d.draft_tokens, h->draft_tokens, rows * 4, H2D},
+        {(void*)d.sampled_tokens, h->sampled_tokens, G * 4, H2D},
+        {(void*)d.requested, h->requested, G * 4, H2D},
+        {(void*)d.top_k, h->top_k, G * 4, H2D},
+        {(void*)d.token_ids, h->token_ids, G * LP_MAX_IDS * 4, H2D},
+        {(void*)d.id_counts, h->id_counts, G * 4, H2D},
+    };
+    // outputs are staged in too, so rows the run does not write keep the caller's contents
+    const Cp keep[] = {
+        {d.records, h->records, rows * LP_RECORD_WORDS * 4, H2D},
+        {d.accepted, h->accepted, G * 4, H2D},
+        {d.emitted_tokens, h->emitted_tokens, rows * 4, H2D},
+        {d.lse_out, h->lse_out, h->lse_out ? rows * 4 : 0, H2D},
+    };
+    for (const Cp& c : keep) {
+        if (c.n == 0) continue;
+        const cudaError_t e = cudaMemcpyAsync(c.dst, c.src, c.n, c.k, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    for (const Cp& c : in) {
+        if (c.n == 0) continue;
+        const cudaError_t e = cudaMemcpyAsync(c.dst, c.src, c.n, c.k, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    lp_io run_io = d;
+    run_io.rows = h->rows;
+    run_io.groups = h->groups;
+    if (!h->lse_out) run_io.lse_out = nullptr;
+    const lp::Params p = make_params(plan, run_io);
+    cudaError_t e = lp::launch_epilogue(p, plan->d.dtype, plan->cfg, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    const Cp out[] = {
+        {h->records, d.records, rows * LP_RECORD_WORDS * 4, D2H},
+        {h->accepted, d.accepted, G * 4, D2H},
+        {h->emitted_tokens, d.emitted_tokens, rows * 4, D2H},
+        {h->lse_out, d.lse_out, h->lse_out ? rows * 4 : 0, D2H},
+        {h->status, d.status, 4, D2H},
+    };
+    for (const Cp& c : out) {
+        if (c.n == 0) continue;
+        e = cudaMemcpyAsync(c.dst, c.src, c.n, c.k, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    plan->last_stream = s;
+    return LP_OK;
+}
+
+int lp_debug_tiles_read(lp_plan_t plan, int32_t* host_tiles, int32_t rows) {
+    if (!plan || !host_tiles || rows < 0 || rows > plan->d.max_rows) return LP_EINVAL;
+    DeviceGuard guard(plan->d.device);
+    cudaError_t e = cudaStreamSynchronize(plan->last_stream);
+    if (e == cudaSuccess && rows > 0) e = cudaMemcpy(host_tiles, plan->done, (size_t)rows * 4, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return LP_OK;
+}
+
+int lp_debug_poison_scratch(lp_plan_t plan, void* stream) {
+    if (!plan) return LP_EINVAL;
+    DeviceGuard guard(plan->d.device);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(plan->part_ms, 0xFF, plan->part_ms_bytes, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(plan->part_keys, 0xFF, plan->part_keys_bytes, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return LP_OK;
+}
+
+int lp_plan_tiles_per_row(lp_plan_t plan) { return plan ? plan->T : LP_EINVAL; }
+
+const char* lp_strerror(int code) {
+    switch (code) {
+        case LP_OK: return "ok";
+        case LP_EINVAL: return "invalid argument (NULL pointer or nonsensical value)";
+        case LP_ESHAPE: return "inconsistent sizes (V, V_padded, rows or groups beyond the plan)";
+        case LP_EALIGN: return "misaligned buffer (logits need 16 bytes, int32 buffers 4; V_padded*elt multiple of 16)";
+        case LP_ECAPACITY: return "request beyond the plan's limits (k_max, k_alt_max, max_ids)";
+        case LP_EDTYPE: return "unknown dtype";
+        case LP_ECUDA: return "CUDA runtime error (see lp_last_cuda_error)";
+        case LP_ESTATE: return "plan not ready (nothing bound, or no host staging)";
+        default: return "unknown error code";
+    }
+}
+
+int lp_last_cuda_error(void) { return g_last_cuda_error; }
+
+}  // extern "C"

@@ -1,0 +1,268 @@
+"""CUDA path vs the CPU oracle, element by element, through the C ABI."""
+import os
+
+import numpy as np
+import pytest
+
+import parity as PT
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+THREADS = os.cpu_count() or 8
+
+
+def _check(w, **kw):
+    gpu, plan = PT.run_gpu(w, **kw)
+    orc = PT.run_oracle(w, THREADS)
+    stats = PT.compare(w, gpu, orc)
+    assert np.array_equal(gpu["tiles_read"], PT.expected_tiles(w, orc)), "tiles read per row"
+    plan.close()
+    return gpu, orc, stats
+
+
+# ----------------------------------------------------------------- workloads
+
+SMALL = {
+    "tiny": lambda: W.tiny(),
+    "decode": lambda: W.decode(rows=16),
+    "spec": lambda: W.spec(groups=12),
+    "large": lambda: W.large(groups=12),
+    "wide": lambda: W.wide(),
+}
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_workload_small(name):
+    _, orc, stats = _check(SMALL[name]())
+    assert stats["rows_written"] > 0
+
+
+@pytest.mark.parametrize("name", ["decode", "spec", "large"])
+def test_workload_full_size(name):
+    w = W.make(name)
+    gpu, orc, stats = _check(w)
+    # the benchmark's launch configuration is the plan's default one
+    assert stats["rows_written"] > 0
+
+
+def test_tiny_hand_checked():
+    w = W.tiny()
+    gpu, _ = PT.run_gpu(w)
+    assert gpu["accepted"].tolist() == [2, 0, 0]
+    assert gpu["emitted_tokens"][:3].tolist() == [int(w.draft_tokens[0]), int(w.draft_tokens[1]),
+                                                  int(w.planted_argmax[2])]
+    assert gpu["tiles_read"].tolist() == [1, 1, 1, 0, 1, 0]
+
+
+def test_wide_tie_all_accepted():
+    w = W.wide()
+    gpu, _ = PT.run_gpu(w)
+    assert gpu["accepted"].tolist() == [3]
+    x = w.logits_f32(3)
+    tied = np.sort(np.flatnonzero(x[:w.V] == np.float32(16.0)))
+    assert gpu["records"][3][2:42:2].tolist() == tied[:20].tolist()
+
+
+# ----------------------------------------------------------------- adversarial rows
+
+def _one_group(rows, V, *, dtype="f32", Vp=None, k=None, drafts=None, top_k=20, ids=None, requested=1,
+               sampled=-1):
+    rows = np.asarray(rows, np.float32)
+    n = rows.shape[0]
+    k = n - 1 if k is None else k
+    return W.custom(rows, V, [n], dtype=dtype, Vp=Vp, drafts=drafts, top_k=[top_k],
+                    token_ids=[ids] if ids is not None else None,
+                    id_counts=[len(ids)] if ids is not None else None, requested=[requested],
+                    sampled=[sampled], k_max=max(k, 0))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_subtraction_ties_across_tiles(dtype):
+    rng = np.random.default_rng(3)
+    V = 30_000
+    x = rng.uniform(0.0, 0.01, V).astype(np.float32)
+    x[rng.integers(0, V)] = 1e4
+    w = _one_group(x[None, :], V, dtype=dtype, Vp=V + (8 if dtype == "bf16" else 0))
+    _check(w)
+
+
+def test_subtraction_ties_hidden_below_tile_top32():
+    # one tile holds many logits that collapse to the same logprob, with small ids
+    rng = np.random.default_rng(4)
+    V = 40_000
+    x = rng.normal(-30.0, 1.0, V).astype(np.float32)
+    x[0] = 2000.0
+    x[1:5000] = (rng.uniform(0, 0.003, 4999) + 1990.0).astype(np.float32)
+    _check(_one_group(x[None, :], V))
+
+
+def test_exact_tie_split_across_tiles():
+    rng = np.random.default_rng(5)
+    V = 100_000
+    x = rng.normal(0, 1, V).astype(np.float32)
+    ids = rng.choice(V, 64, replace=False)
+    x[ids] = 16.0
+    _check(_one_group(x[None, :], V, dtype="bf16"))
+
+
+def test_tie_straddles_cutoff():
+    rng = np.random.default_rng(6)
+    V = 50_000
+    x = rng.normal(0, 1, V).astype(np.float32)
+    top = rng.choice(V, 40, replace=False)
+    x[top[:10]] = np.arange(20, 30, dtype=np.float32)
+    x[top[10:]] = 7.0
+    _check(_one_group(x[None, :], V))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_constant_row(dtype):
+    V = 30_000
+    x = np.zeros((1, V), np.float32)
+    _check(_one_group(x, V, dtype=dtype, Vp=V + (8 if dtype == "bf16" else 0)))
+
+
+def test_signed_zero_maximum():
+    V = 9000
+    x = np.full(V, -3.0, np.float32)
+    x[8500] = -0.0
+    x[8200] = 0.0
+    x[100] = -0.0
+    w = _one_group(np.stack([x, x]), V, drafts=[100, -1])
+    gpu, _, _ = _check(w)
+    assert gpu["emitted_tokens"].tolist() == [100, 100]
+
+
+@pytest.mark.parametrize("V,Vp,dtype", [(10_001, 10_008, "bf16"), (10_001, 10_004, "f32"), (7, 8, "bf16"),
+                                        (1, 4, "f32"), (33, 40, "bf16"), (8192, 8192, "f32"),
+                                        (8193, 8200, "bf16"), (16_385, 16_388, "f32")])
+def test_ragged_vocabularies(V, Vp, dtype):
+    rng = np.random.default_rng(V)
+    rows = rng.normal(0, 2, (3, V)).astype(np.float32)
+    rows[:, rng.integers(0, V)] = 20.0
+    w = W.custom(rows, V, [2, 1], dtype=dtype, Vp=Vp, drafts=[int(np.argmax(rows[0])), -1, -1],
+                 top_k=[20, 5], k_max=1)
+    _check(w)
+
+
+@pytest.mark.parametrize("a", [0, 1, 7, 15])
+def test_acceptance_prefixes_k15(a):
+    rng = np.random.default_rng(100 + a)
+    k, V = 15, 20_000
+    rows = rng.normal(0, 1, (k + 1, V)).astype(np.float32)
+    am = rng.integers(0, V, k + 1)
+    rows[np.arange(k + 1), am] = 8.0
+    drafts = np.full(k + 1, -1, np.int32)
+    drafts[:k] = am[:k]
+    if a < k:
+        drafts[a] = (am[a] + 1) % V
+    w = _one_group(rows, V, drafts=drafts, top_k=3)
+    gpu, _, _ = _check(w)
+    assert int(gpu["accepted"][0]) == a
+
+
+def test_explicit_ids_edges_and_errors():
+    rng = np.random.default_rng(8)
+    V = 12_345
+    rows = rng.normal(0, 2, (2, V)).astype(np.float32)
+    ids = [0, V - 1, 5, -1, V, 77]
+    w = W.custom(rows, V, [1, 1], dtype="bf16", Vp=12_352, top_k=[0, 25],
+                 token_ids=[ids, None], id_counts=[len(ids), 0], k_max=0)
+    gpu, orc, _ = _check(w)
+    assert gpu["status"] == (0x1 | 0x4)
+
+
+def test_flags_and_unread_groups():
+    rng = np.random.default_rng(9)
+    V = 5000
+    rows = rng.normal(0, 1, (6, V)).astype(np.float32)
+    # g0 unflagged k=0 with a token (never read), g1 unflagged k=0 argmax (read, no record),
+    # g2 flagged K=0 (lse only), g3 unflagged verify group k=2, g4 flagged with a bad token
+    w = W.custom(rows, V, [1, 1, 1, 2, 1], sampled=[17, -1, 3, -1, V + 5], requested=[0, 0, 1, 0, 1],
+                 top_k=[20, 20, 0, 20, 20], drafts=[-1, -1, -1, int(np.argmax(rows[3])), -1, -1], k_max=1)
+    gpu, orc, _ = _check(w)
+    assert gpu["tiles_read"][0] == 0
+    assert gpu["status"] == 0x2
+
+
+def test_poisoned_scratch_and_repeated_runs():
+    w = W.spec(groups=6)
+    gpu1, plan = PT.run_gpu(w)
+    gpu2, _ = PT.run_gpu(w, plan=plan, poison=True, runs=3)
+    for key in ("records", "accepted", "emitted_tokens", "lse", "tiles_read"):
+        assert np.array_equal(gpu1[key], gpu2[key]), key
+    plan.close()
+
+
+def test_malformed_groups_write_nothing():
+    x = np.zeros((3, 100), np.float32)
+    w = W.custom(x, 100, [2, 1], k_max=0)   # a group of 2 rows with k_max 0
+    gpu, _ = PT.run_gpu(w)
+    assert gpu["status"] == 0x8
+    assert (gpu["emitted_tokens"] == -7).all() and (gpu["records"] == PT.SENTINEL).all()
+    assert (gpu["tiles_read"] == 0).all()
+
+
+def test_no_groups():
+    x = np.zeros((2, 64), np.float32)
+    w = W.custom(x, 64, [], k_max=0)
+    gpu, _ = PT.run_gpu(w)
+    assert gpu["status"] == 0 and (gpu["tiles_read"] == 0).all()
+
+
+def test_forced_timeout_is_reported_and_context_survives():
+    w = W.spec(groups=2, V=20_000, Vp=20_000)
+    plan = PT.make_plan(w, debug_force_timeout=True, timeout_ns=2_000_000)
+    gpu, _ = PT.run_gpu(w, plan=plan)
+    assert gpu["status"] & 0x10
+    assert (gpu["tiles_read"] == 0).all()
+    plan.close()
+    _check(w)
+
+
+def test_cuda_graph_replay():
+    import torch
+    w = W.spec(groups=8)
+    ref, plan = PT.run_gpu(w)
+    d = PT.to_device(w)
+    dev = torch.device("cuda", 0)
+    out = dict(records=torch.full((w.rows, 258), PT.SENTINEL, dtype=torch.int32, device=dev),
+               accepted=torch.zeros(w.groups, dtype=torch.int32, device=dev),
+               emitted_tokens=torch.zeros(w.rows, dtype=torch.int32, device=dev),
+               lse_out=torch.full((w.rows,), PT.LSE_SENTINEL, dtype=torch.float32, device=dev),
+               status=torch.zeros(1, dtype=torch.int32, device=dev))
+    plan.bind(**d, **out)
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        plan.run(s)          # warm-up outside capture
+        s.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            plan.run(s)
+    for _ in range(3):
+        out["records"].fill_(PT.SENTINEL)
+        g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(out["records"].cpu().numpy(), ref["records"])
+    assert np.array_equal(out["emitted_tokens"].cpu().numpy(), ref["emitted_tokens"])
+    plan.close()
+
+
+def test_host_buffers_match_device_run():
+    import torch
+    w = W.spec(groups=4)
+    ref, _ = PT.run_gpu(w)
+    plan = PT.make_plan(w, host_staging=True)
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+    arrays = dict(logits=pin(w.logits), group_indptr=pin(w.group_indptr), draft_tokens=pin(w.draft_tokens),
+                  sampled_tokens=pin(w.sampled_tokens), requested=pin(w.requested), top_k=pin(w.top_k),
+                  token_ids=pin(w.token_ids), id_counts=pin(w.id_counts),
+                  records=pin(np.full((w.rows, 258), PT.SENTINEL, np.int32)),
+                  accepted=pin(np.zeros(w.groups, np.int32)), emitted_tokens=pin(np.zeros(w.rows, np.int32)),
+                  lse_out=pin(np.full(w.rows, PT.LSE_SENTINEL, np.float32)), status=pin(np.zeros(1, np.int32)))
+    plan.run_host(arrays)
+    torch.cuda.synchronize()
+    assert np.array_equal(arrays["records"].numpy(), ref["records"])
+    assert np.array_equal(arrays["accepted"].numpy(), ref["accepted"])
+    assert np.array_equal(arrays["emitted_tokens"].numpy(), ref["emitted_tokens"])
+    plan.close()
