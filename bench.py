@@ -210,6 +210,27 @@ def run_reference(args, world, rank, local, pg):
     return 0
 
 
+class Flusher:
+    """Evicts the inputs from L2 before a timed step: writes a 256 MiB buffer, then
+    (mode "write+read", the default) reads another 256 MiB buffer so that the
+    dirty lines of that write are written back before the step, not during it."""
+
+    MODE = os.environ.get("LP_BENCH_FLUSH", "write+read")
+
+    def __init__(self, dev):
+        import torch
+        self.buf = torch.empty(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+        self.clean = torch.ones(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+
+    def __call__(self, i):
+        import torch
+        if self.MODE == "none":
+            return
+        self.buf.fill_(i)
+        if self.MODE == "write+read":
+            self.last = self.clean.sum()
+
+
 def bench_device(w: W.Workload, steps: int, warmup: int, device: int, staging: bool = True):
     """Times lp_run on device-resident inputs; returns per-step durations (s) and outputs."""
     import torch
@@ -232,10 +253,10 @@ def bench_device(w: W.Workload, steps: int, warmup: int, device: int, staging: b
                 lse_out=torch.zeros(w.rows, dtype=torch.float32, device=dev),
                 status=torch.zeros(1, dtype=torch.int32, device=dev))
     plan.bind(**ins, **outs)
-    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    flush = Flusher(dev)
     stream = torch.cuda.current_stream(dev)
     for _ in range(warmup):
-        flush.fill_(1)
+        flush(1)
         plan.run(stream)
     torch.cuda.synchronize(dev)
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
@@ -312,7 +333,7 @@ def main():
     sampler.start()
     time.sleep(0.2)
     for i in range(args.steps):
-        flush.fill_(i)
+        flush(i)
         starts[i].record(stream)
         plan.run(stream)
         ends[i].record(stream)
@@ -351,7 +372,8 @@ def main():
         "dtype": "f32",
         "data": "synthetic",
         "config": {"workload": DESCRIPTIONS[args.config], "logits_dtype": w.dtype,
-                   "l2": "flushed by a 256 MiB device write before every timed step (outside the events)",
+                   "l2": f"flushed before every timed step, outside the events ({Flusher.MODE}: 256 MiB write"
+                         + (", then a 256 MiB read so its write-back completes before the step)" if Flusher.MODE == "write+read" else ")"),
                    "rows_read_per_step": ab["rows_read"], "parallelism": f"replicas x{world}"},
         "hbm_gbs": achieved_gbs,
         "rows_read_per_s": world * ab["rows_read"] / per_step,
@@ -380,7 +402,7 @@ def main():
             wn = W.make(name)
             p2, i2, o2, fl2, st2, en2, s2 = bench_device(wn, 200, 5, local, staging=False)
             for i in range(200):
-                fl2.fill_(i)
+                fl2(i)
                 st2[i].record(s2)
                 p2.run(s2)
                 en2[i].record(s2)

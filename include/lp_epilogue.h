@@ -91,6 +91,7 @@ enum {
 /* Plan flags. */
 #define LP_PLAN_HOST_STAGING 0x1u     /* also allocate device staging so lp_run_host can be used */
 #define LP_PLAN_DEBUG_FORCE_TIMEOUT 0x100u /* test hook: every bounded wait runs out (no reads) */
+#define LP_PLAN_DEBUG_TRACE 0x200u    /* record a device timeline of each run (see lp_debug_trace) */
 
 typedef struct {
     int32_t max_rows;     /* capacity: rows per run (>= 1) */
@@ -178,14 +179,24 @@ int lp_run_host_bytes(lp_plan_t plan, const lp_io* host_io, int64_t* h2d, int64_
 
 /* Debug: number of vocabulary tiles the last run read for each row (0 = the
  * row was never read), copied into host_tiles[0..rows).  Synchronises the
- * plan's last stream.  Tiles hold 8192 elements (the last one of a row fewer). */
+ * plan's last stream.  A tile is 32 KiB of logits: 16384 BF16 or 8192 FP32
+ * elements (the last tile of a row may be shorter). */
 int lp_debug_tiles_read(lp_plan_t plan, int32_t* host_tiles, int32_t rows);
 
 /* Debug: fills the plan's per-tile partial-result scratch with NaN bytes on
  * `stream` (to show that no result depends on stale scratch). */
 int lp_debug_poison_scratch(lp_plan_t plan, void* stream);
 
-/* Tiles per row for this plan (ceil(V / 8192)). */
+/* Debug: the device timeline of the last run of a plan created with
+ * LP_PLAN_DEBUG_TRACE.  *ctas and *cap receive the geometry: (ctas * 3 + 1)
+ * rings of cap events, each event two uint64 words (globaltimer ns,
+ * type << 56 | row << 24 | tile); ring (cta, role) holds counts[cta * 3 + role]
+ * events (roles: 0 producer, 1 compute, 2 merge); the last ring holds the
+ * prepare kernel's start and end.  With events == NULL only the geometry is
+ * returned.  Synchronises the plan's last stream.  LP_ESTATE without tracing. */
+int lp_debug_trace(lp_plan_t plan, uint64_t* events, uint32_t* counts, int32_t* ctas, int32_t* cap);
+
+/* Tiles per row for this plan (ceil(V / tile elements)). */
 int lp_plan_tiles_per_row(lp_plan_t plan);
 
 /* Message of an LP_E* code. */

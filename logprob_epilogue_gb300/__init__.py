@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_PKG, "liblp_epilogue.so")
 RECORD_WORDS = 258
 MAX_IDS = 128
 UNUSED_LP_BITS = 0x7FC00000
-TILE_ELEMS = 8192
+TILE_BYTES = 32768  # vocabulary tile: 16384 BF16 or 8192 FP32 logits
 
 LP_F32, LP_BF16 = 0, 1
 STATUS_BAD_ID = 0x1
@@ -29,13 +29,15 @@ STATUS_BAD_GROUP = 0x8
 STATUS_TIMEOUT = 0x10
 PLAN_HOST_STAGING = 0x1
 PLAN_DEBUG_FORCE_TIMEOUT = 0x100
+PLAN_DEBUG_TRACE = 0x200
 
 ERRORS = {0: "LP_OK", -1: "LP_EINVAL", -2: "LP_ESHAPE", -3: "LP_EALIGN", -4: "LP_ECAPACITY",
           -5: "LP_EDTYPE", -6: "LP_ECUDA", -7: "LP_ESTATE"}
 
 # Every symbol include/lp_epilogue.h declares.
 EXPORTS = ("lp_plan_create", "lp_plan_destroy", "lp_plan_scratch_bytes", "lp_bind", "lp_run", "lp_run_host",
-           "lp_run_host_bytes", "lp_debug_tiles_read", "lp_debug_poison_scratch", "lp_plan_tiles_per_row",
+           "lp_run_host_bytes", "lp_debug_tiles_read", "lp_debug_poison_scratch", "lp_debug_trace",
+           "lp_plan_tiles_per_row",
            "lp_strerror", "lp_last_cuda_error")
 
 
@@ -106,6 +108,7 @@ def lib() -> ctypes.CDLL:
         L.lp_debug_tiles_read.argtypes = [P, P, ctypes.c_int32]
         L.lp_debug_poison_scratch.argtypes = [P, P]
         L.lp_plan_tiles_per_row.argtypes = [P]
+        L.lp_debug_trace.argtypes = [P, P, P, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]
         L.lp_strerror.argtypes = [ctypes.c_int]
         L.lp_strerror.restype = ctypes.c_char_p
         L.lp_last_cuda_error.argtypes = []
@@ -122,8 +125,9 @@ def _check(rc: int, what: str) -> None:
 
 
 def make_desc(*, max_rows, max_groups, k_max, V, V_padded=None, dtype="bf16", k_alt_max=20, max_ids=128,
-              device=0, host_staging=False, timeout_ns=0, debug_force_timeout=False) -> PlanDesc:
+              device=0, host_staging=False, timeout_ns=0, debug_force_timeout=False, trace=False) -> PlanDesc:
     flags = (PLAN_HOST_STAGING if host_staging else 0) | (PLAN_DEBUG_FORCE_TIMEOUT if debug_force_timeout else 0)
+    flags |= PLAN_DEBUG_TRACE if trace else 0
     return PlanDesc(int(max_rows), int(max_groups), int(k_max), int(V), int(V if V_padded is None else V_padded),
                     LP_BF16 if dtype == "bf16" else (LP_F32 if dtype == "f32" else 99), int(k_alt_max),
                     int(max_ids), int(device), flags, int(timeout_ns))
@@ -258,6 +262,20 @@ class Plan:
         out = np.zeros(max(rows, 1), np.int32)
         _check(lib().lp_debug_tiles_read(self._h, out.ctypes.data, int(rows)), "lp_debug_tiles_read")
         return out[:rows]
+
+    def trace(self):
+        """Device timeline of the last run: (events uint64 [ctas*3+1, cap, 2], counts uint32 [ctas, 3]).
+
+        Event word 1 = type << 56 | row << 24 | tile (types: 1 kernel start, 2 claim, 3 TMA issue,
+        4 tile start, 5 tile end, 6 tile published, 7 merge start, 8 acceptance decided,
+        9 merge end, 10/11 prepare start/end, 12 producer exit)."""
+        ctas, cap = ctypes.c_int32(), ctypes.c_int32()
+        _check(lib().lp_debug_trace(self._h, None, None, ctypes.byref(ctas), ctypes.byref(cap)), "lp_debug_trace")
+        ev = np.zeros(((ctas.value * 3 + 1), cap.value, 2), np.uint64)
+        cnt = np.zeros((ctas.value, 3), np.uint32)
+        _check(lib().lp_debug_trace(self._h, ev.ctypes.data, cnt.ctypes.data, ctypes.byref(ctas), ctypes.byref(cap)),
+               "lp_debug_trace")
+        return ev, cnt
 
     def poison_scratch(self, stream=None) -> None:
         import torch

@@ -14,6 +14,8 @@ LIB = os.path.join(PKG, "liblp_epilogue.so")
 SOURCES = ["lp_plan.cu", "lp_kernels.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
+# Optional extra nvcc flags (e.g. -DLP_BF16_CTAS=2) for tuning builds.
+EXTRA = os.environ.get("LP_EXTRA_NVCC_FLAGS", "").split()
 
 
 def _nvcc() -> str:
@@ -44,7 +46,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     def compile_one(src: str) -> str:
         obj = os.path.join(objdir, src.replace(".cu", ".o"))
-        cmd = [nvcc, *ARCH, *FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+        cmd = [nvcc, *ARCH, *FLAGS, *EXTRA, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
         r = subprocess.run(cmd, capture_output=True, text=True)

@@ -6,33 +6,56 @@
 
 namespace lp {
 
-// Vocabulary tile: 8192 elements (16 KiB of BF16, 32 KiB of FP32).
-constexpr int kTileElems = 8192;
+// Vocabulary tile: 32 KiB of logits (16384 BF16 or 8192 FP32 elements).
+constexpr int kTileBytes = 32768;
+template <int ELT>
+__host__ __device__ constexpr int tile_elems() { return kTileBytes / ELT; }
+inline int tile_elems_of_dtype(int dtype) { return dtype == 1 ? kTileBytes / 2 : kTileBytes / 4; }
 constexpr int kConsumerThreads = 256;   // 8 compute warps
-constexpr int kThreads = kConsumerThreads + 32;  // + 1 producer warp
+constexpr int kThreads = kConsumerThreads + 64;  // + 1 producer warp + 1 merge warp
+constexpr int kRing = 8;                // tile results in flight between compute and merge warps
 constexpr int kKeysPerTile = 32;        // retained sort keys per tile
 constexpr int kRecordWords = 258;
 constexpr int kMaxIds = 128;
 constexpr int kCandCap = 256;           // tile candidate buffer (keys)
 
 // Pipeline stages per CTA and CTAs per SM, per element type.
+#ifndef LP_BF16_STAGES
+#define LP_BF16_STAGES 3
+#endif
+#ifndef LP_BF16_CTAS
+#define LP_BF16_CTAS 2
+#endif
+#ifndef LP_F32_STAGES
+#define LP_F32_STAGES 3
+#endif
+#ifndef LP_F32_CTAS
+#define LP_F32_CTAS 2
+#endif
 template <int kElt> struct StageCfg;
-template <> struct StageCfg<2> { static constexpr int kStages = 4; static constexpr int kMinBlocks = 3; };
-template <> struct StageCfg<4> { static constexpr int kStages = 3; static constexpr int kMinBlocks = 2; };
+template <> struct StageCfg<2> {
+    static constexpr int kStages = LP_BF16_STAGES;
+    static constexpr int kMinBlocks = LP_BF16_CTAS;
+};
+template <> struct StageCfg<4> {
+    static constexpr int kStages = LP_F32_STAGES;
+    static constexpr int kMinBlocks = LP_F32_CTAS;
+};
 
 // Row modes (what a read row needs).
-enum : int { kModeArgmax = 0, kModeLse = 1, kModeNatural = 2 };
+enum : int { kModeArgmax = 0, kModeLse = 1, kModeNatural = 2, kModeRecord = 3 };
 
-// Group descriptor built by the prepare kernel:
-//   x = first row, y = k | mode << 8 | explicit_ids << 12 | requested << 13,
-//   z = top_k (natural) or id count (explicit), w = sampled token.
+// Run control block; each hot word sits in its own 128-byte line.
 struct Ctrl {
-    unsigned int q_head;      // queue position whose row is being split into tiles
-    unsigned int q_tail;      // queue entries reserved
-    int outstanding;          // rows queued or in flight, not yet decided
+    unsigned int next_item;   // next work item (queue position * T + tile) to hand out
+    unsigned int pad0[31];
+    unsigned int q_tail;      // queue positions reserved (depth-0 rows + appended rows)
+    unsigned int pad1[31];
+    int outstanding;          // rows queued or in flight whose acceptance is not decided
+    unsigned int pad2[31];
     unsigned int abort;       // 1: malformed groups, the stream kernel does nothing
     unsigned int never;       // never written: the forced-timeout test hook waits on it
-    unsigned int pad[11];
+    unsigned int pad3[30];
 };
 
 struct Params {
@@ -57,14 +80,20 @@ struct Params {
     unsigned int* status;
     // scratch
     Ctrl* ctrl;
-    int* queue;           // [max_rows] entries g << 4 | j, -1 = not yet published
-    int* ticket;          // [max_rows] next tile to hand out
+    unsigned long long* queue;  // [max_rows] work queue (see queue_entry), all ones = not yet published
     int* done;            // [max_rows] tiles finished
-    int4* gdesc;          // [max_groups]
+    unsigned long long* row_best;   // [max_rows] best (argmax) key over the finished tiles
+    int4* gdesc;          // [max_groups] x = first row, y = k | mode << 8 | explicit << 12 |
+                          // requested << 13, z = top_k or id count, w = sampled token
     float2* part_ms;      // [max_rows * T] tile (max, exp-sum)
     unsigned long long* part_keys;  // [max_rows * T * 32] tile keys, descending
     unsigned long long timeout_ns;
     unsigned int debug_flags;
+    // optional timeline (nullptr unless the plan traces)
+    unsigned long long* trace;    // [(trace_ctas * 3 + 1) * trace_cap * 2]
+    unsigned int* trace_count;    // [trace_ctas * 3]
+    int trace_cap;
+    int trace_ctas;
 };
 
 struct LaunchCfg {

@@ -21,9 +21,9 @@ struct lp_plan_s {
     unsigned char* scratch;
     size_t scratch_bytes;
     lp::Ctrl* ctrl;
-    int* queue;
-    int* ticket;
+    unsigned long long* queue;
     int* done;
+    unsigned long long* row_best;
     int4* gdesc;
     float2* part_ms;
     unsigned long long* part_keys;
@@ -35,6 +35,10 @@ struct lp_plan_s {
     size_t staging_bytes;
     lp_io stage_io;
     cudaStream_t last_stream;
+    // optional timeline (LP_PLAN_DEBUG_TRACE)
+    unsigned long long* trace;
+    unsigned int* trace_count;
+    int trace_cap, trace_ctas;
 };
 
 namespace {
@@ -57,32 +61,33 @@ int check_desc(const lp_plan_desc* d) {
     if (!d) return LP_EINVAL;
     if (elt_of(d->dtype) == 0) return LP_EDTYPE;
     if (d->max_rows < 1 || d->max_groups < 1 || d->V < 1 || d->V_padded < d->V) return LP_ESHAPE;
-    if (d->V > (int64_t)0x7FFFFFFF - lp::kTileElems) return LP_ESHAPE;
+    if (d->V > (int64_t)0x7FFFFFFF - lp::tile_elems_of_dtype(d->dtype)) return LP_ESHAPE;
     if (d->k_max < 0 || d->k_max > LP_MAX_DRAFTS) return LP_ECAPACITY;
     if (d->k_alt_max < 0 || d->k_alt_max > LP_MAX_K_ALT) return LP_ECAPACITY;
     if (d->max_ids < 0 || d->max_ids > LP_MAX_IDS) return LP_ECAPACITY;
-    if (d->max_groups > (1 << 26)) return LP_ECAPACITY;
+    if (d->max_groups > (1 << 26) || d->max_rows >= (1 << 28)) return LP_ECAPACITY;
     if ((d->V_padded * elt_of(d->dtype)) % 16 != 0) return LP_EALIGN;
     if (d->timeout_ns < 0) return LP_EINVAL;
     return LP_OK;
 }
 
 struct Layout {
-    size_t ctrl, queue, ticket, done, gdesc, part_ms, part_keys, total;
+    size_t ctrl, queue, row_best, done, gdesc, part_ms, part_keys, total;
     size_t part_ms_bytes, part_keys_bytes;
 };
 
 Layout layout_of(const lp_plan_desc* d) {
     Layout L{};
     const size_t rows = (size_t)d->max_rows;
-    const size_t T = (size_t)((d->V + lp::kTileElems - 1) / lp::kTileElems);
+    const int64_t te = lp::tile_elems_of_dtype(d->dtype);
+    const size_t T = (size_t)((d->V + te - 1) / te);
     size_t off = 0;
     L.ctrl = off;
     off = align_up(off + sizeof(lp::Ctrl));
     L.queue = off;
-    off = align_up(off + rows * sizeof(int));
-    L.ticket = off;
-    off = align_up(off + rows * sizeof(int));
+    off = align_up(off + rows * sizeof(unsigned long long));
+    L.row_best = off;
+    off = align_up(off + rows * sizeof(unsigned long long));
     L.done = off;
     off = align_up(off + rows * sizeof(int));
     L.gdesc = off;
@@ -181,13 +186,17 @@ lp::Params make_params(const lp_plan_s* plan, const lp_io& io) {
     p.status = io.status;
     p.ctrl = plan->ctrl;
     p.queue = plan->queue;
-    p.ticket = plan->ticket;
+    p.row_best = plan->row_best;
     p.done = plan->done;
     p.gdesc = plan->gdesc;
     p.part_ms = plan->part_ms;
     p.part_keys = plan->part_keys;
     p.timeout_ns = (unsigned long long)(plan->d.timeout_ns > 0 ? plan->d.timeout_ns : kDefaultTimeoutNs);
     p.debug_flags = plan->d.flags & LP_PLAN_DEBUG_FORCE_TIMEOUT;
+    p.trace = plan->trace;
+    p.trace_count = plan->trace_count;
+    p.trace_cap = plan->trace_cap;
+    p.trace_ctas = plan->trace_ctas;
     return p;
 }
 
@@ -230,7 +239,7 @@ int lp_plan_create(lp_plan_t* out, const lp_plan_desc* desc) {
     if (!plan) return LP_EINVAL;
     plan->d = *desc;
     plan->elt = elt_of(desc->dtype);
-    plan->T = (int)((desc->V + lp::kTileElems - 1) / lp::kTileElems);
+    plan->T = (int)((desc->V + lp::tile_elems_of_dtype(desc->dtype) - 1) / lp::tile_elems_of_dtype(desc->dtype));
     cudaError_t e = lp::query_launch_cfg(desc->dtype, &plan->cfg);
     if (e != cudaSuccess) {
         delete plan;
@@ -244,8 +253,8 @@ int lp_plan_create(lp_plan_t* out, const lp_plan_desc* desc) {
     }
     plan->scratch_bytes = L.total;
     plan->ctrl = reinterpret_cast<lp::Ctrl*>(plan->scratch + L.ctrl);
-    plan->queue = reinterpret_cast<int*>(plan->scratch + L.queue);
-    plan->ticket = reinterpret_cast<int*>(plan->scratch + L.ticket);
+    plan->queue = reinterpret_cast<unsigned long long*>(plan->scratch + L.queue);
+    plan->row_best = reinterpret_cast<unsigned long long*>(plan->scratch + L.row_best);
     plan->done = reinterpret_cast<int*>(plan->scratch + L.done);
     plan->gdesc = reinterpret_cast<int4*>(plan->scratch + L.gdesc);
     plan->part_ms = reinterpret_cast<float2*>(plan->scratch + L.part_ms);
@@ -274,8 +283,19 @@ int lp_plan_create(lp_plan_t* out, const lp_plan_desc* desc) {
             s.status = reinterpret_cast<uint32_t*>(plan->staging + S.status);
         }
     }
+    if (e == cudaSuccess && (desc->flags & LP_PLAN_DEBUG_TRACE)) {
+        plan->trace_cap = 2048;
+        plan->trace_ctas = plan->cfg.grid;
+        const size_t ev = ((size_t)plan->trace_ctas * 3 + 1) * plan->trace_cap * 2 * sizeof(unsigned long long);
+        e = cudaMalloc(&plan->trace, ev);
+        if (e == cudaSuccess) e = cudaMalloc(&plan->trace_count, (size_t)plan->trace_ctas * 3 * sizeof(unsigned));
+        if (e == cudaSuccess) e = cudaMemset(plan->trace, 0, ev);
+        if (e == cudaSuccess) e = cudaMemset(plan->trace_count, 0, (size_t)plan->trace_ctas * 3 * sizeof(unsigned));
+    }
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
+        if (plan->trace) cudaFree(plan->trace);
+        if (plan->trace_count) cudaFree(plan->trace_count);
         if (plan->staging) cudaFree(plan->staging);
         cudaFree(plan->scratch);
         delete plan;
@@ -289,6 +309,8 @@ int lp_plan_destroy(lp_plan_t plan) {
     if (!plan) return LP_EINVAL;
     DeviceGuard guard(plan->d.device);
     cudaError_t e = cudaSuccess;
+    if (plan->trace) cudaFree(plan->trace);
+    if (plan->trace_count) cudaFree(plan->trace_count);
     if (plan->staging) e = cudaFree(plan->staging);
     cudaError_t e2 = cudaFree(plan->scratch);
     delete plan;
@@ -410,6 +432,24 @@ int lp_debug_poison_scratch(lp_plan_t plan, void* stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaMemsetAsync(plan->part_ms, 0xFF, plan->part_ms_bytes, s);
     if (e == cudaSuccess) e = cudaMemsetAsync(plan->part_keys, 0xFF, plan->part_keys_bytes, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return LP_OK;
+}
+
+int lp_debug_trace(lp_plan_t plan, uint64_t* events, uint32_t* counts, int32_t* ctas, int32_t* cap) {
+    if (!plan || !ctas || !cap) return LP_EINVAL;
+    if (!plan->trace) return LP_ESTATE;
+    *ctas = plan->trace_ctas;
+    *cap = plan->trace_cap;
+    if (!events) return LP_OK;
+    if (!counts) return LP_EINVAL;
+    DeviceGuard guard(plan->d.device);
+    const size_t ev = ((size_t)plan->trace_ctas * 3 + 1) * plan->trace_cap * 2 * sizeof(unsigned long long);
+    cudaError_t e = cudaStreamSynchronize(plan->last_stream);
+    if (e == cudaSuccess) e = cudaMemcpy(events, plan->trace, ev, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess)
+        e = cudaMemcpy(counts, plan->trace_count, (size_t)plan->trace_ctas * 3 * sizeof(unsigned),
+                       cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return cuda_fail(e);
     return LP_OK;
 }

@@ -182,9 +182,15 @@ def _cmp_lp(r, what, gb, ob, stats, tol=TOL):
         assert (gb & 0xFFFFFFFF) != 0x80000000, f"row {r}: {what} -0 not normalised"
 
 
+def lpe_tile_elems(dtype: str) -> int:
+    """Vocabulary tile of the CUDA path: 32 KiB of logits."""
+    return 32768 // (2 if dtype == "bf16" else 4)
+
+
 def expected_tiles(w: W.Workload, orc: dict) -> np.ndarray:
     """Tiles each row must read: all tiles of rows the path reads, 0 elsewhere."""
-    T = (w.V + 8191) // 8192
+    te = lpe_tile_elems(w.dtype)
+    T = (w.V + te - 1) // te
     tiles = np.zeros(w.rows, np.int32)
     for g in range(w.groups):
         r0, r1 = int(w.group_indptr[g]), int(w.group_indptr[g + 1])
