@@ -78,7 +78,8 @@ enum {
     LP_ECAPACITY = -4, /* request beyond the plan's limits (k_max, k_alt_max, max_ids) */
     LP_EDTYPE = -5,    /* unknown dtype */
     LP_ECUDA = -6,     /* a CUDA runtime call failed (see lp_last_cuda_error) */
-    LP_ESTATE = -7     /* lp_run before lp_bind, or host staging not enabled */
+    LP_ESTATE = -7,    /* lp_run before lp_bind, or host staging not enabled */
+    LP_ESCRATCH = -8   /* lp_run_static: the run needs more scratch than its fixed array */
 };
 
 /* Device status bits (OR-ed into *status by a run). */
@@ -198,6 +199,48 @@ int lp_debug_trace(lp_plan_t plan, uint64_t* events, uint32_t* counts, int32_t* 
 
 /* Tiles per row for this plan (ceil(V / tile elements)). */
 int lp_plan_tiles_per_row(lp_plan_t plan);
+
+/* ---- Run without any device allocation ----
+ *
+ * No counterpart in the paper.  Some callers cannot call cudaMalloc: a serving
+ * process whose framework reserved the whole device for its own caching
+ * allocator (a raw allocation then fails or splits its pool), code called back
+ * from inside such an allocator (allocating there can deadlock on its lock),
+ * and runtimes that fix their device-memory budget when they start.
+ * lp_plan_create needs one cudaMalloc; lp_run_static needs none.
+ *
+ * lp_run_static performs exactly the operation of lp_plan_create + lp_bind +
+ * lp_run with `desc` and `io` (same kernels, same outputs), but its scratch
+ * (control block, work queue, per-row counters, group descriptors, per-tile
+ * partial results) lives in one fixed array of LP_STATIC_SCRATCH_BYTES in the
+ * library's device image.  Every GPU that loads the library holds that array
+ * until the process exits.
+ *
+ *   desc    V, V_padded, dtype, k_max, k_alt_max, max_ids, device, timeout_ns
+ *           as for a plan; max_rows / max_groups must cover io->rows /
+ *           io->groups.  LP_PLAN_HOST_STAGING and LP_PLAN_DEBUG_TRACE are
+ *           ignored (both would allocate).
+ *   io      device buffers as for lp_bind (caller-owned, same layouts).
+ *   stream  a cudaStream_t (NULL = legacy default stream).
+ *
+ * The scratch a run needs grows with io->rows * ceil(V / tile elements)
+ * (about 264 bytes per row tile, plus 20 bytes per row and 16 per group);
+ * a run that needs more than LP_STATIC_SCRATCH_BYTES is rejected with
+ * LP_ESCRATCH before anything is enqueued.  4 MiB covers, for example, 512
+ * rows of a 248,448-lane BF16 vocabulary.
+ *
+ * The first call on a device sets that device up (it looks up the array's
+ * device address and the kernels' launch shape); make that first call before
+ * any stream capture on the device.  Each call clears the array's control
+ * block on `stream` before its kernels; everything else in the array is
+ * written before it is read.  All calls share the one array, so calls whose
+ * work can overlap on the GPU (different streams, or different host threads)
+ * race and corrupt each other: serialise them on one stream.
+ *
+ * Returns after enqueueing.  Errors: LP_EINVAL, LP_ESHAPE, LP_EALIGN,
+ * LP_EDTYPE, LP_ECAPACITY, LP_ESCRATCH, LP_ECUDA. */
+#define LP_STATIC_SCRATCH_BYTES (4u << 20)
+int lp_run_static(const lp_plan_desc* desc, const lp_io* io, void* stream);
 
 /* Message of an LP_E* code. */
 const char* lp_strerror(int code);

@@ -32,12 +32,13 @@ PLAN_DEBUG_FORCE_TIMEOUT = 0x100
 PLAN_DEBUG_TRACE = 0x200
 
 ERRORS = {0: "LP_OK", -1: "LP_EINVAL", -2: "LP_ESHAPE", -3: "LP_EALIGN", -4: "LP_ECAPACITY",
-          -5: "LP_EDTYPE", -6: "LP_ECUDA", -7: "LP_ESTATE"}
+          -5: "LP_EDTYPE", -6: "LP_ECUDA", -7: "LP_ESTATE", -8: "LP_ESCRATCH"}
+STATIC_SCRATCH_BYTES = 4 << 20  # fixed device scratch of run_static
 
 # Every symbol include/lp_epilogue.h declares.
 EXPORTS = ("lp_plan_create", "lp_plan_destroy", "lp_plan_scratch_bytes", "lp_bind", "lp_run", "lp_run_host",
            "lp_run_host_bytes", "lp_debug_tiles_read", "lp_debug_poison_scratch", "lp_debug_trace",
-           "lp_plan_tiles_per_row",
+           "lp_plan_tiles_per_row", "lp_run_static",
            "lp_strerror", "lp_last_cuda_error")
 
 
@@ -109,6 +110,7 @@ def lib() -> ctypes.CDLL:
         L.lp_debug_poison_scratch.argtypes = [P, P]
         L.lp_plan_tiles_per_row.argtypes = [P]
         L.lp_debug_trace.argtypes = [P, P, P, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]
+        L.lp_run_static.argtypes = [ctypes.POINTER(PlanDesc), ctypes.POINTER(IO), P]
         L.lp_strerror.argtypes = [ctypes.c_int]
         L.lp_strerror.restype = ctypes.c_char_p
         L.lp_last_cuda_error.argtypes = []
@@ -282,3 +284,34 @@ class Plan:
         if stream is None:
             stream = torch.cuda.current_stream(self.device)
         _check(lib().lp_debug_poison_scratch(self._h, ctypes.c_void_p(stream.cuda_stream)), "lp_debug_poison_scratch")
+
+
+def run_static(desc: PlanDesc, *, logits, group_indptr, draft_tokens, sampled_tokens, requested, top_k,
+               token_ids, id_counts, records, accepted, emitted_tokens, status, lse_out=None, stream=None) -> None:
+    """Enqueues the epilogue through ``lp_run_static``: the same operation as
+    ``Plan(...).bind(...); run()``, but with no device allocation at all.
+
+    For callers that may not allocate device memory (a framework whose caching
+    allocator already holds the device, code called back from inside such an
+    allocator, runtimes with a fixed memory budget).  The scratch is one fixed
+    array of ``STATIC_SCRATCH_BYTES`` inside the library, shared by every call:
+    runs that need more are refused with ``LP_ESCRATCH``, and calls that can
+    overlap on the GPU (different streams or threads) race; keep them on one
+    stream.  The first call on a device sets it up; make it before any stream
+    capture on that device.  Buffers are CUDA tensors as for ``Plan.bind``."""
+    import torch
+    t = dict(logits=logits, group_indptr=group_indptr, draft_tokens=draft_tokens, sampled_tokens=sampled_tokens,
+             requested=requested, top_k=top_k, token_ids=token_ids, id_counts=id_counts, records=records,
+             accepted=accepted, emitted_tokens=emitted_tokens, status=status, lse_out=lse_out)
+    for name, x in t.items():
+        if x is None:
+            continue
+        if not isinstance(x, torch.Tensor) or not x.is_cuda or not x.is_contiguous():
+            raise ValueError(f"{name}: expected a contiguous CUDA tensor")
+    rows = int(logits.shape[0])
+    groups = int(group_indptr.numel()) - 1
+    io = IO(*[None if t[n] is None else t[n].data_ptr() for n in _IO_NAMES], rows, groups)
+    if stream is None:
+        stream = torch.cuda.current_stream(logits.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    _check(lib().lp_run_static(ctypes.byref(desc), ctypes.byref(io), ctypes.c_void_p(handle)), "lp_run_static")

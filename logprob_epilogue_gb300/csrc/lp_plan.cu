@@ -8,6 +8,7 @@
 
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 #include <new>
 
 #include "lp_epilogue.h"
@@ -466,6 +467,7 @@ const char* lp_strerror(int code) {
         case LP_EDTYPE: return "unknown dtype";
         case LP_ECUDA: return "CUDA runtime error (see lp_last_cuda_error)";
         case LP_ESTATE: return "plan not ready (nothing bound, or no host staging)";
+        case LP_ESCRATCH: return "run needs more scratch than lp_run_static's fixed array (LP_STATIC_SCRATCH_BYTES)";
         default: return "unknown error code";
     }
 }
@@ -473,3 +475,93 @@ const char* lp_strerror(int code) {
 int lp_last_cuda_error(void) { return g_last_cuda_error; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- lp_run_static
+//
+// The same run as plan + bind + run, with its scratch in a fixed array of the
+// library's device image instead of a cudaMalloc'd block (for callers that may
+// not allocate device memory).  Every call shares the array.
+namespace {
+
+constexpr size_t kStaticScratchBytes = LP_STATIC_SCRATCH_BYTES;
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+constexpr int kMaxStaticDevices = 64;
+struct StaticDevice {
+    bool ready;                 // device address looked up
+    unsigned char* base;        // device address of g_static_scratch on this device
+    bool cfg_ready[2];          // launch shape queried, per dtype
+    lp::LaunchCfg cfg[2];
+};
+std::mutex g_static_mu;
+StaticDevice g_static_dev[kMaxStaticDevices];
+
+// One-time set-up of `dev` (current): the array's device address and the
+// launch shape of `dtype`.  In host code g_static_scratch names a host-side
+// shadow, so the kernels only ever get the address returned here.
+cudaError_t static_setup(int dev, int dtype, unsigned char** base, lp::LaunchCfg* cfg) {
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    StaticDevice& sd = g_static_dev[dev];
+    if (!sd.ready) {
+        void* ptr = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&ptr, g_static_scratch);
+        if (e != cudaSuccess) return e;
+        if (ptr == nullptr) return cudaErrorInvalidSymbol;
+        sd.base = static_cast<unsigned char*>(ptr);
+        sd.ready = true;
+    }
+    if (!sd.cfg_ready[dtype]) {
+        const cudaError_t e = lp::query_launch_cfg(dtype, &sd.cfg[dtype]);
+        if (e != cudaSuccess) return e;
+        sd.cfg_ready[dtype] = true;
+    }
+    *base = sd.base;
+    *cfg = sd.cfg[dtype];
+    return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" int lp_run_static(const lp_plan_desc* desc, const lp_io* io, void* stream) {
+    int rc = check_desc(desc);
+    if (rc != LP_OK) return rc;
+    if (desc->device < 0 || desc->device >= kMaxStaticDevices) return LP_EINVAL;
+    // a plan object on the stack: never allocated, only carries the pointers
+    lp_plan_s run{};
+    run.d = *desc;
+    run.d.flags &= ~(LP_PLAN_HOST_STAGING | LP_PLAN_DEBUG_TRACE);
+    rc = check_io(&run, io);
+    if (rc != LP_OK) return rc;
+    // scratch sized for this run's rows and groups, not the descriptor's capacity
+    lp_plan_desc need = run.d;
+    need.max_rows = io->rows > 0 ? io->rows : 1;
+    need.max_groups = io->groups > 0 ? io->groups : 1;
+    const Layout L = layout_of(&need);
+    if (L.total > kStaticScratchBytes) return LP_ESCRATCH;
+
+    DeviceGuard guard(desc->device);
+    if (!guard.ok) return cuda_fail(cudaGetLastError());
+    unsigned char* base = nullptr;
+    cudaError_t e = static_setup(desc->device, desc->dtype, &base, &run.cfg);
+    if (e != cudaSuccess) return cuda_fail(e);
+    run.elt = elt_of(desc->dtype);
+    run.T = (int)((desc->V + lp::tile_elems_of_dtype(desc->dtype) - 1) / lp::tile_elems_of_dtype(desc->dtype));
+    run.ctrl = reinterpret_cast<lp::Ctrl*>(base + L.ctrl);
+    run.queue = reinterpret_cast<unsigned long long*>(base + L.queue);
+    run.row_best = reinterpret_cast<unsigned long long*>(base + L.row_best);
+    run.done = reinterpret_cast<int*>(base + L.done);
+    run.gdesc = reinterpret_cast<int4*>(base + L.gdesc);
+    run.part_ms = reinterpret_cast<float2*>(base + L.part_ms);
+    run.part_keys = reinterpret_cast<unsigned long long*>(base + L.part_keys);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // The array keeps the previous call's contents.  The control block must
+    // start at zero (its never-written word is the forced-timeout test's
+    // flag); the prepare kernel resets the queue, counters and descriptors, and
+    // tile partials are written before they are read.
+    e = cudaMemsetAsync(run.ctrl, 0, sizeof(lp::Ctrl), s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    const lp::Params p = make_params(&run, *io);
+    e = lp::launch_epilogue(p, desc->dtype, run.cfg, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return LP_OK;
+}
