@@ -13,7 +13,7 @@ __host__ __device__ constexpr int tile_elems() { return kTileBytes / ELT; }
 inline int tile_elems_of_dtype(int dtype) { return dtype == 1 ? kTileBytes / 2 : kTileBytes / 4; }
 constexpr int kConsumerThreads = 256;   // 8 compute warps
 constexpr int kThreads = kConsumerThreads + 64;  // + 1 producer warp + 1 merge warp
-constexpr int kRing = 8;                // tile results in flight between compute and merge warps
+constexpr int kRing = 6;                // tile results in flight between compute and merge warps
 constexpr int kKeysPerTile = 32;        // retained sort keys per tile
 constexpr int kRecordWords = 258;
 constexpr int kMaxIds = 128;
@@ -46,16 +46,25 @@ template <> struct StageCfg<4> {
 enum : int { kModeArgmax = 0, kModeLse = 1, kModeNatural = 2, kModeRecord = 3 };
 
 // Run control block; each hot word sits in its own 128-byte line.
+//
+// Work items are (queue position, tile) pairs.  Positions [0, fresh_rows) hold
+// the depth-0 rows written by the prepare kernel ("fresh" items f = pos*T +
+// tile, handed out by fresh_next); rows appended after an acceptance take
+// positions fresh_rows + j ("chained" items c = j*T + tile, handed out by
+// chain_next, in order, before any fresh item once their row is appended).
 struct Ctrl {
-    unsigned int next_item;   // next work item (queue position * T + tile) to hand out
+    unsigned int fresh_next;  // fresh items handed out
     unsigned int pad0[31];
-    unsigned int q_tail;      // queue positions reserved (depth-0 rows + appended rows)
+    unsigned int chain_next;  // chained items claimed (a claim may run ahead of chain_tail)
     unsigned int pad1[31];
-    int outstanding;          // rows queued or in flight whose acceptance is not decided
+    unsigned int chain_tail;  // chained rows reserved (their queue entries follow)
     unsigned int pad2[31];
+    int outstanding;          // groups whose acceptance is not complete
+    unsigned int pad3[31];
+    unsigned int fresh_rows;  // depth-0 rows (set by the prepare kernel)
     unsigned int abort;       // 1: malformed groups, the stream kernel does nothing
     unsigned int never;       // never written: the forced-timeout test hook waits on it
-    unsigned int pad3[30];
+    unsigned int pad4[29];
 };
 
 struct Params {
@@ -85,6 +94,7 @@ struct Params {
     unsigned long long* row_best;   // [max_rows] best (argmax) key over the finished tiles
     int4* gdesc;          // [max_groups] x = first row, y = k | mode << 8 | explicit << 12 |
                           // requested << 13, z = top_k or id count, w = sampled token
+    int4* rec_tasks;      // [max_rows] per row: (chosen token, queue entry, 1 = record to build, 0)
     float2* part_ms;      // [max_rows * T] tile (max, exp-sum)
     unsigned long long* part_keys;  // [max_rows * T * 32] tile keys, descending
     unsigned long long timeout_ns;
@@ -99,9 +109,10 @@ struct Params {
 struct LaunchCfg {
     int grid;           // persistent CTAs
     int smem_bytes;     // dynamic shared memory of the stream kernel
+    int sms;            // multiprocessors of the device
 };
 
-// Enqueue prepare + stream kernels (lp_kernels.cu).
+// Enqueue the prepare, stream and record kernels (lp_kernels.cu).
 cudaError_t launch_epilogue(const Params& p, int dtype, const LaunchCfg& cfg, cudaStream_t stream);
 // Occupancy-derived configuration for a dtype on the current device.
 cudaError_t query_launch_cfg(int dtype, LaunchCfg* cfg);

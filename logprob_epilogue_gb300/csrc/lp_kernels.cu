@@ -56,6 +56,7 @@ namespace {
 constexpr unsigned kFull = 0xffffffffu;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kNegInf = -__builtin_huge_valf();
+constexpr float kPosInf = __builtin_huge_valf();
 constexpr unsigned kStatusBadId = 0x1u, kStatusBadToken = 0x2u, kStatusBadCount = 0x4u,
                    kStatusBadGroup = 0x8u, kStatusTimeout = 0x10u;
 constexpr unsigned kDebugForceTimeout = 0x100u;
@@ -102,31 +103,28 @@ __device__ __forceinline__ float ex2(float x) {
 
 __device__ __forceinline__ void cbar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
-// Barrier over the compute threads that also ORs a predicate across them.
-__device__ __forceinline__ bool cbar_or(bool v) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 q, %1, 0;\n\t"
-        "bar.red.or.pred p, 1, 256, q;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)v)
-        : "memory");
-    return r != 0;
-}
-
 template <typename T>
 __device__ __forceinline__ T vload(const T* p) { return *reinterpret_cast<const volatile T*>(p); }
 template <typename T>
 __device__ __forceinline__ void vstore(T* p, T v) { *reinterpret_cast<volatile T*>(p) = v; }
+
+// atomicAdd with acquire-release semantics at GPU scope: this thread's earlier
+// writes (and those ordered before it by a warp barrier) are visible to whoever
+// reads the result, and the writes released before the values it reads are
+// visible to this thread afterwards.
+__device__ __forceinline__ int atomic_add_acq_rel(int* p, int v) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
 
 // ---- optional device timeline (plans created with the trace flag)
 //
 // Each CTA has three event rings (producer, compute, merge warp) of
 // p.trace_cap events; an event is (globaltimer ns, type << 56 | row << 24 | tile).
 enum : unsigned { kTrKernel = 1, kTrClaim, kTrIssue, kTrTileStart, kTrTileEnd, kTrPublish, kTrMergeStart,
-                  kTrDecision, kTrMergeEnd, kTrPrepStart, kTrPrepEnd, kTrExit, kTrTileB1, kTrTileB2 };
+                  kTrDecision, kTrMergeEnd, kTrPrepStart, kTrPrepEnd, kTrExit, kTrTileB1, kTrTileB2,
+                  kTrWarpAppend, kTrWarpDone };
 
 __shared__ unsigned g_trace_n[3];  // per-CTA event counts (producer, compute, merge)
 
@@ -134,12 +132,11 @@ __device__ __forceinline__ void trace(const Params& p, unsigned type, int row, i
     if (p.trace == nullptr || !writer) return;
     const int role = type == kTrClaim || type == kTrIssue || type == kTrExit ? 0
                    : (type == kTrTileStart || type == kTrTileEnd || type == kTrKernel || type == kTrTileB1 ||
-                      type == kTrTileB2) ? 1 : 2;
+                      type == kTrTileB2 || type == kTrWarpAppend || type == kTrWarpDone) ? 1 : 2;
     unsigned* cnt = g_trace_n + role;
-    const unsigned i = *cnt;
+    const unsigned i = atomicAdd(cnt, 1u);  // several warps may record into one ring
     if (i >= (unsigned)p.trace_cap) return;
-    *cnt = i + 1;
-    p.trace_count[blockIdx.x * 3 + role] = i + 1;
+    atomicMax(&p.trace_count[blockIdx.x * 3 + role], i + 1);
     unsigned long long* e = p.trace + (((size_t)blockIdx.x * 3 + role) * p.trace_cap + i) * 2;
     e[0] = globaltimer();
     e[1] = ((unsigned long long)type << 56) | ((unsigned long long)(row & 0xFFFFFFFF) << 24) |
@@ -263,15 +260,21 @@ __device__ __forceinline__ unsigned long long warp_bitonic_clean_desc(unsigned l
     return v;
 }
 
-constexpr int kTasks = 64;  // record tasks a CTA can hold for its compute warps
 constexpr int kMaxStages = 8;
+constexpr int kWarps = kConsumerThreads / 32;  // compute warps
 static_assert(StageCfg<2>::kStages <= kMaxStages && StageCfg<4>::kStages <= kMaxStages, "stage count");
 
-// One tile result handed from the compute warps to the merge warp.
+// One tile's results, handed from the compute warps (one entry per warp) to the
+// merge warp, which combines them.
 struct ResultSlot {
-    int4 info;                       // row, tile, queue entry (< 0: no more tiles), mode
-    float M, S;                      // tile max and sum exp(x - M)
-    unsigned long long keys[kKeysPerTile];  // descending; keys[0] = tile argmax key
+    int4 info;                              // row, tile, queue entry (< 0: no more tiles), mode
+    float wM[kWarps];                       // warp maximum
+    float wS[kWarps];                       // warp sum exp(x - wM)
+    unsigned long long wkey[kWarps];        // argmax key of the warp's elements (non-natural tiles)
+    float wTheta[kWarps];                   // natural tiles: the warp's 4th largest thread maximum
+    int wcnt[kWarps];                       // natural tiles: keys in cand[w] (<= 32)
+    unsigned long long cand[kWarps][32];    // natural tiles: the warp's keys >= theta (its best 32 if more)
+    unsigned long long keys[32];            // natural tiles: the tile's best 32 keys, descending
 };
 
 struct Shared {
@@ -279,97 +282,22 @@ struct Shared {
     uint64_t empty[kMaxStages];      // stage released (8 compute warps)
     uint64_t rfull[kRing];           // result written (8 compute warps)
     uint64_t rempty[kRing];          // result consumed (merge warp)
+    uint64_t rtheta[kRing];          // natural tiles: thresholds of the 8 warps written
+    uint64_t rcand[kRing];           // natural tiles: candidates of the 8 warps written
     int4 info[kMaxStages];           // work item of each stage
     ResultSlot res[kRing];
-    union {
-        unsigned long long cand[kCandCap];  // natural-alternative candidates of a tile
-        unsigned long long lists[8][32];    // per-warp partial top-32 lists of a record task
-    };
-    unsigned long long wkey[2][8];   // per-warp partials, double-buffered by tile parity
-    float wM[2][8];
-    float wS[2][8];
-    float wTheta[2][8];
-    int ncand[2];
-    int wcnt[2][8];                  // candidates per warp, double-buffered by tile parity
-    unsigned long long red_u64[8];
-    double red_d[8];
-    float red_f[8];
-    float red_f2[8];
-    int red_i[8];
-    float lse;
-    float xchosen;
-    int rec[kRecordWords + 2];       // record being assembled by the compute warps
     int2 batch[kRing];               // (row, queue entry) of the tiles in a merge-warp batch
-    int mrec[kRecordWords + 2];      // record assembled by the merge warp (task ring full)
-    int4 task[kTasks];               // record tasks: (row, chosen, queue entry, kModeRecord)
-    unsigned task_head;              // tasks taken by the compute warps
-    unsigned task_tail;              // tasks pushed by the merge warp
-    unsigned task_snap[2];           // task_tail seen at a tile's first barrier (by tile parity)
 };
 
-// ---- block reductions over the 256 compute threads (slow path only)
-
-__device__ __forceinline__ float block_max_f(float v, Shared& sm, int lane, int warp) {
-    v = warp_max_f(v);
-    if (lane == 0) sm.red_f[warp] = v;
-    cbar();
-    float r = sm.red_f[0];
-#pragma unroll
-    for (int i = 1; i < 8; ++i) r = fmaxf(r, sm.red_f[i]);
-    cbar();
-    return r;
-}
-
-__device__ __forceinline__ int block_sum_i(int v, Shared& sm, int lane, int warp) {
-    v = warp_sum_i(v);
-    if (lane == 0) sm.red_i[warp] = v;
-    cbar();
-    int r = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) r += sm.red_i[i];
-    cbar();
-    return r;
-}
-
-__device__ __forceinline__ double block_sum_d(double v, Shared& sm, int lane, int warp) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-    if (lane == 0) sm.red_d[warp] = v;
-    cbar();
-    double r = 0.0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) r += sm.red_d[i];
-    cbar();
-    return r;
-}
-
-// Exclusive prefix sum over the 256 compute threads; *total = the sum.
-__device__ __forceinline__ int block_excl_scan_i(int v, int* total, Shared& sm, int lane, int warp) {
-    int incl = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int n = __shfl_up_sync(kFull, incl, o);
-        if (lane >= o) incl += n;
-    }
-    if (lane == 31) sm.red_i[warp] = incl;
-    cbar();
-    int before = 0, all = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int t = sm.red_i[i];
-        before += (i < warp) ? t : 0;
-        all += t;
-    }
-    cbar();
-    *total = all;
-    return before + incl - v;
-}
-
-__device__ __forceinline__ double warp_sum_d(double v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-    return v;
-}
+// Shared memory of the record kernel.
+struct RecShared {
+    unsigned long long lists[kWarps][32];   // per-warp partial top-32 lists
+    float red_f[kWarps];
+    float red_f2[kWarps];
+    float lse;
+    float xchosen;
+    int rec[kRecordWords + 2];              // record being assembled
+};
 
 // ---- tile element access
 //
@@ -400,55 +328,8 @@ __device__ __forceinline__ uint4 lds128(const void* p) {
     return v;
 }
 
-__device__ __forceinline__ int atomic_add_shared(int* p, int v) {
-    int old;
-    asm volatile("atom.shared.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(smem_u32(p)), "r"(v) : "memory");
-    return old;
-}
-
-__device__ __forceinline__ void st_shared_u64(unsigned long long* p, unsigned long long v) {
-    asm volatile("st.shared.u64 [%0], %1;" ::"r"(smem_u32(p)), "l"(v) : "memory");
-}
-
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-// Register copy of a thread's tile elements: FP32 as floats, BF16 kept packed
-// two per word (element k in the low half of word k/2 when k is even).
-template <int ELT>
-struct TileRegs;
-
-template <>
-struct TileRegs<4> {
-    static constexpr int kN = TileLayout<4>::EPT;
-    float x[kN];
-    __device__ __forceinline__ float get(int k) const { return x[k]; }
-    __device__ __forceinline__ float max() const {
-        float m = x[0];
-#pragma unroll
-        for (int k = 1; k < kN; ++k) m = fmaxf(m, x[k]);
-        return m;
-    }
-    __device__ __forceinline__ void load(const unsigned char* stage, bool full, int nv, int tid) {
-        if (full) {
-#pragma unroll
-            for (int c = 0; c < TileLayout<4>::NCH; ++c) {
-                const uint4 v = lds128(stage + (size_t)(c * kConsumerThreads + tid) * 16);
-                x[c * 4 + 0] = __uint_as_float(v.x);
-                x[c * 4 + 1] = __uint_as_float(v.y);
-                x[c * 4 + 2] = __uint_as_float(v.z);
-                x[c * 4 + 3] = __uint_as_float(v.w);
-            }
-        } else {
-            const float* f = reinterpret_cast<const float*>(stage);
-#pragma unroll
-            for (int k = 0; k < kN; ++k) {
-                const int e = k * kConsumerThreads + tid;
-                x[k] = e < nv ? f[e] : kNegInf;
-            }
-        }
-    }
-};
 
 __device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
     uint32_t d;
@@ -456,102 +337,136 @@ __device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
     return d;
 }
 
-template <>
-struct TileRegs<2> {
-    static constexpr int kN = TileLayout<2>::EPT;
-    uint32_t w[kN / 2];
-    __device__ __forceinline__ float get(int k) const { return (k & 1) ? bf16_hi(w[k >> 1]) : bf16_lo(w[k >> 1]); }
-    __device__ __forceinline__ float max() const {
-        uint32_t m = w[0];
-#pragma unroll
-        for (int i = 1; i < kN / 2; ++i) m = bf16x2_max(m, w[i]);
-        return fmaxf(bf16_lo(m), bf16_hi(m));
-    }
-    __device__ __forceinline__ void load(const unsigned char* stage, bool full, int nv, int tid) {
-        if (full) {
-#pragma unroll
-            for (int c = 0; c < TileLayout<2>::NCH; ++c) {
-                const uint4 v = lds128(stage + (size_t)(c * kConsumerThreads + tid) * 16);
-                w[c * 4 + 0] = v.x;
-                w[c * 4 + 1] = v.y;
-                w[c * 4 + 2] = v.z;
-                w[c * 4 + 3] = v.w;
-            }
-        } else {
-            const unsigned short* h = reinterpret_cast<const unsigned short*>(stage);
-#pragma unroll
-            for (int i = 0; i < kN / 2; ++i) {
-                const int e0 = (2 * i) * kConsumerThreads + tid, e1 = (2 * i + 1) * kConsumerThreads + tid;
-                const uint32_t lo = e0 < nv ? h[e0] : 0xFF80u;  // -inf in masked lanes
-                const uint32_t hi = e1 < nv ? h[e1] : 0xFF80u;
-                w[i] = lo | (hi << 16);
-            }
-        }
-    }
-};
-
 // Streaming passes over a full stage (thread i reads vectors c*256 + i).
+//
+// Pass 1 keeps the maximum of each of the thread's 16-byte vectors in cm[c]
+// (BF16: packed bf16x2, the even elements' maximum in the low half, the odd
+// ones' in the high half; FP32: the float bits), so that the argmax search and
+// the candidate selection later touch only the vectors that can matter.
 template <int ELT>
-__device__ __forceinline__ float stage_max(const unsigned char* sp, int tid) {
+__device__ __forceinline__ float vec_max(uint32_t cm) {
+    if constexpr (ELT == 2) {
+        return fmaxf(bf16_lo(cm), bf16_hi(cm));
+    } else {
+        return __uint_as_float(cm);
+    }
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+template <int ELT>
+__device__ __forceinline__ float stage_max(const unsigned char* sp, int tid, uint32_t (&cm)[TileLayout<ELT>::NCH]) {
     constexpr int NCH = TileLayout<ELT>::NCH;
     if constexpr (ELT == 2) {
-        uint32_t a = 0xFF80FF80u, b = 0xFF80FF80u;
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
             const uint4 v = lds128(sp + (size_t)(c * kConsumerThreads + tid) * 16);
-            a = bf16x2_max(a, bf16x2_max(v.x, v.y));
-            b = bf16x2_max(b, bf16x2_max(v.z, v.w));
+            cm[c] = bf16x2_max(bf16x2_max(v.x, v.y), bf16x2_max(v.z, v.w));
+        }
+        uint32_t a = cm[0], b = cm[1];
+#pragma unroll
+        for (int c = 2; c < NCH; c += 2) {
+            a = bf16x2_max(a, cm[c]);
+            b = bf16x2_max(b, cm[c + 1]);
         }
         a = bf16x2_max(a, b);
         return fmaxf(bf16_lo(a), bf16_hi(a));
     } else {
-        float a = kNegInf, b = kNegInf;
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
             const uint4 v = lds128(sp + (size_t)(c * kConsumerThreads + tid) * 16);
-            a = fmaxf(a, fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)));
-            b = fmaxf(b, fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
+            cm[c] = __float_as_uint(fmax3(__uint_as_float(v.x), __uint_as_float(v.y),
+                                          fmaxf(__uint_as_float(v.z), __uint_as_float(v.w))));
+        }
+        float a = __uint_as_float(cm[0]), b = __uint_as_float(cm[1]);
+#pragma unroll
+        for (int c = 2; c < NCH; c += 2) {
+            a = fmaxf(a, __uint_as_float(cm[c]));
+            b = fmaxf(b, __uint_as_float(cm[c + 1]));
         }
         return fmaxf(a, b);
     }
 }
 
+// Packed FP32 pairs (two lanes of work per instruction on the FMA pipe).
+__device__ __forceinline__ unsigned long long f2_pack(float lo, float hi) {
+    return (static_cast<unsigned long long>(__float_as_uint(hi)) << 32) | __float_as_uint(lo);
+}
+__device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsigned long long b,
+                                                     unsigned long long c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ unsigned long long f2_ex2(unsigned long long a) {
+    return f2_pack(ex2(__uint_as_float(static_cast<uint32_t>(a))), ex2(__uint_as_float(static_cast<uint32_t>(a >> 32))));
+}
+__device__ __forceinline__ float f2_sum(unsigned long long a) {
+    return __uint_as_float(static_cast<uint32_t>(a)) + __uint_as_float(static_cast<uint32_t>(a >> 32));
+}
+
+// Pass 2: sum of 2^(x*log2e - mb) over the thread's elements, two at a time.
 template <int ELT>
 __device__ __forceinline__ float stage_expsum(const unsigned char* sp, int tid, float mb) {
     constexpr int NCH = TileLayout<ELT>::NCH;
-    float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
+    const unsigned long long L2E = f2_pack(kLog2e, kLog2e), NMB = f2_pack(-mb, -mb);
+    unsigned long long s0 = 0ull, s1 = 0ull;  // two accumulators: the vector maxima stay live
 #pragma unroll
     for (int c = 0; c < NCH; ++c) {
         const uint4 v = lds128(sp + (size_t)(c * kConsumerThreads + tid) * 16);
         if constexpr (ELT == 2) {
-            s0 += ex2(fmaf(bf16_lo(v.x), kLog2e, -mb)) + ex2(fmaf(bf16_hi(v.x), kLog2e, -mb));
-            s1 += ex2(fmaf(bf16_lo(v.y), kLog2e, -mb)) + ex2(fmaf(bf16_hi(v.y), kLog2e, -mb));
-            s2 += ex2(fmaf(bf16_lo(v.z), kLog2e, -mb)) + ex2(fmaf(bf16_hi(v.z), kLog2e, -mb));
-            s3 += ex2(fmaf(bf16_lo(v.w), kLog2e, -mb)) + ex2(fmaf(bf16_hi(v.w), kLog2e, -mb));
+            s0 = f2_add(s0, f2_ex2(f2_fma(f2_pack(bf16_lo(v.x), bf16_hi(v.x)), L2E, NMB)));
+            s1 = f2_add(s1, f2_ex2(f2_fma(f2_pack(bf16_lo(v.y), bf16_hi(v.y)), L2E, NMB)));
+            s0 = f2_add(s0, f2_ex2(f2_fma(f2_pack(bf16_lo(v.z), bf16_hi(v.z)), L2E, NMB)));
+            s1 = f2_add(s1, f2_ex2(f2_fma(f2_pack(bf16_lo(v.w), bf16_hi(v.w)), L2E, NMB)));
         } else {
-            s0 += ex2(fmaf(__uint_as_float(v.x), kLog2e, -mb));
-            s1 += ex2(fmaf(__uint_as_float(v.y), kLog2e, -mb));
-            s2 += ex2(fmaf(__uint_as_float(v.z), kLog2e, -mb));
-            s3 += ex2(fmaf(__uint_as_float(v.w), kLog2e, -mb));
+            const unsigned long long a = (static_cast<unsigned long long>(v.y) << 32) | v.x;
+            const unsigned long long b = (static_cast<unsigned long long>(v.w) << 32) | v.z;
+            s0 = f2_add(s0, f2_ex2(f2_fma(a, L2E, NMB)));
+            s1 = f2_add(s1, f2_ex2(f2_fma(b, L2E, NMB)));
         }
     }
-    return (s0 + s1) + (s2 + s3);
+    return f2_sum(f2_add(s0, s1));
+}
+
+// Partial tile (the last of a row): element k of thread i is tile element
+// k*256 + i, read one at a time; lanes past nv hold -inf.
+template <int ELT>
+__device__ __forceinline__ float partial_elem(const unsigned char* sp, int nv, int k, int tid) {
+    const int e = k * kConsumerThreads + tid;
+    if (e >= nv) return kNegInf;
+    if constexpr (ELT == 4) {
+        return reinterpret_cast<const float*>(sp)[e];
+    } else {
+        return __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const unsigned short*>(sp)[e]) << 16);
+    }
 }
 
 template <int ELT>
 __device__ __forceinline__ float partial_max(const unsigned char* sp, int nv, int tid) {
-    TileRegs<ELT> x;
-    x.load(sp, false, nv, tid);
-    return x.max();
+    float m = kNegInf;
+#pragma unroll 4
+    for (int k = 0; k < TileLayout<ELT>::EPT; ++k) m = fmaxf(m, partial_elem<ELT>(sp, nv, k, tid));
+    return m;
 }
 
 template <int ELT>
 __device__ __forceinline__ float partial_expsum(const unsigned char* sp, int nv, int tid, float mb) {
-    TileRegs<ELT> x;
-    x.load(sp, false, nv, tid);
     float s = 0.0f;
-#pragma unroll
-    for (int k = 0; k < TileRegs<ELT>::kN; ++k) s += ex2(fmaf(x.get(k), kLog2e, -mb));
+#pragma unroll 4
+    for (int k = 0; k < TileLayout<ELT>::EPT; ++k) {
+        const float x = partial_elem<ELT>(sp, nv, k, tid);
+        s += x > kNegInf ? ex2(fmaf(x, kLog2e, -mb)) : 0.0f;
+    }
     return s;
 }
 
@@ -590,6 +505,7 @@ __global__ void __launch_bounds__(1024) lp_prepare_kernel(Params p) {
         p.done[r] = 0;
         p.queue[r] = ~0ull;
         p.row_best[r] = 0ull;
+        p.rec_tasks[r] = make_int4(0, 0, 0, 0);
     }
     if (tid == 0) *p.status = 0u;
     const int G = p.G;
@@ -606,8 +522,10 @@ __global__ void __launch_bounds__(1024) lp_prepare_kernel(Params p) {
         if (tid == 0) {
             atomicOr(p.status, kStatusBadGroup);
             p.ctrl->abort = 1u;
-            p.ctrl->next_item = 0u;
-            p.ctrl->q_tail = 0u;
+            p.ctrl->fresh_next = 0u;
+            p.ctrl->chain_next = 0u;
+            p.ctrl->chain_tail = 0u;
+            p.ctrl->fresh_rows = 0u;
             p.ctrl->outstanding = 0;
         }
         return;
@@ -685,8 +603,10 @@ __global__ void __launch_bounds__(1024) lp_prepare_kernel(Params p) {
             e[2] = globaltimer();
             e[3] = (unsigned long long)kTrPrepEnd << 56;
         }
-        p.ctrl->next_item = 0u;
-        p.ctrl->q_tail = static_cast<unsigned>(s_base);
+        p.ctrl->fresh_next = 0u;
+        p.ctrl->chain_next = 0u;
+        p.ctrl->chain_tail = 0u;
+        p.ctrl->fresh_rows = static_cast<unsigned>(s_base);
         p.ctrl->outstanding = s_base;
         p.ctrl->abort = 0u;
     }
@@ -694,39 +614,33 @@ __global__ void __launch_bounds__(1024) lp_prepare_kernel(Params p) {
 
 // ------------------------------------------------------------------ producer
 //
-// Work items are numbered in queue order: item i is tile (i % T) of the row
-// at queue position i / T.  Positions below q_tail exist (depth-0 rows from
-// the prepare kernel, then rows appended by merges); a producer that draws an
-// item of a position not yet appended waits until it is, or until no row is
-// outstanding (then the run is complete).
-
-// Items drawn per atomic: 4 while the queue holds plenty of work for every
-// CTA, else 1 (short queues are latency-bound: spread a row's tiles wide).
-__device__ __forceinline__ unsigned claim_size(unsigned tail_items, unsigned next) {
-    return tail_items > next + 16u * gridDim.x ? 4u : 1u;
-}
+// One lane draws work items one at a time and streams each 32 KiB tile into a
+// shared-memory stage with a TMA bulk copy.  Chained items (rows appended after
+// an acceptance) come first: each producer always owns the next chained item
+// it claimed (claims run ahead of the appended rows, in order) and takes it as
+// soon as its row exists; otherwise it takes a fresh item.  Rows deep in a
+// verify chain therefore start at once instead of queueing behind the depth-0
+// rows, and single-item claims spread a row's tiles over many CTAs.  The next
+// item is chosen right after a copy is issued, while the stages are busy.
+constexpr unsigned kNone = 0xFFFFFFFFu;
 
 template <int ELT>
 __device__ __noinline__ void producer_loop(const Params& p, Shared& sm, unsigned char* stages, unsigned long long t0) {
     constexpr int S = StageCfg<ELT>::kStages;
-    constexpr int TILE_BYTES = kTileBytes;
     constexpr int kTE = tile_elems<ELT>();
     const unsigned long long deadline = t0 + p.timeout_ns;
     const uint64_t policy = evict_first_policy();
     Ctrl* ctrl = p.ctrl;
     const unsigned T = (unsigned)p.T;
+    const unsigned F = vload(&ctrl->fresh_rows);
+    const unsigned fresh_items = F * T;
     int stage = 0;
     uint32_t phase = 0;
-    unsigned cached_tail = vload(&ctrl->q_tail);
-    unsigned last_pos = 0xFFFFFFFFu;
-    int cur_entry = -1, cur_row = 0, cur_mode = 0;
-    // claims: the current chunk, plus (while the queue is long) the next chunk
-    // with its atomic already in flight
-    unsigned cur = 0, cur_n = 0, nxt = 0, nxt_n = 0;
-    unsigned pre_pos = 0xFFFFFFFFu;   // queue position whose entry was prefetched
-    unsigned long long pre_val = ~0ull;
-    int prev_stage = -1;              // stage of the last fill and the phase bit of that fill
-    uint32_t prev_phase = 0;
+    unsigned chain_claim = kNone;    // chained item owned by this producer, not yet issued
+    unsigned chain_rows = 0;         // chained rows seen appended
+    unsigned fresh_ahead = kNone;    // fresh item already claimed
+    bool fresh_done = fresh_items == 0;
+    bool timed_out = false;
     for (;;) {
         int4 item = make_int4(0, 0, -1, 0);
         if (p.debug_flags & kDebugForceTimeout) {
@@ -735,78 +649,55 @@ __device__ __noinline__ void producer_loop(const Params& p, Shared& sm, unsigned
                 if (globaltimer() > deadline) break;
                 __nanosleep(1000);
             }
-            atomicOr(p.status, kStatusTimeout);
+            timed_out = true;
         } else {
-            if (cur_n == 0) {
-                const unsigned tail_items = cached_tail * T;
-                const unsigned seen = nxt_n > 0 ? nxt : cur;
-                if (prev_stage >= 0 && tail_items < seen + 2u * gridDim.x) {
-                    // short queue: take a tile only once the compute warps hold the
-                    // previous one, so a row's tiles spread over many CTAs
-                    if (!mbar_wait(&sm.empty[prev_stage], prev_phase, deadline)) {
-                        atomicOr(p.status, kStatusTimeout);
-                        return;
-                    }
-                }
-                if (nxt_n > 0) {
-                    cur = nxt;
-                    cur_n = nxt_n;
-                    nxt_n = 0;
-                } else {
-                    cur_n = claim_size(tail_items, seen);
-                    cur = atomicAdd(&ctrl->next_item, cur_n);
-                }
-                if (cached_tail * T > cur + cur_n + 4u * gridDim.x) {
-                    nxt_n = claim_size(cached_tail * T, cur + cur_n);
-                    nxt = atomicAdd(&ctrl->next_item, nxt_n);
-                }
-            }
-            const unsigned pos = cur / T;
-            const unsigned tile = cur - pos * T;
-            trace(p, kTrClaim, (int)pos, (int)tile, true);
-            bool avail = pos < cached_tail;
-            while (!avail) {
-                cached_tail = vload(&ctrl->q_tail);
-                if (pos < cached_tail) {
-                    avail = true;
+            if (chain_claim == kNone) chain_claim = atomicAdd(&ctrl->chain_next, 1u);
+            unsigned pos = kNone, tile = 0;
+            for (;;) {
+                if (chain_claim / T >= chain_rows) chain_rows = vload(&ctrl->chain_tail);
+                if (chain_claim / T < chain_rows) {
+                    pos = F + chain_claim / T;
+                    tile = chain_claim % T;
+                    chain_claim = kNone;
                     break;
                 }
+                if (!fresh_done) {
+                    const unsigned f = fresh_ahead != kNone ? fresh_ahead : atomicAdd(&ctrl->fresh_next, 1u);
+                    fresh_ahead = kNone;
+                    if (f < fresh_items) {
+                        pos = f / T;
+                        tile = f % T;
+                        break;
+                    }
+                    fresh_done = true;
+                }
+                // nothing to take yet: the run is complete once no group is outstanding
                 if (vload(&ctrl->outstanding) <= 0) {
                     __threadfence();
-                    cached_tail = vload(&ctrl->q_tail);  // final once nothing is outstanding
-                    avail = pos < cached_tail;
+                    chain_rows = vload(&ctrl->chain_tail);  // final once nothing is outstanding
+                    if (chain_claim / T < chain_rows) continue;
                     break;
                 }
                 if (globaltimer() > deadline) {
-                    atomicOr(p.status, kStatusTimeout);
+                    timed_out = true;
                     break;
                 }
-                __nanosleep(20);
+                __nanosleep(32);
             }
-            if (avail) {
-                if (pos != last_pos) {
-                    unsigned long long e = (pos == pre_pos) ? pre_val : vload(&p.queue[pos]);
-                    for (uint32_t k = 0; (long long)e < 0; ++k) {  // reserved, not yet published
-                        if ((k & 63u) == 63u && globaltimer() > deadline) break;
-                        e = vload(&p.queue[pos]);
-                    }
-                    if ((long long)e < 0) {
-                        atomicOr(p.status, kStatusTimeout);
-                        avail = false;
-                    } else {
-                        cur_entry = (int)(e >> 32);
-                        cur_row = (int)(e & 0x0FFFFFFFu);
-                        cur_mode = (int)((e >> 28) & 3u);
-                        last_pos = pos;
-                    }
+            if (pos != kNone) {
+                unsigned long long e = vload(&p.queue[pos]);
+                for (uint32_t k = 0; (long long)e < 0; ++k) {  // reserved, not yet published
+                    if ((k & 63u) == 63u && globaltimer() > deadline) break;
+                    e = vload(&p.queue[pos]);
                 }
-                if (avail) {
-                    item = make_int4(cur_row, (int)tile, cur_entry, cur_mode);
-                    ++cur;
-                    --cur_n;
+                if ((long long)e < 0) {
+                    timed_out = true;
+                } else {
+                    item = make_int4((int)(e & 0x0FFFFFFFu), (int)tile, (int)(e >> 32), (int)((e >> 28) & 3u));
                 }
             }
         }
+        if (timed_out) atomicOr(p.status, kStatusTimeout);
         if (!mbar_wait(&sm.empty[stage], phase ^ 1u, deadline)) {
             atomicOr(p.status, kStatusTimeout);
             return;
@@ -824,25 +715,18 @@ __device__ __noinline__ void producer_loop(const Params& p, Shared& sm, unsigned
         const unsigned char* src =
             reinterpret_cast<const unsigned char*>(p.logits) + ((long long)item.x * p.Vp + tbase) * ELT;
         mbar_arrive_expect_tx(&sm.full[stage], bytes);
-        bulk_load(stages + (size_t)stage * TILE_BYTES, src, bytes, &sm.full[stage], policy);
+        bulk_load(stages + (size_t)stage * kTileBytes, src, bytes, &sm.full[stage], policy);
         trace(p, kTrIssue, item.x, item.y, true);
-        prev_stage = stage;
-        prev_phase = phase;
         if (++stage == S) {
             stage = 0;
             phase ^= 1u;
         }
-        // prefetch the queue entry of the next item (its load overlaps the next stage wait)
-        const unsigned nidx = cur_n > 0 ? cur : (nxt_n > 0 ? nxt : 0xFFFFFFFFu);
-        const unsigned npos = nidx / T;
-        if (nidx != 0xFFFFFFFFu && npos != last_pos && npos != pre_pos && npos < cached_tail) {
-            pre_pos = npos;
-            pre_val = vload(&p.queue[npos]);
-        }
+        // claim a fresh item ahead while fresh ones remain (its atomic overlaps the next waits)
+        if (!fresh_done && fresh_ahead == kNone) fresh_ahead = atomicAdd(&ctrl->fresh_next, 1u);
     }
 }
 
-// ------------------------------------------------------------------ tile: exact slow top-32
+// ------------------------------------------------------------------ tile: candidate selection
 
 // Element k of the calling thread (tile layout), read from the stage; -inf past nv.
 template <int ELT>
@@ -856,94 +740,79 @@ __device__ __forceinline__ float stage_elem(const unsigned char* sp, bool full, 
     }
 }
 
-// Exact top-32 keys of a tile when a warp overflowed its candidate region
-// (massive ties): the 32nd largest value v is found by walking distinct values
-// down from the maximum; the result is every lane above v plus the smallest ids
-// equal to v.  Reads the stage element by element (no register copy).
+__device__ __forceinline__ int warp_excl_scan_i(int v, int lane, int* total) {
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += t;
+    }
+    *total = __shfl_sync(kFull, incl, 31);
+    return incl - v;
+}
+
+// Exact best 32 keys (value descending, id ascending) of the warp's share of a
+// tile, for the rare warp with more than 32 elements >= theta (large runs of
+// equal values): the 32nd largest value v is found by walking distinct values
+// down from the warp's maximum; the result is every element above v, then the
+// smallest ids equal to v, written to region[0..32) in no particular order.
+// Reads the stage element by element.
 template <int ELT>
-__device__ __forceinline__ void tile_top32_slow(const unsigned char* stage, bool full, int nv, long long tbase,
-                                                Shared& sm, unsigned long long* out) {
+__device__ __forceinline__ void warp_top32_exact(const unsigned char* sp, bool full, int nv, int tbase, int tid,
+                                              unsigned long long* region) {
     using L = TileLayout<ELT>;
-    constexpr int N = L::EPT;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    float v = __builtin_huge_valf();
-    int cnt_ge = 0;
+    const int lane = tid & 31;
+    float v = kPosInf;
     for (int it = 0; it < 33; ++it) {
         float loc = kNegInf;
-#pragma unroll 8
-        for (int k = 0; k < N; ++k) {
-            const float x = stage_elem<ELT>(stage, full, nv, k, tid);
+        for (int k = 0; k < L::EPT; ++k) {
+            const float x = stage_elem<ELT>(sp, full, nv, k, tid);
             loc = (x < v && x > loc) ? x : loc;
         }
-        const float vn = block_max_f(loc, sm, lane, warp);
-        if (!(vn > kNegInf)) break;  // no value left below v
+        const float vn = warp_max_f(loc);
+        if (!(vn > kNegInf)) break;  // nothing left below v
         v = vn;
         int c = 0;
-#pragma unroll 8
-        for (int k = 0; k < N; ++k) {
-            const float x = stage_elem<ELT>(stage, full, nv, k, tid);
+        for (int k = 0; k < L::EPT; ++k) {
+            const float x = stage_elem<ELT>(sp, full, nv, k, tid);
             c += (x >= v && x > kNegInf) ? 1 : 0;
         }
-        cnt_ge = block_sum_i(c, sm, lane, warp);
-        if (cnt_ge >= 32) break;
+        if (warp_sum_i(c) >= 32) break;
     }
-    int c = 0;
-#pragma unroll 8
-    for (int k = 0; k < N; ++k) {
-        const float x = stage_elem<ELT>(stage, full, nv, k, tid);
-        c += (x > v && x > kNegInf) ? 1 : 0;
+    int gt = 0;
+    for (int k = 0; k < L::EPT; ++k) {
+        const float x = stage_elem<ELT>(sp, full, nv, k, tid);
+        gt += (x > v && x > kNegInf) ? 1 : 0;
     }
-    const int cnt_gt = block_sum_i(c, sm, lane, warp);
-    const int take = (cnt_ge < 32 ? cnt_ge : 32);
-    const int need_eq = take - cnt_gt;
-    if (tid == 0) sm.red_i[0] = 0;
-    cbar();
-#pragma unroll 8
-    for (int k = 0; k < N; ++k) {
-        const float x = stage_elem<ELT>(stage, full, nv, k, tid);
-        if (x > v && x > kNegInf) {
-            const int pos = atomicAdd(&sm.red_i[0], 1);
-            if (pos < 32) sm.cand[pos] = make_key(x, (uint32_t)(tbase + tile_elem_id<ELT>(full, k, tid)));
-        }
-    }
-    cbar();
-    // lanes equal to v, in ascending id order, until need_eq are taken
-    const int NQ = full ? L::NCH : N;
-    const int SPQ = full ? L::EPV : 1;
     int got = 0;
-    for (int q = 0; q < NQ && got < need_eq; ++q) {
+    int pos = warp_excl_scan_i(gt, lane, &got);  // got < 32: v is the 32nd largest value
+    for (int k = 0; k < L::EPT; ++k) {
+        const float x = stage_elem<ELT>(sp, full, nv, k, tid);
+        if (x > v && x > kNegInf) region[pos++] = make_key(x, (uint32_t)(tbase + tile_elem_id<ELT>(full, k, tid)));
+    }
+    // elements equal to v in ascending id order: vector by vector (full tiles) or
+    // element by element (partial tiles), lanes in order within each
+    const int NQ = full ? L::NCH : L::EPT;
+    const int SPQ = full ? L::EPV : 1;
+    for (int q = 0; q < NQ && got < 32; ++q) {
         int mine = 0;
         for (int e = 0; e < SPQ; ++e) {
-            const float x = stage_elem<ELT>(stage, full, nv, q * SPQ + e, tid);
+            const float x = stage_elem<ELT>(sp, full, nv, q * SPQ + e, tid);
             mine += (x == v && x > kNegInf) ? 1 : 0;
         }
         int total = 0;
-        int before = block_excl_scan_i(mine, &total, sm, lane, warp);
+        int before = warp_excl_scan_i(mine, lane, &total);
         for (int e = 0; e < SPQ; ++e) {
             const int k = q * SPQ + e;
-            const float x = stage_elem<ELT>(stage, full, nv, k, tid);
+            const float x = stage_elem<ELT>(sp, full, nv, k, tid);
             if (x == v && x > kNegInf) {
-                const int pos = got + before;
-                if (pos < need_eq)
-                    sm.cand[cnt_gt + pos] = make_key(x, (uint32_t)(tbase + tile_elem_id<ELT>(full, k, tid)));
+                if (got + before < 32) region[got + before] = make_key(x, (uint32_t)(tbase + tile_elem_id<ELT>(full, k, tid)));
                 ++before;
             }
         }
         got += total;
     }
-    cbar();
-    const int n = take;
-    if (tid < n) {
-        const unsigned long long key = sm.cand[tid];
-        int rank = 0;
-        for (int u = 0; u < n; ++u) rank += sm.cand[u] > key ? 1 : 0;
-        out[rank] = key;
-    }
-    if (tid >= n && tid < 32) out[tid] = 0ull;
-    cbar();
 }
-
-// ------------------------------------------------------------------ compute warps
 
 // Warp-level top-4 extraction on ord32 values: returns the 4th largest
 // (knocking out one lane per round), and the largest through *mx.
@@ -959,257 +828,276 @@ __device__ __forceinline__ uint32_t warp_fourth_largest(uint32_t u, int lane, ui
     return r;
 }
 
-// Tile element id (within the tile) of the thread's first element equal to m.
+// Tile element id (within the tile) of the thread's first element equal to m,
+// in a partial tile.
 template <int ELT>
-__device__ __forceinline__ int first_equal(const unsigned char* sp, bool full, int nv, int tid, float m) {
-    TileRegs<ELT> y;
-    y.load(sp, full, nv, tid);
-    int kf = TileRegs<ELT>::kN - 1;
-#pragma unroll
-    for (int k = TileRegs<ELT>::kN - 1; k >= 0; --k) kf = (y.get(k) == m) ? k : kf;
-    return tile_elem_id<ELT>(full, kf, tid);
+__device__ __forceinline__ int first_equal_partial(const unsigned char* sp, int nv, int tid, float m) {
+    int kf = -1;
+    for (int k = 0; k < TileLayout<ELT>::EPT && kf < 0; ++k)
+        if (partial_elem<ELT>(sp, nv, k, tid) == m) kf = k;
+    return kf * kConsumerThreads + tid;
 }
 
-// Appends the keys of the thread's elements >= theta to its warp's region
-// (32 keys; the counter may pass 32, which signals an overflow).  Vectors whose
-// maximum is below theta are skipped after one packed compare.
+// Same for a full tile, from the vector maxima: the first vector whose maximum
+// equals m, then the first element of that vector equal to m.
 template <int ELT>
-__device__ __forceinline__ void append_candidates(const unsigned char* sp, int tid, float theta, int tbase,
-                                                  unsigned long long* region, int* count) {
-    constexpr int NCH = TileLayout<ELT>::NCH;
-    constexpr int EPV = TileLayout<ELT>::EPV;
-#pragma unroll 1
-    for (int c = 0; c < NCH; ++c) {
-        const uint4 v = lds128(sp + (size_t)(c * kConsumerThreads + tid) * 16);
-        float vmax;
-        if constexpr (ELT == 2) {
-            const uint32_t mm = bf16x2_max(bf16x2_max(v.x, v.y), bf16x2_max(v.z, v.w));
-            vmax = fmaxf(bf16_lo(mm), bf16_hi(mm));
-        } else {
-            vmax = fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)),
-                         fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
-        }
-        if (!(vmax >= theta)) continue;
-        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+__device__ __forceinline__ int first_equal_full(const unsigned char* sp, int tid, float m,
+                                                const uint32_t (&cm)[TileLayout<ELT>::NCH]) {
+    using L = TileLayout<ELT>;
+    int cf = L::NCH - 1;
 #pragma unroll
-        for (int e = 0; e < EPV; ++e) {
-            const float x = (ELT == 2) ? ((e & 1) ? bf16_hi(wv[e >> 1]) : bf16_lo(wv[e >> 1])) : __uint_as_float(wv[e]);
-            if (x >= theta && x > kNegInf) {
-                const int pos = atomic_add_shared(count, 1);
-                if (pos < 32) st_shared_u64(region + pos, make_key(x, (uint32_t)(tbase + (c * kConsumerThreads + tid) * EPV + e)));
+    for (int c = L::NCH - 1; c >= 0; --c) cf = (vec_max<ELT>(cm[c]) == m) ? c : cf;
+    const uint4 v = lds128(sp + (size_t)(cf * kConsumerThreads + tid) * 16);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    int ef = L::EPV - 1;
+#pragma unroll
+    for (int e = L::EPV - 1; e >= 0; --e) {
+        const float x = (ELT == 2) ? ((e & 1) ? bf16_hi(w[e >> 1]) : bf16_lo(w[e >> 1])) : __uint_as_float(w[e]);
+        ef = (x == m) ? e : ef;
+    }
+    return (cf * kConsumerThreads + tid) * L::EPV + ef;
+}
+
+// Writes the keys of the warp's elements >= theta (full tile) into its region
+// of 32 keys and returns the warp's count (above 32 means the region holds only
+// some of them).  Each lane re-reads only its vectors whose maximum reaches
+// theta and keeps its first two candidates in registers; ballots give the
+// slots.  A lane with more than two candidates (rare) writes the rest after a
+// warp scan.  Every lane of the warp calls it.
+template <int ELT>
+__device__ __forceinline__ int capture_candidates(const unsigned char* sp, int tid, float theta, int tbase,
+                                                  const uint32_t (&cm)[TileLayout<ELT>::NCH],
+                                                  unsigned long long* region) {
+    using L = TileLayout<ELT>;
+    const int lane = tid & 31;
+    unsigned pass = 0u;
+#pragma unroll
+    for (int c = 0; c < L::NCH; ++c) pass |= (vec_max<ELT>(cm[c]) >= theta ? 1u : 0u) << c;
+    int n = 0, k0 = 0, k1 = 0;     // k: the thread's element index c*EPV + e
+    float x0 = 0.0f, x1 = 0.0f;
+    for (unsigned q = pass; q; q &= q - 1u) {
+        const int c = __ffs(q) - 1;
+        const uint4 v = lds128(sp + (size_t)(c * kConsumerThreads + tid) * 16);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < L::EPV; ++e) {
+            const float x = (ELT == 2) ? ((e & 1) ? bf16_hi(w[e >> 1]) : bf16_lo(w[e >> 1])) : __uint_as_float(w[e]);
+            const bool take = x >= theta;
+            x1 = (take && n == 1) ? x : x1;
+            k1 = (take && n == 1) ? c * L::EPV + e : k1;
+            x0 = (take && n == 0) ? x : x0;
+            k0 = (take && n == 0) ? c * L::EPV + e : k0;
+            n += take ? 1 : 0;
+        }
+    }
+    const unsigned lt = (1u << lane) - 1u;
+    const unsigned b0 = __ballot_sync(kFull, n >= 1), b1 = __ballot_sync(kFull, n >= 2);
+    const int p0 = __popc(b0 & lt), p1 = __popc(b0) + __popc(b1 & lt);
+    if (n >= 1 && p0 < 32)
+        region[p0] = make_key(x0, (uint32_t)(tbase + ((k0 / L::EPV) * kConsumerThreads + tid) * L::EPV + k0 % L::EPV));
+    if (n >= 2 && p1 < 32)
+        region[p1] = make_key(x1, (uint32_t)(tbase + ((k1 / L::EPV) * kConsumerThreads + tid) * L::EPV + k1 % L::EPV));
+    const int total = (int)__reduce_add_sync(kFull, (unsigned)n);
+    if (__any_sync(kFull, n > 2)) {
+        // candidates beyond a lane's second: slots after all first and second ones
+        int unused = 0;
+        int pos = __popc(b0) + __popc(b1) + warp_excl_scan_i(n > 2 ? n - 2 : 0, lane, &unused);
+        if (n > 2) {
+            int j = 0;
+            for (unsigned q = pass; q && pos < 32; q &= q - 1u) {
+                const int c = __ffs(q) - 1;
+                const uint4 v = lds128(sp + (size_t)(c * kConsumerThreads + tid) * 16);
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int e = 0; e < L::EPV; ++e) {
+                    const float x =
+                        (ELT == 2) ? ((e & 1) ? bf16_hi(w[e >> 1]) : bf16_lo(w[e >> 1])) : __uint_as_float(w[e]);
+                    if (x >= theta) {
+                        if (j >= 2 && pos < 32) {
+                            region[pos] = make_key(x, (uint32_t)(tbase + (c * kConsumerThreads + tid) * L::EPV + e));
+                            ++pos;
+                        }
+                        ++j;
+                    }
+                }
             }
         }
     }
+    return total;
 }
 
+// Partial tile (the last of a row): the same, element by element.
 template <int ELT>
-__device__ __forceinline__ void append_candidates_partial(const unsigned char* sp, int nv, int tid, float theta,
-                                                          int tbase, unsigned long long* region, int* count) {
-#pragma unroll 4
-    for (int k = 0; k < TileLayout<ELT>::EPT; ++k) {
+__device__ __forceinline__ int capture_partial(const unsigned char* sp, int nv, int tid, float theta, int tbase,
+                                               unsigned long long* region) {
+    using L = TileLayout<ELT>;
+    const int lane = tid & 31;
+    int cnt = 0;
+    for (int k = 0; k < L::EPT; ++k) {
         const float x = stage_elem<ELT>(sp, false, nv, k, tid);
-        if (x >= theta && x > kNegInf) {
-            const int pos = atomic_add_shared(count, 1);
-            if (pos < 32) st_shared_u64(region + pos, make_key(x, (uint32_t)(tbase + k * kConsumerThreads + tid)));
-        }
+        cnt += (x >= theta && x > kNegInf) ? 1 : 0;
     }
+    int total = 0;
+    int pos = warp_excl_scan_i(cnt, lane, &total);
+    for (int k = 0; k < L::EPT && pos < 32; ++k) {
+        const float x = stage_elem<ELT>(sp, false, nv, k, tid);
+        if (x >= theta && x > kNegInf) region[pos++] = make_key(x, (uint32_t)(tbase + k * kConsumerThreads + tid));
+    }
+    return total;
 }
 
-// Top-32 (descending) of the candidate regions when they hold <= 64 keys in
-// total, by one warp: two 32-key bitonic sorts and a bitonic merge.
-__device__ __forceinline__ unsigned long long warp_top32_of_regions(const unsigned long long* cand, const int* wcnt,
-                                                                    int lane) {
-    unsigned long long a = 0ull, b = 0ull;
-    int before = 0;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) {
-        const int cw = wcnt[w];
-        const int ia = lane - before, ib = lane + 32 - before;
-        if (ia >= 0 && ia < cw) a = cand[w * 32 + ia];
-        if (ib >= 0 && ib < cw) b = cand[w * 32 + ib];
-        before += cw;
-    }
-    a = warp_sort_desc(a, lane);
-    b = warp_sort_desc(b, lane);
+__device__ __forceinline__ unsigned long long merge_lists(unsigned long long a, unsigned long long b, int lane) {
     const unsigned long long rev = __shfl_sync(kFull, b, 31 - lane);
     return warp_bitonic_clean_desc(rev > a ? rev : a, lane);
 }
 
-template <int ELT>
-__device__ __noinline__ void record_block(const Params& p, Shared& sm, int row, int entry, int chosen);
-
-// Builds the records the merge warp queued, up to the snapshot `upto` (the
-// same value in every compute thread).  Returns the new head.
-template <int ELT>
-__device__ __forceinline__ unsigned run_tasks(const Params& p, Shared& sm, unsigned head, unsigned upto) {
-    cbar();  // the tile's readers of the candidate buffer are done (it aliases the task lists)
-    while (head != upto) {
-        const int4 t = sm.task[head % kTasks];
-        ++head;
-        record_block<ELT>(p, sm, t.x, t.z, t.y);
+// Best 32 keys (descending, lane i holds the i-th) of a tile's candidate
+// regions: the keys are taken 64 at a time in region order, each half sorted
+// (bitonic), the halves and the running result merged.
+__device__ __forceinline__ unsigned long long slot_top32(const ResultSlot& R, int lane) {
+    int cw[kWarps];
+    int n = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        cw[w] = R.wcnt[w];
+        n += cw[w];
     }
-    if (threadIdx.x == 0) vstore(&sm.task_head, head);
-    return head;
+    unsigned long long r = 0ull;
+    for (int q0 = 0; q0 < n; q0 += 64) {
+        unsigned long long a = 0ull, b = 0ull;
+        int before = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            const int ia = q0 + lane - before, ib = ia + 32;
+            if (ia >= 0 && ia < cw[w]) a = R.cand[w][ia];
+            if (ib >= 0 && ib < cw[w]) b = R.cand[w][ib];
+            before += cw[w];
+        }
+        a = warp_sort_desc(a, lane);
+        b = warp_sort_desc(b, lane);
+        const unsigned long long c = merge_lists(a, b, lane);
+        r = q0 == 0 ? c : merge_lists(r, c, lane);
+    }
+    return r;
 }
 
+// ------------------------------------------------------------------ compute warps
+//
+// Each compute warp reduces its share of every tile on its own and hands its
+// partial results to the merge warp through the ring: the warps never wait for
+// one another, except on natural-alternative tiles, where the 8 warp
+// thresholds are exchanged (a bounded mbarrier wait) before the candidates are
+// taken.
 template <int ELT>
 __device__ void compute_loop(const Params& p, Shared& sm, unsigned char* stages, unsigned long long t0) {
     constexpr int S = StageCfg<ELT>::kStages;
-    constexpr int TILE_BYTES = kTileBytes;
     constexpr int kTE = tile_elems<ELT>();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const unsigned long long deadline = t0 + p.timeout_ns;
     const int V = (int)p.V;
     int stage = 0, rslot = 0;
-    uint32_t phase = 0, rphase = 0;
-    unsigned task_head = 0;
-    for (int seq = 0;; ++seq) {
-        const int par = seq & 1;
+    uint32_t phase = 0, rphase = 0, tphase = 0;  // tphase bit r: phase of rtheta[r] and rcand[r]
+    unsigned tcount = 0;                           // tiles seen (picks the selecting warp)
+    for (;;) {
         bool late = !mbar_wait(&sm.full[stage], phase, deadline);
         const int4 info = sm.info[stage];
-        const bool done = info.z < 0;
         late = late || !mbar_wait(&sm.rempty[rslot], rphase ^ 1u, deadline);
-        late = __any_sync(kFull, late);  // warp-uniform before any warp collective
-        const unsigned char* sp = stages + (size_t)stage * TILE_BYTES;
+        if (__any_sync(kFull, late)) {
+            if (lane == 0) atomicOr(p.status, kStatusTimeout);
+            return;
+        }
+        ResultSlot& R = sm.res[rslot];
+        if (info.z < 0) {
+            // no more tiles: the merge warp finishes once every compute warp is here
+            if (tid == 0) R.info = info;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.rfull[rslot]);
+            return;
+        }
+        const unsigned char* sp = stages + (size_t)stage * kTileBytes;
         const int tile = info.y, mode = info.w;
         const int tbase = tile * kTE;
         const int rem = V - tbase;
         const int nv = rem < kTE ? (rem > 0 ? rem : 0) : kTE;
         const bool full = nv == kTE;
-        ResultSlot& R = sm.res[rslot];
-        const bool work = !late && !done;
-        trace(p, kTrTileStart, info.x, tile, tid == 0 && work);
+        trace(p, kTrTileStart, info.x, tile, tid == 0);
 
-        float m = kNegInf, s = 0.0f;
-        if (work) {
-            // two passes over the stage: max, then sum exp(x - m); the tile is never
-            // held in registers
-            m = full ? stage_max<ELT>(sp, tid) : partial_max<ELT>(sp, nv, tid);
-            if (mode != kModeArgmax && m > kNegInf) {
-                // exp(x - m) = 2^(x*log2e - mb - mb_lo): mb_lo, the rounding residual
-                // of m*log2e, is applied once, so large |m| costs no accuracy
-                const float mb = m * kLog2e;
-                const float mb_lo = fmaf(m, kLog2e, -mb);
-                s = (full ? stage_expsum<ELT>(sp, tid, mb) : partial_expsum<ELT>(sp, nv, tid, mb)) * ex2(-mb_lo);
-            }
-        }
+        // pass 1: maxima (per vector for a full tile)
+        uint32_t cm[TileLayout<ELT>::NCH];
+        const float m = full ? stage_max<ELT>(sp, tid, cm) : partial_max<ELT>(sp, nv, tid);
         const uint32_t om = ord32(__fadd_rn(m, 0.0f));
-        if (work) {
-            uint32_t omx;
-            if (mode == kModeNatural) {
-                // theta: min over warps of the warp's 4th largest thread maximum;
-                // at least 32 lanes of the tile are >= theta
-                const uint32_t o4 = warp_fourth_largest(om, lane, &omx);
-                if (lane == 0) sm.wTheta[par][warp] = unord32(o4);
-            } else {
-                omx = __reduce_max_sync(kFull, om);
-                // argmax key: smallest id among the lanes holding the warp maximum
-                uint32_t id = 0xFFFFFFFFu;
-                if (om == omx && m > kNegInf) id = (uint32_t)(tbase + first_equal<ELT>(sp, full, nv, tid, m));
-                const uint32_t idmin = __reduce_min_sync(kFull, id);
-                if (lane == 0) sm.wkey[par][warp] = ((unsigned long long)omx << 32) | (unsigned long long)(~idmin);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sm.empty[stage]);  // no more reads of this stage
-            }
-            const float Mw = unord32(omx);
-            const float sc = (m > kNegInf && mode != kModeArgmax) ? s * ex2((m - Mw) * kLog2e) : 0.0f;
-            const float sw = warp_sum_f(sc);
-            if (lane == 0) {
-                sm.wM[par][warp] = Mw;
-                sm.wS[par][warp] = sw;
-            }
-        }
-        if (lane == 0) sm.wcnt[par][warp] = 0;
-        if (tid == 0) sm.task_snap[par] = vload(&sm.task_tail);
-        // B1: partials visible; every compute thread leaves together on timeout or end
-        if (cbar_or(late || done)) {
-            if (late) {
-                if (tid == 0) atomicOr(p.status, kStatusTimeout);
-            } else {
-                // every record this CTA owes is queued by now (nothing is outstanding)
-                task_head = run_tasks<ELT>(p, sm, task_head, sm.task_snap[par]);
-                if (tid == 0) R.info = info;  // tells the merge warp to finish
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sm.rfull[rslot]);
-            }
-            return;
-        }
-        const unsigned task_snap = sm.task_snap[par];
-        trace(p, kTrTileB1, info.x, tile, tid == 0);
-        float M = sm.wM[par][0];
-#pragma unroll
-        for (int w = 1; w < 8; ++w) M = fmaxf(M, sm.wM[par][w]);
+        uint32_t omx;
         if (mode == kModeNatural) {
-            float theta = sm.wTheta[par][0];
-#pragma unroll
-            for (int w = 1; w < 8; ++w) theta = fminf(theta, sm.wTheta[par][w]);
-            // candidates: each warp packs its own into cand[32*warp ..] (no atomics)
-            if (m >= theta && m > kNegInf) {
-                if (full) {
-                    append_candidates<ELT>(sp, tid, theta, tbase, sm.cand + warp * 32, &sm.wcnt[par][warp]);
-                } else {
-                    append_candidates_partial<ELT>(sp, nv, tid, theta, tbase, sm.cand + warp * 32,
-                                                   &sm.wcnt[par][warp]);
-                }
-            }
-            cbar();  // B2: candidates complete
-            int n = 0, over = 0;
-#pragma unroll
-            for (int w = 0; w < 8; ++w) {
-                const int cw = sm.wcnt[par][w];
-                n += cw;
-                over |= cw > 32;
-            }
-            trace(p, kTrTileB2, info.x, n, tid == 0);
-            if (!over) {
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sm.empty[stage]);
-                if (n <= 64) {
-                    // one warp (rotating with the tile) sorts the <= 64 candidates
-                    if (warp == (seq & 7)) R.keys[lane] = warp_top32_of_regions(sm.cand, sm.wcnt[par], lane);
-                } else if (lane < sm.wcnt[par][warp]) {
-                    // thread 32w+j holds candidate j of warp w; rank = # larger keys
-                    const unsigned long long key = sm.cand[tid];
-                    int rank = 0;
-#pragma unroll 1
-                    for (int w = 0; w < 8; ++w) {
-                        const int cw = sm.wcnt[par][w];
-                        const unsigned long long* cp = sm.cand + w * 32;
-#pragma unroll 4
-                        for (int u = 0; u < cw; ++u) rank += cp[u] > key ? 1 : 0;
-                    }
-                    if (rank < kKeysPerTile) R.keys[rank] = key;
-                }
-            } else {
-                tile_top32_slow<ELT>(sp, full, nv, tbase, sm, R.keys);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sm.empty[stage]);
-            }
-        } else if (tid == 0) {
-            unsigned long long k0 = sm.wkey[par][0];
-#pragma unroll
-            for (int w = 1; w < 8; ++w) k0 = sm.wkey[par][w] > k0 ? sm.wkey[par][w] : k0;
-            R.keys[0] = k0;
-        }
-        if (warp == 0) {
-            float St = 0.0f;
-            if (mode != kModeArgmax && lane < 8) {
-                const float mw = sm.wM[par][lane];
-                St = (mw > kNegInf) ? sm.wS[par][lane] * ex2((mw - M) * kLog2e) : 0.0f;
-            }
-            St += __shfl_xor_sync(kFull, St, 4);
-            St += __shfl_xor_sync(kFull, St, 2);
-            St += __shfl_xor_sync(kFull, St, 1);
+            // theta = min over warps of the warp's 4th largest thread maximum: at
+            // least 32 elements of the tile are >= theta, so its best 32 are among
+            // them.  The warp publishes its part now and reads the others' after
+            // its exp pass, so the exchange costs no wait in the common case.
+            const uint32_t o4 = warp_fourth_largest(om, lane, &omx);
             if (lane == 0) {
-                R.info = info;
-                R.M = M;
-                R.S = St;
+                R.wTheta[warp] = unord32(o4);
+                mbar_arrive(&sm.rtheta[rslot]);
             }
+        } else {
+            omx = __reduce_max_sync(kFull, om);
+            // argmax key: smallest id among the lanes holding the warp maximum
+            uint32_t id = 0xFFFFFFFFu;
+            if (om == omx && m > kNegInf)
+                id = (uint32_t)(tbase + (full ? first_equal_full<ELT>(sp, tid, m, cm)
+                                              : first_equal_partial<ELT>(sp, nv, tid, m)));
+            const uint32_t idmin = __reduce_min_sync(kFull, id);
+            if (lane == 0) R.wkey[warp] = ((unsigned long long)omx << 32) | (unsigned long long)(~idmin);
+        }
+        // pass 2: sum exp(x - m) = 2^(x*log2e - mb - mb_lo): mb_lo, the rounding
+        // residual of m*log2e, is applied once, so large |m| costs no accuracy
+        float s = 0.0f;
+        if (mode != kModeArgmax && m > kNegInf) {
+            const float mb = m * kLog2e;
+            const float mb_lo = fmaf(m, kLog2e, -mb);
+            s = (full ? stage_expsum<ELT>(sp, tid, mb) : partial_expsum<ELT>(sp, nv, tid, mb)) * ex2(-mb_lo);
+        }
+        if (mode == kModeNatural) {
+            const uint32_t tpar = (tphase >> rslot) & 1u;
+            tphase ^= 1u << rslot;
+            if (__any_sync(kFull, !mbar_wait(&sm.rtheta[rslot], tpar, deadline))) {
+                if (lane == 0) atomicOr(p.status, kStatusTimeout);
+                return;
+            }
+            float theta = R.wTheta[0];
+#pragma unroll
+            for (int w = 1; w < kWarps; ++w) theta = fminf(theta, R.wTheta[w]);
+            int cw = full ? capture_candidates<ELT>(sp, tid, m > kNegInf ? theta : kPosInf, tbase, cm, R.cand[warp])
+                          : capture_partial<ELT>(sp, nv, tid, theta, tbase, R.cand[warp]);
+            if (cw > 32) {
+                warp_top32_exact<ELT>(sp, full, nv, tbase, tid, R.cand[warp]);
+                cw = 32;
+            }
+            if (lane == 0) R.wcnt[warp] = cw;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.rcand[rslot]);
+            if (warp == (int)(tcount & (kWarps - 1))) {
+                // this tile's selecting warp (rotating): the best 32 of all warps' candidates
+                if (__any_sync(kFull, !mbar_wait(&sm.rcand[rslot], tpar, deadline))) {
+                    if (lane == 0) atomicOr(p.status, kStatusTimeout);
+                    return;
+                }
+                R.keys[lane] = slot_top32(R, lane);
+            }
+        }
+        ++tcount;
+        const float Mw = unord32(omx);
+        const float sc = (m > kNegInf && mode != kModeArgmax) ? s * ex2((m - Mw) * kLog2e) : 0.0f;
+        const float sw = warp_sum_f(sc);
+        if (lane == 0) {
+            R.wM[warp] = Mw;
+            R.wS[warp] = sw;
+            if (warp == 0) R.info = info;
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.rfull[rslot]);
+        if (lane == 0) {
+            mbar_arrive(&sm.empty[stage]);   // no more reads of this stage by this warp
+            mbar_arrive(&sm.rfull[rslot]);   // this warp's results are in the slot
+        }
         trace(p, kTrTileEnd, info.x, tile, tid == 0);
-        if (task_snap != task_head) task_head = run_tasks<ELT>(p, sm, task_head, task_snap);
         if (++stage == S) {
             stage = 0;
             phase ^= 1u;
@@ -1223,26 +1111,21 @@ __device__ void compute_loop(const Params& p, Shared& sm, unsigned char* stages,
 
 // ------------------------------------------------------------------ merge warp
 
-__device__ __forceinline__ unsigned long long merge_lists(unsigned long long a, unsigned long long b, int lane) {
-    const unsigned long long rev = __shfl_sync(kFull, b, 31 - lane);
-    return warp_bitonic_clean_desc(rev > a ? rev : a, lane);
-}
-
-// Acceptance decision of a row whose tiles are all published (lane 0 of the
-// merge warp): argmax = the row's best key; on acceptance the next row of the
-// group is appended to the queue.  Returns the chosen token; *terminal is set
-// when the group ends here (the caller then retires the row from
-// ctrl->outstanding, after queueing its record).
-__device__ __noinline__ int decide_row(const Params& p, int row, int entry, bool* requested, bool* terminal) {
+// Acceptance decision of a row whose tiles are all published (one lane of the
+// merge warp; d = the group's descriptor and draft = the row's draft token,
+// loaded by the caller): argmax = the row's best key; on acceptance the next row of the
+// group is appended to the chained queue, else the group ends (*terminal).  A
+// requesting row is flagged for the record kernel.  Returns the chosen token.
+__device__ __noinline__ int decide_row(const Params& p, int row, int entry, int4 d, int draft, unsigned fresh_rows,
+                                      bool* terminal) {
     const int g = entry >> 4, j = entry & 15;
-    const int4 d = __ldcg(&p.gdesc[g]);
-    const int r0 = d.x, k = d.y & 0xFF, req = (d.y >> 13) & 1, samp = d.w;
     const unsigned long long bk = __ldcg(&p.row_best[row]);
+    const int r0 = d.x, k = d.y & 0xFF, req = (d.y >> 13) & 1, samp = d.w;
     const uint32_t amax = key_id(bk);
     const int chosen = (k == 0 && samp >= 0) ? samp : (int)amax;
-    const bool accept = (j < k) && (__ldg(&p.drafts[row]) == (int)amax);
+    const bool accept = (j < k) && (draft == (int)amax);
     if (accept) {
-        const unsigned pos = atomicAdd(&p.ctrl->q_tail, 1u);
+        const unsigned pos = fresh_rows + atomicAdd(&p.ctrl->chain_tail, 1u);
         vstore(&p.queue[pos], queue_entry((g << 4) | (j + 1), row + 1, (d.y >> 8) & 3));
     }
     p.emitted[row] = chosen;
@@ -1250,15 +1133,161 @@ __device__ __noinline__ int decide_row(const Params& p, int row, int entry, bool
         p.accepted[g] = j;
         for (int jj = j + 1; jj <= k; ++jj) p.emitted[r0 + jj] = -1;
     }
-    if (req && chosen >= p.V) atomicOr(p.status, kStatusBadToken);
-    *requested = req != 0;
+    if (req) {
+        if (chosen >= p.V) atomicOr(p.status, kStatusBadToken);
+        p.rec_tasks[row] = make_int4(chosen, entry, 1, 0);  // built by the record kernel
+    }
     *terminal = !accept;
     trace(p, kTrDecision, row, accept ? 1 : 0, true);
     return chosen;
 }
 
+// The merge warp combines the compute warps' partial results of each tile
+// (max, exp-sum, argmax key, or the best 32 of the candidates), publishes them
+// to global memory and counts each row's finished tiles; for a row's last
+// tile it takes the acceptance decision at once and, for a requesting row,
+// appends a record task for the record kernel.  Results are taken in batches
+// (the slots already written, up to the ring size): one fence, then one
+// done-counter atomic per tile from separate lanes.
+template <int ELT>
+__device__ __noinline__ void merge_loop(const Params& p, Shared& sm, unsigned long long t0) {
+    const int lane = threadIdx.x & 31;
+    const unsigned long long deadline = t0 + p.timeout_ns;
+    const int T = p.T;
+    const unsigned fresh_rows = vload(&p.ctrl->fresh_rows);
+    int rslot = 0;
+    uint32_t rphase = 0;
+    for (;;) {
+        if (!mbar_wait(&sm.rfull[rslot], rphase, deadline)) {
+            if (lane == 0) atomicOr(p.status, kStatusTimeout);
+            return;
+        }
+        int n = 0;
+        bool finished = false;
+        trace(p, kTrMergeStart, 0, rslot, lane == 0);
+        do {
+            const ResultSlot& R = sm.res[rslot];
+            const int4 info = R.info;
+            if (info.z < 0) {
+                finished = true;
+                break;
+            }
+            const int mode = info.w;
+            // tile (max, sum exp(x - max)) from the 8 warps' partials
+            // lanes 0..7 hold the warps' partials; xor steps 4, 2, 1 stay within them
+            const int wl = lane & (kWarps - 1);
+            const float mw = R.wM[wl];
+            float M = mw;
+            M = fmaxf(M, __shfl_xor_sync(kFull, M, 4));
+            M = fmaxf(M, __shfl_xor_sync(kFull, M, 2));
+            M = fmaxf(M, __shfl_xor_sync(kFull, M, 1));
+            float St = (mode != kModeArgmax && mw > kNegInf) ? R.wS[wl] * ex2((mw - M) * kLog2e) : 0.0f;
+            St += __shfl_xor_sync(kFull, St, 4);
+            St += __shfl_xor_sync(kFull, St, 2);
+            St += __shfl_xor_sync(kFull, St, 1);
+            unsigned long long key;
+            if (mode == kModeNatural) {
+                key = R.keys[lane];
+            } else {
+                key = R.wkey[wl];
+#pragma unroll
+                for (int o = 4; o > 0; o >>= 1) {
+                    const unsigned long long k2 = __shfl_xor_sync(kFull, key, o);
+                    key = k2 > key ? k2 : key;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&sm.rempty[rslot]);
+                sm.batch[n] = make_int2(info.x, info.z);
+            }
+            const long long slot = (long long)info.x * T + info.y;
+            if (mode == kModeNatural || lane == 0) p.part_keys[slot * kKeysPerTile + lane] = key;
+            if (lane == 0) {
+                p.part_ms[slot] = make_float2(M, St);
+                atomicMax(&p.row_best[info.x], key);
+            }
+            trace(p, kTrPublish, info.x, info.y, lane == 0);
+            ++n;
+            if (++rslot == kRing) {
+                rslot = 0;
+                rphase ^= 1u;
+            }
+        } while (n < kRing && mbar_test_wait(&sm.rfull[rslot], rphase));
+        // one acquire-release increment per tile (separate lanes): the tile's results
+        // are visible to whoever counts the row's last tile
+        __syncwarp();
+        int last = 0;
+        int2 b = make_int2(0, 0);
+        int4 gd = make_int4(0, 0, 0, 0);
+        int draft = -1;
+        if (lane < n) {
+            b = sm.batch[lane];
+            last = atomic_add_acq_rel(&p.done[b.x], 1) == T - 1;
+            gd = __ldcg(&p.gdesc[b.y >> 4]);  // for the decision, loaded while the count is in flight
+            draft = __ldg(&p.drafts[b.x]);
+        }
+        unsigned lastmask = __ballot_sync(kFull, last);
+        trace(p, kTrMergeEnd, n, __popc(lastmask), lane == 0);
+        while (lastmask) {
+            const int i = __ffs(lastmask) - 1;
+            lastmask &= lastmask - 1;
+            if (lane == i) {
+                bool terminal = false;
+                decide_row(p, b.x, b.y, gd, draft, fresh_rows, &terminal);
+                if (terminal) atomicSub(&p.ctrl->outstanding, 1);
+            }
+        }
+        __syncwarp();
+        if (finished) return;
+    }
+}
+
+template <int ELT>
+__global__ void __launch_bounds__(kThreads, StageCfg<ELT>::kMinBlocks) lp_stream_kernel(Params p) {
+    constexpr int S = StageCfg<ELT>::kStages;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    unsigned char* stages = smem_raw;
+    Shared& sm = *reinterpret_cast<Shared*>(smem_raw + (size_t)S * kTileBytes);
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&sm.full[s], 1);
+            mbar_init(&sm.empty[s], kWarps);
+        }
+        for (int s = 0; s < kRing; ++s) {
+            mbar_init(&sm.rfull[s], kWarps);
+            mbar_init(&sm.rempty[s], 1);
+            mbar_init(&sm.rtheta[s], kWarps);
+            mbar_init(&sm.rcand[s], kWarps);
+        }
+        g_trace_n[0] = g_trace_n[1] = g_trace_n[2] = 0u;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    __syncthreads();
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // the record kernel may be scheduled now; it waits for this grid to complete
+    asm volatile("griddepcontrol.launch_dependents;");
+    if (vload(&p.ctrl->abort) != 0u) return;
+    const unsigned long long t0 = globaltimer();
+    trace(p, kTrKernel, 0, 0, tid == 0);
+    const int warp = tid >> 5;
+    if (warp == kWarps) {
+        if (tid == kConsumerThreads) producer_loop<ELT>(p, sm, stages, t0);
+        return;
+    }
+    if (warp == kWarps + 1) {
+        merge_loop<ELT>(p, sm, t0);
+        return;
+    }
+    compute_loop<ELT>(p, sm, stages, t0);
+}
+
+// ------------------------------------------------------------------ records
+
 // Natural alternatives from the row's raw top-32 keys r (one per lane, descending),
-// written into sm.rec by one warp.  Exact for the (logprob desc, id asc) order:
+// written into rec by one warp.  Exact for the (logprob desc, id asc) order:
 // see the note at the top of the file.
 template <int ELT>
 __device__ __noinline__ void natural_from_top32(const Params& p, int* rec, int row, long long base, int kc,
@@ -1334,86 +1363,6 @@ __device__ __noinline__ void natural_from_top32(const Params& p, int* rec, int r
     }
 }
 
-// Record of a requested, emitted row (whole merge warp): lse, the chosen pair,
-// the natural alternatives or the explicit ids, written as 258 words.
-template <int ELT>
-__device__ __noinline__ void record_row(const Params& p, Shared& sm, int row, int entry, int chosen) {
-    const int lane = threadIdx.x & 31;
-    const int g = entry >> 4;
-    const int4 d = __ldcg(&p.gdesc[g]);
-    const int mode = (d.y >> 8) & 3, ids = (d.y >> 12) & 1, kc = d.z;
-    const int T = p.T;
-    const long long base = (long long)row * T;
-    trace(p, kTrMergeStart, row, 0, lane == 0);
-
-    // lse = M + log(sum_t s_t exp(m_t - M)); the per-tile terms are combined in
-    // FP64 and the result is rounded once to FP32
-    float tm = kNegInf;
-    for (int t = lane; t < T; t += 32) tm = fmaxf(tm, __ldcg(&p.part_ms[base + t]).x);
-    const float M = warp_max_f(tm);
-    double ps = 0.0;
-    for (int t = lane; t < T; t += 32) {
-        const float2 ms = __ldcg(&p.part_ms[base + t]);
-        ps += (double)ms.y * exp((double)ms.x - (double)M);
-    }
-    const double S = warp_sum_d(ps);
-    const float lse = __double2float_rn((double)M + log(S));
-
-    for (int w = lane; w < kRecordWords; w += 32) sm.mrec[w] = (w >= 2 && (w & 1) == 0) ? -1 : (int)kUnusedBits;
-    __syncwarp();
-    if (lane == 0) {
-        sm.mrec[0] = chosen;
-        sm.mrec[1] = (chosen >= 0 && chosen < p.V) ? (int)__float_as_uint(logprob(load_logit<ELT>(p, row, chosen), lse))
-                                                  : (int)kUnusedBits;
-        if (p.lse_out) p.lse_out[row] = lse;
-    }
-    if (ids) {
-        int id[kMaxIds / 32];
-        float xv[kMaxIds / 32];
-#pragma unroll
-        for (int q = 0; q < kMaxIds / 32; ++q) {
-            const int i = lane + 32 * q;
-            id[q] = i < kc ? __ldg(&p.token_ids[(long long)g * kMaxIds + i]) : -1;
-        }
-#pragma unroll
-        for (int q = 0; q < kMaxIds / 32; ++q)
-            xv[q] = (id[q] >= 0 && id[q] < p.V) ? load_logit<ELT>(p, row, id[q]) : 0.0f;
-#pragma unroll
-        for (int q = 0; q < kMaxIds / 32; ++q) {
-            const int i = lane + 32 * q;
-            if (i < kc) {
-                int bits = (int)kUnusedBits;
-                if (id[q] >= 0 && id[q] < p.V) {
-                    bits = (int)__float_as_uint(logprob(xv[q], lse));
-                } else {
-                    atomicOr(p.status, kStatusBadId);
-                }
-                sm.mrec[2 + 2 * i] = id[q];
-                sm.mrec[3 + 2 * i] = bits;
-            }
-        }
-    } else if (mode == kModeNatural && kc > 0) {
-        // global raw top-32: tiles merged four at a time
-        const unsigned long long* kp = p.part_keys + base * kKeysPerTile + lane;
-        unsigned long long r = 0;
-        for (int t0 = 0; t0 < T; t0 += 4) {
-            const unsigned long long a0 = __ldcg(kp + (long long)t0 * kKeysPerTile);
-            const unsigned long long a1 = (t0 + 1 < T) ? __ldcg(kp + (long long)(t0 + 1) * kKeysPerTile) : 0ull;
-            const unsigned long long a2 = (t0 + 2 < T) ? __ldcg(kp + (long long)(t0 + 2) * kKeysPerTile) : 0ull;
-            const unsigned long long a3 = (t0 + 3 < T) ? __ldcg(kp + (long long)(t0 + 3) * kKeysPerTile) : 0ull;
-            const unsigned long long b0 = merge_lists(a0, a1, lane);
-            const unsigned long long b1 = merge_lists(a2, a3, lane);
-            r = merge_lists(r, merge_lists(b0, b1, lane), lane);
-        }
-        natural_from_top32<ELT>(p, sm.mrec, row, base, kc, lse, r);
-    }
-    __syncwarp();
-    int* out = p.records + (long long)row * kRecordWords;
-    for (int w = lane; w < kRecordWords; w += 32) out[w] = sm.mrec[w];
-    __syncwarp();
-    trace(p, kTrMergeEnd, row, 1, lane == 0);
-}
-
 // Merges two (max, sum exp(x - max)) pairs.
 __device__ __forceinline__ void ms_merge(float& m, float& s, float m2, float s2) {
     const float M = fmaxf(m, m2);
@@ -1422,13 +1371,12 @@ __device__ __forceinline__ void ms_merge(float& m, float& s, float m2, float s2)
     m = M;
 }
 
-// Record of a requested, emitted row built by the 256 compute threads (a task
-// the merge warp queued after the acceptance decision): lse from the tile
-// partials, the chosen pair, then the explicit-id gather or the natural
-// alternatives (each warp merges every 8th tile list, warp 0 merges the 8).
-// Every global load is issued before the first barrier.
+// Record of a requested, emitted row, built by one CTA of 256 threads: lse from
+// the tile partials, the chosen pair, then the explicit-id gather or the
+// natural alternatives (each warp merges every 8th tile list, warp 0 merges
+// the 8).  Every global load is issued before the first barrier.
 template <int ELT>
-__device__ __noinline__ void record_block(const Params& p, Shared& sm, int row, int entry, int chosen) {
+__device__ __noinline__ void record_block(const Params& p, RecShared& sm, int row, int entry, int chosen) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = entry >> 4;
     const int4 d = __ldcg(&p.gdesc[g]);
@@ -1436,7 +1384,6 @@ __device__ __noinline__ void record_block(const Params& p, Shared& sm, int row, 
     const int T = p.T;
     const long long base = (long long)row * T;
     const bool natural = !ids && mode == kModeNatural && kc > 0;
-    trace(p, kTrMergeStart, row, 0, tid == 0);
     for (int w = tid; w < kRecordWords; w += kConsumerThreads)
         sm.rec[w] = (w >= 2 && (w & 1) == 0) ? -1 : (int)kUnusedBits;
     // loads: tile partials, the chosen logit, explicit-id logits, tile key lists
@@ -1513,144 +1460,19 @@ __device__ __noinline__ void record_block(const Params& p, Shared& sm, int row, 
     int* out = p.records + (long long)row * kRecordWords;
     for (int w = tid; w < kRecordWords; w += kConsumerThreads) out[w] = sm.rec[w];
     cbar();
-    trace(p, kTrMergeEnd, row, 1, tid == 0);
 }
 
-// The merge warp publishes tile results to global memory and counts each
-// row's finished tiles; for a row's last tile it takes the acceptance decision
-// at once and queues the row's record as a task for the compute warps (or,
-// when the CTA's task ring is full, writes it itself).  Results are taken in
-// batches (the slots already written, up to the ring size): one fence, then
-// one done-counter atomic per tile from separate lanes.
+// Builds the records of the rows the stream kernel flagged (launched after it
+// with programmatic dependent launch: it waits for the stream grid to finish).
 template <int ELT>
-__device__ __noinline__ void merge_loop(const Params& p, Shared& sm, unsigned long long t0) {
-    const int lane = threadIdx.x & 31;
-    const unsigned long long deadline = t0 + p.timeout_ns;
-    const int T = p.T;
-    int rslot = 0;
-    uint32_t rphase = 0;
-    for (;;) {
-        if (!mbar_wait(&sm.rfull[rslot], rphase, deadline)) {
-            if (lane == 0) atomicOr(p.status, kStatusTimeout);
-            return;
-        }
-        int n = 0;
-        bool finished = false;
-        do {
-            const ResultSlot& R = sm.res[rslot];
-            const int4 info = R.info;
-            if (info.z < 0) {
-                finished = true;
-                break;
-            }
-            const int mode = info.w;
-            const unsigned long long key = (mode == kModeNatural || lane == 0) ? R.keys[lane] : 0ull;
-            const float Mt = R.M, St = R.S;
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&sm.rempty[rslot]);
-                sm.batch[n] = make_int2(info.x, info.z);
-            }
-            const long long slot = (long long)info.x * T + info.y;
-            if (mode == kModeNatural || lane == 0) p.part_keys[slot * kKeysPerTile + lane] = key;
-            if (lane == 0) {
-                p.part_ms[slot] = make_float2(Mt, St);
-                atomicMax(&p.row_best[info.x], key);
-            }
-            trace(p, kTrPublish, info.x, info.y, lane == 0);
-            ++n;
-            if (++rslot == kRing) {
-                rslot = 0;
-                rphase ^= 1u;
-            }
-        } while (n < kRing && mbar_test_wait(&sm.rfull[rslot], rphase));
-        __threadfence();
-        __syncwarp();
-        int last = 0;
-        int2 b = make_int2(0, 0);
-        if (lane < n) {
-            b = sm.batch[lane];
-            last = atomicAdd(&p.done[b.x], 1) == T - 1;
-        }
-        unsigned lastmask = __ballot_sync(kFull, last);
-        if (lastmask) __threadfence();
-        while (lastmask) {
-            const int i = __ffs(lastmask) - 1;
-            lastmask &= lastmask - 1;
-            int4 task = make_int4(0, 0, -1, 0);
-            int own = 0;  // 1: the task ring is full, the merge warp writes the record
-            if (lane == 0) {
-                const int2 bi = sm.batch[i];
-                bool req = false, terminal = false;
-                const int chosen = decide_row(p, bi.x, bi.y, &req, &terminal);
-                if (req) {
-                    task = make_int4(bi.x, chosen, bi.y, kModeRecord);
-                    const unsigned tail = sm.task_tail;
-                    if (tail - vload(&sm.task_head) < (unsigned)kTasks) {
-                        sm.task[tail % kTasks] = task;
-                        __threadfence_block();
-                        vstore(&sm.task_tail, tail + 1u);
-                    } else {
-                        own = 1;
-                    }
-                }
-                // the record is queued (or about to be written here) before the row retires
-                __threadfence();
-                if (terminal) atomicSub(&p.ctrl->outstanding, 1);
-            }
-            own = __shfl_sync(kFull, own, 0);
-            if (own) {
-                const int row = __shfl_sync(kFull, task.x, 0);
-                const int chosen = __shfl_sync(kFull, task.y, 0);
-                const int entry = __shfl_sync(kFull, task.z, 0);
-                record_row<ELT>(p, sm, row, entry, chosen);
-            }
-        }
-        if (finished) return;
-    }
-}
-
-template <int ELT>
-__global__ void __launch_bounds__(kThreads, StageCfg<ELT>::kMinBlocks) lp_stream_kernel(Params p) {
-    constexpr int S = StageCfg<ELT>::kStages;
-    constexpr int TILE_BYTES = kTileBytes;
-    constexpr int kTE = tile_elems<ELT>();
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    unsigned char* stages = smem_raw;
-    Shared& sm = *reinterpret_cast<Shared*>(smem_raw + (size_t)S * TILE_BYTES);
-    const int tid = threadIdx.x;
-    if (tid == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(&sm.full[s], 1);
-            mbar_init(&sm.empty[s], kConsumerThreads / 32);
-        }
-        for (int s = 0; s < kRing; ++s) {
-            mbar_init(&sm.rfull[s], kConsumerThreads / 32);
-            mbar_init(&sm.rempty[s], 1);
-        }
-        sm.ncand[0] = 0;
-        sm.ncand[1] = 0;
-        g_trace_n[0] = g_trace_n[1] = g_trace_n[2] = 0u;
-        sm.task_head = 0u;
-        sm.task_tail = 0u;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    }
-    __syncthreads();
+__global__ void __launch_bounds__(kConsumerThreads) lp_record_kernel(Params p) {
+    __shared__ RecShared rs;
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (vload(&p.ctrl->abort) != 0u) return;
-    const unsigned long long t0 = globaltimer();
-    trace(p, kTrKernel, 0, 0, tid == 0);
-    const int warp = tid >> 5;
-    if (warp == kConsumerThreads / 32) {
-        if (tid == kConsumerThreads) producer_loop<ELT>(p, sm, stages, t0);
-        return;
+    for (int row = blockIdx.x; row < p.rows; row += gridDim.x) {
+        const int4 t = __ldcg(&p.rec_tasks[row]);
+        if (t.z == 1) record_block<ELT>(p, rs, row, t.y, t.x);
     }
-    if (warp == kConsumerThreads / 32 + 1) {
-        merge_loop<ELT>(p, sm, t0);
-        return;
-    }
-    compute_loop<ELT>(p, sm, stages, t0);
 }
 
 template <int ELT>
@@ -1681,6 +1503,7 @@ cudaError_t query_launch_cfg(int dtype, LaunchCfg* cfg) {
     }
     if (e != cudaSuccess) return e;
     cfg->grid = sms * (occ > 0 ? occ : 1);
+    cfg->sms = sms;
     return cudaSuccess;
 }
 
@@ -1691,18 +1514,29 @@ cudaError_t launch_epilogue(const Params& p, int dtype, const LaunchCfg& cfg, cu
     long long work = (long long)p.rows * p.T;
     int grid = cfg.grid;
     if (work < grid) grid = work > 0 ? (int)work : 1;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(grid);
     lc.blockDim = dim3(kThreads);
     lc.dynamicSmemBytes = cfg.smem_bytes;
     lc.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
     lc.attrs = attr;
     lc.numAttrs = 1;
-    if (dtype == 1) return cudaLaunchKernelEx(&lc, lp_stream_kernel<2>, p);
-    return cudaLaunchKernelEx(&lc, lp_stream_kernel<4>, p);
+    e = dtype == 1 ? cudaLaunchKernelEx(&lc, lp_stream_kernel<2>, p) : cudaLaunchKernelEx(&lc, lp_stream_kernel<4>, p);
+    if (e != cudaSuccess) return e;
+    // records: one CTA per requesting row, at most two per SM (grid-stride)
+    int rgrid = p.rows < 2 * cfg.sms ? p.rows : 2 * cfg.sms;
+    if (rgrid < 1) rgrid = 1;
+    cudaLaunchConfig_t rc = {};
+    rc.gridDim = dim3(rgrid);
+    rc.blockDim = dim3(kConsumerThreads);
+    rc.dynamicSmemBytes = 0;
+    rc.stream = stream;
+    rc.attrs = attr;
+    rc.numAttrs = 1;
+    return dtype == 1 ? cudaLaunchKernelEx(&rc, lp_record_kernel<2>, p) : cudaLaunchKernelEx(&rc, lp_record_kernel<4>, p);
 }
 
 }  // namespace lp

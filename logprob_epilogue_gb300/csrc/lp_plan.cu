@@ -26,6 +26,7 @@ struct lp_plan_s {
     int* done;
     unsigned long long* row_best;
     int4* gdesc;
+    int4* rec_tasks;
     float2* part_ms;
     unsigned long long* part_keys;
     size_t part_ms_bytes, part_keys_bytes;
@@ -73,7 +74,7 @@ int check_desc(const lp_plan_desc* d) {
 }
 
 struct Layout {
-    size_t ctrl, queue, row_best, done, gdesc, part_ms, part_keys, total;
+    size_t ctrl, queue, row_best, done, gdesc, rec_tasks, part_ms, part_keys, total;
     size_t part_ms_bytes, part_keys_bytes;
 };
 
@@ -93,6 +94,8 @@ Layout layout_of(const lp_plan_desc* d) {
     off = align_up(off + rows * sizeof(int));
     L.gdesc = off;
     off = align_up(off + (size_t)d->max_groups * sizeof(int4));
+    L.rec_tasks = off;
+    off = align_up(off + rows * sizeof(int4));
     L.part_ms = off;
     L.part_ms_bytes = rows * T * sizeof(float2);
     off = align_up(off + L.part_ms_bytes);
@@ -190,6 +193,7 @@ lp::Params make_params(const lp_plan_s* plan, const lp_io& io) {
     p.row_best = plan->row_best;
     p.done = plan->done;
     p.gdesc = plan->gdesc;
+    p.rec_tasks = plan->rec_tasks;
     p.part_ms = plan->part_ms;
     p.part_keys = plan->part_keys;
     p.timeout_ns = (unsigned long long)(plan->d.timeout_ns > 0 ? plan->d.timeout_ns : kDefaultTimeoutNs);
@@ -258,6 +262,7 @@ int lp_plan_create(lp_plan_t* out, const lp_plan_desc* desc) {
     plan->row_best = reinterpret_cast<unsigned long long*>(plan->scratch + L.row_best);
     plan->done = reinterpret_cast<int*>(plan->scratch + L.done);
     plan->gdesc = reinterpret_cast<int4*>(plan->scratch + L.gdesc);
+    plan->rec_tasks = reinterpret_cast<int4*>(plan->scratch + L.rec_tasks);
     plan->part_ms = reinterpret_cast<float2*>(plan->scratch + L.part_ms);
     plan->part_keys = reinterpret_cast<unsigned long long*>(plan->scratch + L.part_keys);
     plan->part_ms_bytes = L.part_ms_bytes;
@@ -551,6 +556,7 @@ extern "C" int lp_run_static(const lp_plan_desc* desc, const lp_io* io, void* st
     run.row_best = reinterpret_cast<unsigned long long*>(base + L.row_best);
     run.done = reinterpret_cast<int*>(base + L.done);
     run.gdesc = reinterpret_cast<int4*>(base + L.gdesc);
+    run.rec_tasks = reinterpret_cast<int4*>(base + L.rec_tasks);
     run.part_ms = reinterpret_cast<float2*>(base + L.part_ms);
     run.part_keys = reinterpret_cast<unsigned long long*>(base + L.part_keys);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
