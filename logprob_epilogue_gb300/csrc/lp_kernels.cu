@@ -358,13 +358,45 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     return d;
 }
 
-template <int ELT>
-__device__ __forceinline__ float stage_max(const unsigned char* sp, int tid, uint32_t (&cm)[TileLayout<ELT>::NCH]) {
+// Vector c of the calling thread (16 bytes, elements (c*256 + tid)*EPV + e).
+// In the last, partial tile of a row (FULL = false) elements at or past nv
+// read as -inf, and vectors wholly past nv are not read at all.
+template <int ELT, bool FULL>
+__device__ __forceinline__ uint4 ld_vec(const unsigned char* sp, int c, int tid, int nv) {
+    const int v = c * kConsumerThreads + tid;
+    if constexpr (FULL) {
+        return lds128(sp + (size_t)v * 16);
+    } else {
+        constexpr int EPV = 16 / ELT;
+        constexpr uint32_t kNegInfW = ELT == 2 ? 0xFF80FF80u : 0xFF800000u;
+        const int valid = nv - v * EPV;
+        if (valid <= 0) return make_uint4(kNegInfW, kNegInfW, kNegInfW, kNegInfW);
+        uint4 x = lds128(sp + (size_t)v * 16);
+        if (valid < EPV) {
+            uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                if constexpr (ELT == 2) {
+                    if (2 * i >= valid) w[i] = kNegInfW;
+                    else if (2 * i + 1 >= valid) w[i] = (w[i] & 0xFFFFu) | 0xFF800000u;
+                } else {
+                    if (i >= valid) w[i] = kNegInfW;
+                }
+            }
+            x = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        return x;
+    }
+}
+
+template <int ELT, bool FULL>
+__device__ __forceinline__ float stage_max(const unsigned char* sp, int tid, int nv,
+                                           uint32_t (&cm)[TileLayout<ELT>::NCH]) {
     constexpr int NCH = TileLayout<ELT>::NCH;
     if constexpr (ELT == 2) {
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
-            const uint4 v = lds128(sp + (size_t)(c * kConsumerThreads + tid) * 16);
+            const uint4 v = ld_vec<ELT, FULL>(sp, c, tid, nv);
             cm[c] = bf16x2_max(bf16x2_max(v.x, v.y), bf16x2_max(v.z, v.w));
         }
         uint32_t a = cm[0], b = cm[1];
@@ -378,7 +410,7 @@ __device__ __forceinline__ float stage_max(const unsigned char* sp, int tid, uin
     } else {
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
-            const uint4 v = lds128(sp + (size_t)(c * kConsumerThreads + tid) * 16);
+            const uint4 v = ld_vec<ELT, FULL>(sp, c, tid, nv);
             cm[c] = __float_as_uint(fmax3(__uint_as_float(v.x), __uint_as_float(v.y),
                                           fmaxf(__uint_as_float(v.z), __uint_as_float(v.w))));
         }
@@ -414,15 +446,16 @@ __device__ __forceinline__ float f2_sum(unsigned long long a) {
     return __uint_as_float(static_cast<uint32_t>(a)) + __uint_as_float(static_cast<uint32_t>(a >> 32));
 }
 
-// Pass 2: sum of 2^(x*log2e - mb) over the thread's elements, two at a time.
-template <int ELT>
-__device__ __forceinline__ float stage_expsum(const unsigned char* sp, int tid, float mb) {
+// Pass 2: sum of 2^(x*log2e - mb) over the thread's elements, two at a time
+// (-inf elements contribute 0).
+template <int ELT, bool FULL>
+__device__ __forceinline__ float stage_expsum(const unsigned char* sp, int tid, int nv, float mb) {
     constexpr int NCH = TileLayout<ELT>::NCH;
     const unsigned long long L2E = f2_pack(kLog2e, kLog2e), NMB = f2_pack(-mb, -mb);
     unsigned long long s0 = 0ull, s1 = 0ull;  // two accumulators: the vector maxima stay live
 #pragma unroll
     for (int c = 0; c < NCH; ++c) {
-        const uint4 v = lds128(sp + (size_t)(c * kConsumerThreads + tid) * 16);
+        const uint4 v = ld_vec<ELT, FULL>(sp, c, tid, nv);
         if constexpr (ELT == 2) {
             s0 = f2_add(s0, f2_ex2(f2_fma(f2_pack(bf16_lo(v.x), bf16_hi(v.x)), L2E, NMB)));
             s1 = f2_add(s1, f2_ex2(f2_fma(f2_pack(bf16_lo(v.y), bf16_hi(v.y)), L2E, NMB)));
@@ -436,38 +469,6 @@ __device__ __forceinline__ float stage_expsum(const unsigned char* sp, int tid, 
         }
     }
     return f2_sum(f2_add(s0, s1));
-}
-
-// Partial tile (the last of a row): element k of thread i is tile element
-// k*256 + i, read one at a time; lanes past nv hold -inf.
-template <int ELT>
-__device__ __forceinline__ float partial_elem(const unsigned char* sp, int nv, int k, int tid) {
-    const int e = k * kConsumerThreads + tid;
-    if (e >= nv) return kNegInf;
-    if constexpr (ELT == 4) {
-        return reinterpret_cast<const float*>(sp)[e];
-    } else {
-        return __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const unsigned short*>(sp)[e]) << 16);
-    }
-}
-
-template <int ELT>
-__device__ __forceinline__ float partial_max(const unsigned char* sp, int nv, int tid) {
-    float m = kNegInf;
-#pragma unroll 4
-    for (int k = 0; k < TileLayout<ELT>::EPT; ++k) m = fmaxf(m, partial_elem<ELT>(sp, nv, k, tid));
-    return m;
-}
-
-template <int ELT>
-__device__ __forceinline__ float partial_expsum(const unsigned char* sp, int nv, int tid, float mb) {
-    float s = 0.0f;
-#pragma unroll 4
-    for (int k = 0; k < TileLayout<ELT>::EPT; ++k) {
-        const float x = partial_elem<ELT>(sp, nv, k, tid);
-        s += x > kNegInf ? ex2(fmaf(x, kLog2e, -mb)) : 0.0f;
-    }
-    return s;
 }
 
 template <int ELT>
@@ -829,25 +830,16 @@ __device__ __forceinline__ uint32_t warp_fourth_largest(uint32_t u, int lane, ui
 }
 
 // Tile element id (within the tile) of the thread's first element equal to m,
-// in a partial tile.
-template <int ELT>
-__device__ __forceinline__ int first_equal_partial(const unsigned char* sp, int nv, int tid, float m) {
-    int kf = -1;
-    for (int k = 0; k < TileLayout<ELT>::EPT && kf < 0; ++k)
-        if (partial_elem<ELT>(sp, nv, k, tid) == m) kf = k;
-    return kf * kConsumerThreads + tid;
-}
-
-// Same for a full tile, from the vector maxima: the first vector whose maximum
-// equals m, then the first element of that vector equal to m.
-template <int ELT>
-__device__ __forceinline__ int first_equal_full(const unsigned char* sp, int tid, float m,
-                                                const uint32_t (&cm)[TileLayout<ELT>::NCH]) {
+// from the vector maxima: the first vector whose maximum equals m, then the
+// first element of that vector equal to m.
+template <int ELT, bool FULL>
+__device__ __forceinline__ int first_equal(const unsigned char* sp, int tid, int nv, float m,
+                                           const uint32_t (&cm)[TileLayout<ELT>::NCH]) {
     using L = TileLayout<ELT>;
     int cf = L::NCH - 1;
 #pragma unroll
     for (int c = L::NCH - 1; c >= 0; --c) cf = (vec_max<ELT>(cm[c]) == m) ? c : cf;
-    const uint4 v = lds128(sp + (size_t)(cf * kConsumerThreads + tid) * 16);
+    const uint4 v = ld_vec<ELT, FULL>(sp, cf, tid, nv);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     int ef = L::EPV - 1;
 #pragma unroll
@@ -864,8 +856,8 @@ __device__ __forceinline__ int first_equal_full(const unsigned char* sp, int tid
 // theta and keeps its first two candidates in registers; ballots give the
 // slots.  A lane with more than two candidates (rare) writes the rest after a
 // warp scan.  Every lane of the warp calls it.
-template <int ELT>
-__device__ __forceinline__ int capture_candidates(const unsigned char* sp, int tid, float theta, int tbase,
+template <int ELT, bool FULL>
+__device__ __forceinline__ int capture_candidates(const unsigned char* sp, int tid, int nv, float theta, int tbase,
                                                   const uint32_t (&cm)[TileLayout<ELT>::NCH],
                                                   unsigned long long* region) {
     using L = TileLayout<ELT>;
@@ -877,12 +869,12 @@ __device__ __forceinline__ int capture_candidates(const unsigned char* sp, int t
     float x0 = 0.0f, x1 = 0.0f;
     for (unsigned q = pass; q; q &= q - 1u) {
         const int c = __ffs(q) - 1;
-        const uint4 v = lds128(sp + (size_t)(c * kConsumerThreads + tid) * 16);
+        const uint4 v = ld_vec<ELT, FULL>(sp, c, tid, nv);
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int e = 0; e < L::EPV; ++e) {
             const float x = (ELT == 2) ? ((e & 1) ? bf16_hi(w[e >> 1]) : bf16_lo(w[e >> 1])) : __uint_as_float(w[e]);
-            const bool take = x >= theta;
+            const bool take = x >= theta && (FULL || x > kNegInf);
             x1 = (take && n == 1) ? x : x1;
             k1 = (take && n == 1) ? c * L::EPV + e : k1;
             x0 = (take && n == 0) ? x : x0;
@@ -906,13 +898,13 @@ __device__ __forceinline__ int capture_candidates(const unsigned char* sp, int t
             int j = 0;
             for (unsigned q = pass; q && pos < 32; q &= q - 1u) {
                 const int c = __ffs(q) - 1;
-                const uint4 v = lds128(sp + (size_t)(c * kConsumerThreads + tid) * 16);
+                const uint4 v = ld_vec<ELT, FULL>(sp, c, tid, nv);
                 const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                 for (int e = 0; e < L::EPV; ++e) {
                     const float x =
                         (ELT == 2) ? ((e & 1) ? bf16_hi(w[e >> 1]) : bf16_lo(w[e >> 1])) : __uint_as_float(w[e]);
-                    if (x >= theta) {
+                    if (x >= theta && (FULL || x > kNegInf)) {
                         if (j >= 2 && pos < 32) {
                             region[pos] = make_key(x, (uint32_t)(tbase + (c * kConsumerThreads + tid) * L::EPV + e));
                             ++pos;
@@ -926,25 +918,6 @@ __device__ __forceinline__ int capture_candidates(const unsigned char* sp, int t
     return total;
 }
 
-// Partial tile (the last of a row): the same, element by element.
-template <int ELT>
-__device__ __forceinline__ int capture_partial(const unsigned char* sp, int nv, int tid, float theta, int tbase,
-                                               unsigned long long* region) {
-    using L = TileLayout<ELT>;
-    const int lane = tid & 31;
-    int cnt = 0;
-    for (int k = 0; k < L::EPT; ++k) {
-        const float x = stage_elem<ELT>(sp, false, nv, k, tid);
-        cnt += (x >= theta && x > kNegInf) ? 1 : 0;
-    }
-    int total = 0;
-    int pos = warp_excl_scan_i(cnt, lane, &total);
-    for (int k = 0; k < L::EPT && pos < 32; ++k) {
-        const float x = stage_elem<ELT>(sp, false, nv, k, tid);
-        if (x >= theta && x > kNegInf) region[pos++] = make_key(x, (uint32_t)(tbase + k * kConsumerThreads + tid));
-    }
-    return total;
-}
 
 __device__ __forceinline__ unsigned long long merge_lists(unsigned long long a, unsigned long long b, int lane) {
     const unsigned long long rev = __shfl_sync(kFull, b, 31 - lane);
@@ -981,6 +954,86 @@ __device__ __forceinline__ unsigned long long slot_top32(const ResultSlot& R, in
     return r;
 }
 
+// The compute warp's share of one tile: passes, candidates, partial results
+// into the ring slot.  FULL = false for the last, partial tile of a row.
+// False after a timeout (the status is flagged).
+template <int ELT, bool FULL>
+__device__ __forceinline__ bool tile_work(const Params& p, Shared& sm, ResultSlot& R, const unsigned char* sp, int nv,
+                                          int tbase, const int4& info, int rslot, uint32_t& tphase, unsigned tcount,
+                                          unsigned long long deadline) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int mode = info.w;
+    // pass 1: maxima (per vector for a full tile)
+    uint32_t cm[TileLayout<ELT>::NCH];
+    const float m = stage_max<ELT, FULL>(sp, tid, nv, cm);
+    const uint32_t om = ord32(__fadd_rn(m, 0.0f));
+    uint32_t omx;
+    if (mode == kModeNatural) {
+        // theta = min over warps of the warp's 4th largest thread maximum: at
+        // least 32 elements of the tile are >= theta, so its best 32 are among
+        // them.  The warp publishes its part now and reads the others' after
+        // its exp pass, so the exchange costs no wait in the common case.
+        const uint32_t o4 = warp_fourth_largest(om, lane, &omx);
+        if (lane == 0) {
+            R.wTheta[warp] = unord32(o4);
+            mbar_arrive(&sm.rtheta[rslot]);
+        }
+    } else {
+        omx = __reduce_max_sync(kFull, om);
+        // argmax key: smallest id among the lanes holding the warp maximum
+        uint32_t id = 0xFFFFFFFFu;
+        if (om == omx && m > kNegInf)
+            id = (uint32_t)(tbase + first_equal<ELT, FULL>(sp, tid, nv, m, cm));
+        const uint32_t idmin = __reduce_min_sync(kFull, id);
+        if (lane == 0) R.wkey[warp] = ((unsigned long long)omx << 32) | (unsigned long long)(~idmin);
+    }
+    // pass 2: sum exp(x - m) = 2^(x*log2e - mb - mb_lo): mb_lo, the rounding
+    // residual of m*log2e, is applied once, so large |m| costs no accuracy
+    float s = 0.0f;
+    if (mode != kModeArgmax && m > kNegInf) {
+        const float mb = m * kLog2e;
+        const float mb_lo = fmaf(m, kLog2e, -mb);
+        s = stage_expsum<ELT, FULL>(sp, tid, nv, mb) * ex2(-mb_lo);
+    }
+    if (mode == kModeNatural) {
+        const uint32_t tpar = (tphase >> rslot) & 1u;
+        tphase ^= 1u << rslot;
+        if (__any_sync(kFull, !mbar_wait(&sm.rtheta[rslot], tpar, deadline))) {
+            if (lane == 0) atomicOr(p.status, kStatusTimeout);
+            return false;
+        }
+        float theta = R.wTheta[0];
+#pragma unroll
+        for (int w = 1; w < kWarps; ++w) theta = fminf(theta, R.wTheta[w]);
+        const float th = m > kNegInf ? theta : kPosInf;
+        int cw = capture_candidates<ELT, FULL>(sp, tid, nv, th, tbase, cm, R.cand[warp]);
+        if (cw > 32) {
+            warp_top32_exact<ELT>(sp, true, nv, tbase, tid, R.cand[warp]);  // vector layout, -inf past nv
+            cw = 32;
+        }
+        if (lane == 0) R.wcnt[warp] = cw;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.rcand[rslot]);
+        if (warp == (int)(tcount & (kWarps - 1))) {
+            // this tile's selecting warp (rotating): the best 32 of all warps' candidates
+            if (__any_sync(kFull, !mbar_wait(&sm.rcand[rslot], tpar, deadline))) {
+                if (lane == 0) atomicOr(p.status, kStatusTimeout);
+                return false;
+            }
+            R.keys[lane] = slot_top32(R, lane);
+        }
+    }
+    const float Mw = unord32(omx);
+    const float sc = (m > kNegInf && mode != kModeArgmax) ? s * ex2((m - Mw) * kLog2e) : 0.0f;
+    const float sw = warp_sum_f(sc);
+    if (lane == 0) {
+        R.wM[warp] = Mw;
+        R.wS[warp] = sw;
+        if (warp == 0) R.info = info;
+    }
+    return true;
+}
+
 // ------------------------------------------------------------------ compute warps
 //
 // Each compute warp reduces its share of every tile on its own and hands its
@@ -1015,83 +1068,21 @@ __device__ void compute_loop(const Params& p, Shared& sm, unsigned char* stages,
             return;
         }
         const unsigned char* sp = stages + (size_t)stage * kTileBytes;
-        const int tile = info.y, mode = info.w;
+        const int tile = info.y;
         const int tbase = tile * kTE;
         const int rem = V - tbase;
         const int nv = rem < kTE ? (rem > 0 ? rem : 0) : kTE;
         const bool full = nv == kTE;
         trace(p, kTrTileStart, info.x, tile, tid == 0);
 
-        // pass 1: maxima (per vector for a full tile)
-        uint32_t cm[TileLayout<ELT>::NCH];
-        const float m = full ? stage_max<ELT>(sp, tid, cm) : partial_max<ELT>(sp, nv, tid);
-        const uint32_t om = ord32(__fadd_rn(m, 0.0f));
-        uint32_t omx;
-        if (mode == kModeNatural) {
-            // theta = min over warps of the warp's 4th largest thread maximum: at
-            // least 32 elements of the tile are >= theta, so its best 32 are among
-            // them.  The warp publishes its part now and reads the others' after
-            // its exp pass, so the exchange costs no wait in the common case.
-            const uint32_t o4 = warp_fourth_largest(om, lane, &omx);
-            if (lane == 0) {
-                R.wTheta[warp] = unord32(o4);
-                mbar_arrive(&sm.rtheta[rslot]);
-            }
+        bool ok;
+        if (__builtin_expect(full, 1)) {
+            ok = tile_work<ELT, true>(p, sm, R, sp, nv, tbase, info, rslot, tphase, tcount, deadline);
         } else {
-            omx = __reduce_max_sync(kFull, om);
-            // argmax key: smallest id among the lanes holding the warp maximum
-            uint32_t id = 0xFFFFFFFFu;
-            if (om == omx && m > kNegInf)
-                id = (uint32_t)(tbase + (full ? first_equal_full<ELT>(sp, tid, m, cm)
-                                              : first_equal_partial<ELT>(sp, nv, tid, m)));
-            const uint32_t idmin = __reduce_min_sync(kFull, id);
-            if (lane == 0) R.wkey[warp] = ((unsigned long long)omx << 32) | (unsigned long long)(~idmin);
-        }
-        // pass 2: sum exp(x - m) = 2^(x*log2e - mb - mb_lo): mb_lo, the rounding
-        // residual of m*log2e, is applied once, so large |m| costs no accuracy
-        float s = 0.0f;
-        if (mode != kModeArgmax && m > kNegInf) {
-            const float mb = m * kLog2e;
-            const float mb_lo = fmaf(m, kLog2e, -mb);
-            s = (full ? stage_expsum<ELT>(sp, tid, mb) : partial_expsum<ELT>(sp, nv, tid, mb)) * ex2(-mb_lo);
-        }
-        if (mode == kModeNatural) {
-            const uint32_t tpar = (tphase >> rslot) & 1u;
-            tphase ^= 1u << rslot;
-            if (__any_sync(kFull, !mbar_wait(&sm.rtheta[rslot], tpar, deadline))) {
-                if (lane == 0) atomicOr(p.status, kStatusTimeout);
-                return;
-            }
-            float theta = R.wTheta[0];
-#pragma unroll
-            for (int w = 1; w < kWarps; ++w) theta = fminf(theta, R.wTheta[w]);
-            int cw = full ? capture_candidates<ELT>(sp, tid, m > kNegInf ? theta : kPosInf, tbase, cm, R.cand[warp])
-                          : capture_partial<ELT>(sp, nv, tid, theta, tbase, R.cand[warp]);
-            if (cw > 32) {
-                warp_top32_exact<ELT>(sp, full, nv, tbase, tid, R.cand[warp]);
-                cw = 32;
-            }
-            if (lane == 0) R.wcnt[warp] = cw;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.rcand[rslot]);
-            if (warp == (int)(tcount & (kWarps - 1))) {
-                // this tile's selecting warp (rotating): the best 32 of all warps' candidates
-                if (__any_sync(kFull, !mbar_wait(&sm.rcand[rslot], tpar, deadline))) {
-                    if (lane == 0) atomicOr(p.status, kStatusTimeout);
-                    return;
-                }
-                R.keys[lane] = slot_top32(R, lane);
-            }
+            ok = tile_work<ELT, false>(p, sm, R, sp, nv, tbase, info, rslot, tphase, tcount, deadline);
         }
         ++tcount;
-        const float Mw = unord32(omx);
-        const float sc = (m > kNegInf && mode != kModeArgmax) ? s * ex2((m - Mw) * kLog2e) : 0.0f;
-        const float sw = warp_sum_f(sc);
-        if (lane == 0) {
-            R.wM[warp] = Mw;
-            R.wS[warp] = sw;
-            if (warp == 0) R.info = info;
-        }
+        if (!ok) return;
         __syncwarp();
         if (lane == 0) {
             mbar_arrive(&sm.empty[stage]);   // no more reads of this stage by this warp
