@@ -13,24 +13,28 @@ __host__ __device__ constexpr int tile_elems() { return kTileBytes / ELT; }
 inline int tile_elems_of_dtype(int dtype) { return dtype == 1 ? kTileBytes / 2 : kTileBytes / 4; }
 constexpr int kConsumerThreads = 256;   // 8 compute warps
 constexpr int kThreads = kConsumerThreads + 64;  // + 1 producer warp + 1 merge warp
-constexpr int kRing = 6;                // tile results in flight between compute and merge warps
+#ifndef LP_RING
+#define LP_RING 4
+#endif
+constexpr int kRing = LP_RING;          // tile results in flight between compute and merge warps
 constexpr int kKeysPerTile = 32;        // retained sort keys per tile
 constexpr int kRecordWords = 258;
 constexpr int kMaxIds = 128;
 constexpr int kCandCap = 256;           // tile candidate buffer (keys)
 
-// Pipeline stages per CTA and CTAs per SM, per element type.
+// Pipeline stages per CTA and CTAs per SM, per element type: three CTAs of two
+// 32 KiB stages fill the SM's shared memory and give 24 compute warps per SM.
 #ifndef LP_BF16_STAGES
-#define LP_BF16_STAGES 3
+#define LP_BF16_STAGES 2
 #endif
 #ifndef LP_BF16_CTAS
-#define LP_BF16_CTAS 2
+#define LP_BF16_CTAS 3
 #endif
 #ifndef LP_F32_STAGES
-#define LP_F32_STAGES 3
+#define LP_F32_STAGES 2
 #endif
 #ifndef LP_F32_CTAS
-#define LP_F32_CTAS 2
+#define LP_F32_CTAS 3
 #endif
 template <int kElt> struct StageCfg;
 template <> struct StageCfg<2> {
