@@ -619,10 +619,10 @@ __global__ void __launch_bounds__(1024) lp_prepare_kernel(Params p) {
 // shared-memory stage with a TMA bulk copy.  Chained items (rows appended after
 // an acceptance) come first: each producer always owns the next chained item
 // it claimed (claims run ahead of the appended rows, in order) and takes it as
-// soon as its row exists; otherwise it takes a fresh item.  Rows deep in a
+// soon as the queue entry of its row is published; otherwise it takes a fresh
+// item, claimed one ahead with its queue entry already loaded.  Rows deep in a
 // verify chain therefore start at once instead of queueing behind the depth-0
-// rows, and single-item claims spread a row's tiles over many CTAs.  The next
-// item is chosen right after a copy is issued, while the stages are busy.
+// rows, and single-item claims spread a row's tiles over many CTAs.
 constexpr unsigned kNone = 0xFFFFFFFFu;
 
 template <int ELT>
@@ -633,14 +633,15 @@ __device__ __noinline__ void producer_loop(const Params& p, Shared& sm, unsigned
     const uint64_t policy = evict_first_policy();
     Ctrl* ctrl = p.ctrl;
     const unsigned T = (unsigned)p.T;
+    // first claims in parallel: one chained, one fresh
+    unsigned chain_claim = atomicAdd(&ctrl->chain_next, 1u);
+    unsigned fresh_ahead = atomicAdd(&ctrl->fresh_next, 1u);
     const unsigned F = vload(&ctrl->fresh_rows);
     const unsigned fresh_items = F * T;
+    unsigned long long fresh_entry = fresh_ahead < fresh_items ? vload(&p.queue[fresh_ahead / T]) : ~0ull;
+    bool fresh_done = fresh_ahead >= fresh_items;
     int stage = 0;
     uint32_t phase = 0;
-    unsigned chain_claim = kNone;    // chained item owned by this producer, not yet issued
-    unsigned chain_rows = 0;         // chained rows seen appended
-    unsigned fresh_ahead = kNone;    // fresh item already claimed
-    bool fresh_done = fresh_items == 0;
     bool timed_out = false;
     for (;;) {
         int4 item = make_int4(0, 0, -1, 0);
@@ -653,50 +654,48 @@ __device__ __noinline__ void producer_loop(const Params& p, Shared& sm, unsigned
             timed_out = true;
         } else {
             if (chain_claim == kNone) chain_claim = atomicAdd(&ctrl->chain_next, 1u);
-            unsigned pos = kNone, tile = 0;
+            unsigned long long e = ~0ull;
+            unsigned tile = 0;
             for (;;) {
-                if (chain_claim / T >= chain_rows) chain_rows = vload(&ctrl->chain_tail);
-                if (chain_claim / T < chain_rows) {
-                    pos = F + chain_claim / T;
-                    tile = chain_claim % T;
-                    chain_claim = kNone;
+                // the chained item, once the queue entry of its row is published
+                const unsigned cpos = F + chain_claim / T;
+                if (cpos < (unsigned)p.rows) {
+                    e = vload(&p.queue[cpos]);
+                    if ((long long)e >= 0) {
+                        tile = chain_claim % T;
+                        chain_claim = kNone;
+                        break;
+                    }
+                }
+                if (!fresh_done && fresh_ahead != kNone) {
+                    e = fresh_entry;
+                    tile = fresh_ahead % T;
+                    fresh_ahead = kNone;  // the next one is claimed once this copy is issued
                     break;
                 }
                 if (!fresh_done) {
-                    const unsigned f = fresh_ahead != kNone ? fresh_ahead : atomicAdd(&ctrl->fresh_next, 1u);
-                    fresh_ahead = kNone;
-                    if (f < fresh_items) {
-                        pos = f / T;
-                        tile = f % T;
-                        break;
-                    }
-                    fresh_done = true;
+                    fresh_ahead = atomicAdd(&ctrl->fresh_next, 1u);
+                    fresh_done = fresh_ahead >= fresh_items;
+                    if (!fresh_done) fresh_entry = vload(&p.queue[fresh_ahead / T]);
+                    continue;
                 }
                 // nothing to take yet: the run is complete once no group is outstanding
                 if (vload(&ctrl->outstanding) <= 0) {
                     __threadfence();
-                    chain_rows = vload(&ctrl->chain_tail);  // final once nothing is outstanding
-                    if (chain_claim / T < chain_rows) continue;
+                    // final once nothing is outstanding: a claim below it has its entry published
+                    if (chain_claim / T < vload(&ctrl->chain_tail)) continue;
+                    e = ~0ull;
                     break;
                 }
                 if (globaltimer() > deadline) {
                     timed_out = true;
+                    e = ~0ull;
                     break;
                 }
                 __nanosleep(32);
             }
-            if (pos != kNone) {
-                unsigned long long e = vload(&p.queue[pos]);
-                for (uint32_t k = 0; (long long)e < 0; ++k) {  // reserved, not yet published
-                    if ((k & 63u) == 63u && globaltimer() > deadline) break;
-                    e = vload(&p.queue[pos]);
-                }
-                if ((long long)e < 0) {
-                    timed_out = true;
-                } else {
-                    item = make_int4((int)(e & 0x0FFFFFFFu), (int)tile, (int)(e >> 32), (int)((e >> 28) & 3u));
-                }
-            }
+            if ((long long)e >= 0)
+                item = make_int4((int)(e & 0x0FFFFFFFu), (int)tile, (int)(e >> 32), (int)((e >> 28) & 3u));
         }
         if (timed_out) atomicOr(p.status, kStatusTimeout);
         if (!mbar_wait(&sm.empty[stage], phase ^ 1u, deadline)) {
@@ -722,8 +721,13 @@ __device__ __noinline__ void producer_loop(const Params& p, Shared& sm, unsigned
             stage = 0;
             phase ^= 1u;
         }
-        // claim a fresh item ahead while fresh ones remain (its atomic overlaps the next waits)
-        if (!fresh_done && fresh_ahead == kNone) fresh_ahead = atomicAdd(&ctrl->fresh_next, 1u);
+        // the next fresh item and its entry (depth-0 entries are all published),
+        // overlapping the next stage wait
+        if (!fresh_done && fresh_ahead == kNone) {
+            fresh_ahead = atomicAdd(&ctrl->fresh_next, 1u);
+            fresh_done = fresh_ahead >= fresh_items;
+            if (!fresh_done) fresh_entry = vload(&p.queue[fresh_ahead / T]);
+        }
     }
 }
 
