@@ -12,7 +12,7 @@ template <int ELT>
 __host__ __device__ constexpr int tile_elems() { return kTileBytes / ELT; }
 inline int tile_elems_of_dtype(int dtype) { return dtype == 1 ? kTileBytes / 2 : kTileBytes / 4; }
 constexpr int kConsumerThreads = 256;   // 8 compute warps
-constexpr int kThreads = kConsumerThreads + 64;  // + 1 producer warp + 1 merge warp
+constexpr int kThreads = kConsumerThreads + 32;  // + 1 producer warp
 #ifndef LP_RING
 #define LP_RING 4
 #endif
@@ -99,7 +99,7 @@ struct Params {
     int4* gdesc;          // [max_groups] x = first row, y = k | mode << 8 | explicit << 12 |
                           // requested << 13, z = top_k or id count, w = sampled token
     int4* rec_tasks;      // [max_rows] per row: (chosen token, queue entry, 1 = record to build, 0)
-    float2* part_ms;      // [max_rows * T] tile (max, exp-sum)
+    float2* part_ms;      // [max_rows * T * 8] (max, exp-sum) of each compute warp's share of a tile
     unsigned long long* part_keys;  // [max_rows * T * 32] tile keys, descending
     unsigned long long timeout_ns;
     unsigned int debug_flags;

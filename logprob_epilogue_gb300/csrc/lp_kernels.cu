@@ -112,6 +112,12 @@ __device__ __forceinline__ void vstore(T* p, T v) { *reinterpret_cast<volatile T
 // writes (and those ordered before it by a warp barrier) are visible to whoever
 // reads the result, and the writes released before the values it reads are
 // visible to this thread afterwards.
+__device__ __forceinline__ int atomic_add_acq_rel_cta_shared(int* p, int v) {
+    int old;
+    asm volatile("atom.acq_rel.cta.shared::cta.add.s32 %0, [%1], %2;" : "=r"(old) : "r"(smem_u32(p)), "r"(v) : "memory");
+    return old;
+}
+
 __device__ __forceinline__ int atomic_add_acq_rel(int* p, int v) {
     int old;
     asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
@@ -264,29 +270,23 @@ constexpr int kMaxStages = 8;
 constexpr int kWarps = kConsumerThreads / 32;  // compute warps
 static_assert(StageCfg<2>::kStages <= kMaxStages && StageCfg<4>::kStages <= kMaxStages, "stage count");
 
-// One tile's results, handed from the compute warps (one entry per warp) to the
-// merge warp, which combines them.
-struct ResultSlot {
-    int4 info;                              // row, tile, queue entry (< 0: no more tiles), mode
-    float wM[kWarps];                       // warp maximum
-    float wS[kWarps];                       // warp sum exp(x - wM)
-    unsigned long long wkey[kWarps];        // argmax key of the warp's elements (non-natural tiles)
-    float wTheta[kWarps];                   // natural tiles: the warp's 4th largest thread maximum
-    int wcnt[kWarps];                       // natural tiles: keys in cand[w] (<= 32)
-    unsigned long long cand[kWarps][32];    // natural tiles: the warp's keys >= theta (its best 32 if more)
-    unsigned long long keys[32];            // natural tiles: the tile's best 32 keys, descending
+// Natural-alternative tiles: the 8 compute warps exchange their candidate
+// thresholds and candidates through a slot of this ring (one slot per tile).
+struct CandSlot {
+    float wTheta[kWarps];                   // the warp's 4th largest thread maximum
+    int wcnt[kWarps];                       // keys in cand[w] (<= 32)
+    unsigned long long cand[kWarps][32];    // the warp's keys >= theta (its best 32 if more)
 };
 
 struct Shared {
     uint64_t full[kMaxStages];       // stage filled (producer + TMA)
     uint64_t empty[kMaxStages];      // stage released (8 compute warps)
-    uint64_t rfull[kRing];           // result written (8 compute warps)
-    uint64_t rempty[kRing];          // result consumed (merge warp)
-    uint64_t rtheta[kRing];          // natural tiles: thresholds of the 8 warps written
-    uint64_t rcand[kRing];           // natural tiles: candidates of the 8 warps written
+    uint64_t ctheta[kRing];          // candidate slot: thresholds of the 8 warps written
+    uint64_t ccand[kRing];           // candidate slot: candidates of the 8 warps written
+    uint64_t cfree[kRing];           // candidate slot: read by the tile's selecting warp
     int4 info[kMaxStages];           // work item of each stage
-    ResultSlot res[kRing];
-    int2 batch[kRing];               // (row, queue entry) of the tiles in a merge-warp batch
+    int tcnt[kMaxStages];            // compute warps done with the stage's tile
+    CandSlot cs[kRing];
 };
 
 // Shared memory of the record kernel.
@@ -931,7 +931,7 @@ __device__ __forceinline__ unsigned long long merge_lists(unsigned long long a, 
 // Best 32 keys (descending, lane i holds the i-th) of a tile's candidate
 // regions: the keys are taken 64 at a time in region order, each half sorted
 // (bitonic), the halves and the running result merged.
-__device__ __forceinline__ unsigned long long slot_top32(const ResultSlot& R, int lane) {
+__device__ __forceinline__ unsigned long long slot_top32(const CandSlot& R, int lane) {
     int cw[kWarps];
     int n = 0;
 #pragma unroll
@@ -958,39 +958,72 @@ __device__ __forceinline__ unsigned long long slot_top32(const ResultSlot& R, in
     return r;
 }
 
-// The compute warp's share of one tile: passes, candidates, partial results
-// into the ring slot.  FULL = false for the last, partial tile of a row.
-// False after a timeout (the status is flagged).
+// The row's done count taken by a compute warp that finished a tile last; its
+// result is read later (lane 0).  The row's decision falls to the warp whose
+// count completes the row.
+struct Pending {
+    bool valid;
+    unsigned old;     // value the counter held before this warp's increment
+    int row, entry;
+};
+
+__device__ __noinline__ int decide_row(const Params& p, int row, int entry, unsigned fresh_rows, bool* terminal);
+
+// Reads the pending count (waiting for it if needed) and decides the row when
+// this warp finished it.
+__device__ __forceinline__ void resolve(const Params& p, Pending& pd, unsigned fresh_rows) {
+    if ((threadIdx.x & 31) == 0 && pd.valid) {
+        if (pd.old == (unsigned)(p.T - 1)) {
+            bool terminal = false;
+            decide_row(p, pd.row, pd.entry, fresh_rows, &terminal);
+            // the record flag and the emitted tokens are written before the group retires
+            if (terminal) atomicSub(&p.ctrl->outstanding, 1);
+        }
+    }
+    pd.valid = false;
+}
+
+// The compute warp's share of one tile: passes, candidates (natural tiles,
+// through a candidate slot), then its partial results published to global
+// memory: (max, exp-sum), the argmax key (atomicMax on the row's best key) and
+// one acquire-release increment of the row's done count, read back later.
+// FULL = false for the last, partial tile of a row.  False after a timeout.
 template <int ELT, bool FULL>
-__device__ __forceinline__ bool tile_work(const Params& p, Shared& sm, ResultSlot& R, const unsigned char* sp, int nv,
-                                          int tbase, const int4& info, int rslot, uint32_t& tphase, unsigned tcount,
-                                          unsigned long long deadline) {
+__device__ __forceinline__ bool tile_work(const Params& p, Shared& sm, const unsigned char* sp, int nv, int tbase,
+                                          const int4& info, int stage, int& ns, uint32_t& nphase, unsigned tcount,
+                                          Pending& pd, unsigned fresh_rows, unsigned long long deadline) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int mode = info.w;
+    const bool natural = mode == kModeNatural;
     // pass 1: maxima (per vector for a full tile)
     uint32_t cm[TileLayout<ELT>::NCH];
     const float m = stage_max<ELT, FULL>(sp, tid, nv, cm);
     const uint32_t om = ord32(__fadd_rn(m, 0.0f));
     uint32_t omx;
-    if (mode == kModeNatural) {
+    CandSlot& C = sm.cs[ns];
+    const uint32_t npar = (nphase >> ns) & 1u;
+    if (natural) {
         // theta = min over warps of the warp's 4th largest thread maximum: at
         // least 32 elements of the tile are >= theta, so its best 32 are among
         // them.  The warp publishes its part now and reads the others' after
         // its exp pass, so the exchange costs no wait in the common case.
         const uint32_t o4 = warp_fourth_largest(om, lane, &omx);
+        if (__any_sync(kFull, !mbar_wait(&sm.cfree[ns], npar, deadline))) {  // slot read by its last user
+            if (lane == 0) atomicOr(p.status, kStatusTimeout);
+            return false;
+        }
         if (lane == 0) {
-            R.wTheta[warp] = unord32(o4);
-            mbar_arrive(&sm.rtheta[rslot]);
+            C.wTheta[warp] = unord32(o4);
+            mbar_arrive(&sm.ctheta[ns]);
         }
     } else {
         omx = __reduce_max_sync(kFull, om);
-        // argmax key: smallest id among the lanes holding the warp maximum
-        uint32_t id = 0xFFFFFFFFu;
-        if (om == omx && m > kNegInf)
-            id = (uint32_t)(tbase + first_equal<ELT, FULL>(sp, tid, nv, m, cm));
-        const uint32_t idmin = __reduce_min_sync(kFull, id);
-        if (lane == 0) R.wkey[warp] = ((unsigned long long)omx << 32) | (unsigned long long)(~idmin);
     }
+    // argmax key: smallest id among the lanes holding the warp maximum
+    uint32_t id = 0xFFFFFFFFu;
+    if (om == omx && m > kNegInf) id = (uint32_t)(tbase + first_equal<ELT, FULL>(sp, tid, nv, m, cm));
+    const uint32_t idmin = __reduce_min_sync(kFull, id);
+    const unsigned long long wkey = ((unsigned long long)omx << 32) | (unsigned long long)(~idmin);
     // pass 2: sum exp(x - m) = 2^(x*log2e - mb - mb_lo): mb_lo, the rounding
     // residual of m*log2e, is applied once, so large |m| costs no accuracy
     float s = 0.0f;
@@ -999,76 +1032,100 @@ __device__ __forceinline__ bool tile_work(const Params& p, Shared& sm, ResultSlo
         const float mb_lo = fmaf(m, kLog2e, -mb);
         s = stage_expsum<ELT, FULL>(sp, tid, nv, mb) * ex2(-mb_lo);
     }
-    if (mode == kModeNatural) {
-        const uint32_t tpar = (tphase >> rslot) & 1u;
-        tphase ^= 1u << rslot;
-        if (__any_sync(kFull, !mbar_wait(&sm.rtheta[rslot], tpar, deadline))) {
+    // the previous tile's count is back by now
+    resolve(p, pd, fresh_rows);
+    if (natural) {
+        if (__any_sync(kFull, !mbar_wait(&sm.ctheta[ns], npar, deadline))) {
             if (lane == 0) atomicOr(p.status, kStatusTimeout);
             return false;
         }
-        float theta = R.wTheta[0];
+        float theta = C.wTheta[0];
 #pragma unroll
-        for (int w = 1; w < kWarps; ++w) theta = fminf(theta, R.wTheta[w]);
+        for (int w = 1; w < kWarps; ++w) theta = fminf(theta, C.wTheta[w]);
         const float th = m > kNegInf ? theta : kPosInf;
-        int cw = capture_candidates<ELT, FULL>(sp, tid, nv, th, tbase, cm, R.cand[warp]);
+        int cw = capture_candidates<ELT, FULL>(sp, tid, nv, th, tbase, cm, C.cand[warp]);
         if (cw > 32) {
-            warp_top32_exact<ELT>(sp, true, nv, tbase, tid, R.cand[warp]);  // vector layout, -inf past nv
+            warp_top32_exact<ELT>(sp, true, nv, tbase, tid, C.cand[warp]);  // vector layout, -inf past nv
             cw = 32;
         }
-        if (lane == 0) R.wcnt[warp] = cw;
+        if (lane == 0) C.wcnt[warp] = cw;
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.rcand[rslot]);
-        if (warp == (int)(tcount & (kWarps - 1))) {
-            // this tile's selecting warp (rotating): the best 32 of all warps' candidates
-            if (__any_sync(kFull, !mbar_wait(&sm.rcand[rslot], tpar, deadline))) {
-                if (lane == 0) atomicOr(p.status, kStatusTimeout);
-                return false;
-            }
-            R.keys[lane] = slot_top32(R, lane);
-        }
+        if (lane == 0) mbar_arrive(&sm.ccand[ns]);
     }
+    // partial results of the warp; the last of the 8 warps to finish the tile
+    // counts it for the row (one acquire-release increment per tile, which
+    // publishes the other warps' results too: they are ordered before it by
+    // the CTA-scope count)
     const float Mw = unord32(omx);
     const float sc = (m > kNegInf && mode != kModeArgmax) ? s * ex2((m - Mw) * kLog2e) : 0.0f;
     const float sw = warp_sum_f(sc);
+    bool counted = false;
     if (lane == 0) {
-        R.wM[warp] = Mw;
-        R.wS[warp] = sw;
-        if (warp == 0) R.info = info;
+        const long long wslot = ((long long)info.x * p.T + info.y) * kWarps + warp;
+        p.part_ms[wslot] = make_float2(Mw, sw);
+        atomicMax(&p.row_best[info.x], wkey);
+        if (atomic_add_acq_rel_cta_shared(&sm.tcnt[stage], 1) == kWarps - 1) {
+            sm.tcnt[stage] = 0;  // the stage is not refilled before this warp releases it below
+            pd.old = (unsigned)atomic_add_acq_rel(&p.done[info.x], 1);  // read back at the next resolve
+            pd.row = info.x;
+            pd.entry = info.z;
+            counted = true;
+        }
+    }
+    pd.valid = __shfl_sync(kFull, counted, 0);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.empty[stage]);  // no more reads of this stage by this warp
+    if (natural) {
+        if (warp == (int)(tcount & (kWarps - 1))) {
+            // this tile's selecting warp (rotating): the tile's best 32 keys
+            if (__any_sync(kFull, !mbar_wait(&sm.ccand[ns], npar, deadline))) {
+                if (lane == 0) atomicOr(p.status, kStatusTimeout);
+                return false;
+            }
+            const unsigned long long key = slot_top32(C, lane);
+            const long long tslot = (long long)info.x * p.T + info.y;
+            p.part_keys[tslot * kKeysPerTile + lane] = key;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.cfree[ns]);
+        }
+        nphase ^= 1u << ns;
+        if (++ns == kRing) ns = 0;
     }
     return true;
 }
 
 // ------------------------------------------------------------------ compute warps
 //
-// Each compute warp reduces its share of every tile on its own and hands its
-// partial results to the merge warp through the ring: the warps never wait for
-// one another, except on natural-alternative tiles, where the 8 warp
-// thresholds are exchanged (a bounded mbarrier wait) before the candidates are
-// taken.
+// Each compute warp reduces its share of every tile on its own and publishes
+// its partial results itself: the warps never wait for one another, except on
+// natural-alternative tiles, where the 8 warp thresholds and candidates are
+// exchanged through a candidate slot (bounded mbarrier waits).
 template <int ELT>
 __device__ void compute_loop(const Params& p, Shared& sm, unsigned char* stages, unsigned long long t0) {
     constexpr int S = StageCfg<ELT>::kStages;
     constexpr int kTE = tile_elems<ELT>();
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x, lane = tid & 31;
     const unsigned long long deadline = t0 + p.timeout_ns;
     const int V = (int)p.V;
-    int stage = 0, rslot = 0;
-    uint32_t phase = 0, rphase = 0, tphase = 0;  // tphase bit r: phase of rtheta[r] and rcand[r]
-    unsigned tcount = 0;                           // tiles seen (picks the selecting warp)
+    const unsigned fresh_rows = vload(&p.ctrl->fresh_rows);
+    int stage = 0, ns = 0;
+    uint32_t phase = 0, nphase = 0;   // nphase bit r: uses of candidate slot r, mod 2
+    unsigned tcount = 0;              // tiles seen (picks the selecting warp)
+    Pending pd;
+    pd.valid = false;
+    pd.old = 0;
+    pd.row = pd.entry = 0;
     for (;;) {
-        bool late = !mbar_wait(&sm.full[stage], phase, deadline);
-        const int4 info = sm.info[stage];
-        late = late || !mbar_wait(&sm.rempty[rslot], rphase ^ 1u, deadline);
-        if (__any_sync(kFull, late)) {
+        // a pending count is read before this warp can block: the row it may
+        // complete could be what the next tile waits for
+        if (pd.valid && !mbar_test_wait(&sm.full[stage], phase)) resolve(p, pd, fresh_rows);
+        if (__any_sync(kFull, !mbar_wait(&sm.full[stage], phase, deadline))) {
             if (lane == 0) atomicOr(p.status, kStatusTimeout);
             return;
         }
-        ResultSlot& R = sm.res[rslot];
-        if (info.z < 0) {
-            // no more tiles: the merge warp finishes once every compute warp is here
-            if (tid == 0) R.info = info;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.rfull[rslot]);
+        const int4 info = sm.info[stage];
+        if (info.z < 0) {  // no more tiles
+            resolve(p, pd, fresh_rows);
             return;
         }
         const unsigned char* sp = stages + (size_t)stage * kTileBytes;
@@ -1076,45 +1133,35 @@ __device__ void compute_loop(const Params& p, Shared& sm, unsigned char* stages,
         const int tbase = tile * kTE;
         const int rem = V - tbase;
         const int nv = rem < kTE ? (rem > 0 ? rem : 0) : kTE;
-        const bool full = nv == kTE;
         trace(p, kTrTileStart, info.x, tile, tid == 0);
-
         bool ok;
-        if (__builtin_expect(full, 1)) {
-            ok = tile_work<ELT, true>(p, sm, R, sp, nv, tbase, info, rslot, tphase, tcount, deadline);
+        if (__builtin_expect(nv == kTE, 1)) {
+            ok = tile_work<ELT, true>(p, sm, sp, nv, tbase, info, stage, ns, nphase, tcount, pd, fresh_rows, deadline);
         } else {
-            ok = tile_work<ELT, false>(p, sm, R, sp, nv, tbase, info, rslot, tphase, tcount, deadline);
+            ok = tile_work<ELT, false>(p, sm, sp, nv, tbase, info, stage, ns, nphase, tcount, pd, fresh_rows, deadline);
         }
         ++tcount;
         if (!ok) return;
-        __syncwarp();
-        if (lane == 0) {
-            mbar_arrive(&sm.empty[stage]);   // no more reads of this stage by this warp
-            mbar_arrive(&sm.rfull[rslot]);   // this warp's results are in the slot
-        }
         trace(p, kTrTileEnd, info.x, tile, tid == 0);
         if (++stage == S) {
             stage = 0;
             phase ^= 1u;
         }
-        if (++rslot == kRing) {
-            rslot = 0;
-            rphase ^= 1u;
-        }
     }
 }
 
-// ------------------------------------------------------------------ merge warp
+// ------------------------------------------------------------------ decisions
 
-// Acceptance decision of a row whose tiles are all published (one lane of the
-// merge warp; d = the group's descriptor and draft = the row's draft token,
-// loaded by the caller): argmax = the row's best key; on acceptance the next row of the
-// group is appended to the chained queue, else the group ends (*terminal).  A
-// requesting row is flagged for the record kernel.  Returns the chosen token.
-__device__ __noinline__ int decide_row(const Params& p, int row, int entry, int4 d, int draft, unsigned fresh_rows,
-                                      bool* terminal) {
+// Acceptance decision of a row whose tiles are all counted (lane 0 of the
+// compute warp whose count completed it): argmax = the row's best key; on
+// acceptance the next row of the group is appended to the chained queue, else
+// the group ends (*terminal).  A requesting row is flagged for the record
+// kernel.  Returns the chosen token.
+__device__ __noinline__ int decide_row(const Params& p, int row, int entry, unsigned fresh_rows, bool* terminal) {
     const int g = entry >> 4, j = entry & 15;
+    const int4 d = __ldcg(&p.gdesc[g]);
     const unsigned long long bk = __ldcg(&p.row_best[row]);
+    const int draft = __ldg(&p.drafts[row]);
     const int r0 = d.x, k = d.y & 0xFF, req = (d.y >> 13) & 1, samp = d.w;
     const uint32_t amax = key_id(bk);
     const int chosen = (k == 0 && samp >= 0) ? samp : (int)amax;
@@ -1137,107 +1184,6 @@ __device__ __noinline__ int decide_row(const Params& p, int row, int entry, int4
     return chosen;
 }
 
-// The merge warp combines the compute warps' partial results of each tile
-// (max, exp-sum, argmax key, or the best 32 of the candidates), publishes them
-// to global memory and counts each row's finished tiles; for a row's last
-// tile it takes the acceptance decision at once and, for a requesting row,
-// appends a record task for the record kernel.  Results are taken in batches
-// (the slots already written, up to the ring size): one fence, then one
-// done-counter atomic per tile from separate lanes.
-template <int ELT>
-__device__ __noinline__ void merge_loop(const Params& p, Shared& sm, unsigned long long t0) {
-    const int lane = threadIdx.x & 31;
-    const unsigned long long deadline = t0 + p.timeout_ns;
-    const int T = p.T;
-    const unsigned fresh_rows = vload(&p.ctrl->fresh_rows);
-    int rslot = 0;
-    uint32_t rphase = 0;
-    for (;;) {
-        if (!mbar_wait(&sm.rfull[rslot], rphase, deadline)) {
-            if (lane == 0) atomicOr(p.status, kStatusTimeout);
-            return;
-        }
-        int n = 0;
-        bool finished = false;
-        trace(p, kTrMergeStart, 0, rslot, lane == 0);
-        do {
-            const ResultSlot& R = sm.res[rslot];
-            const int4 info = R.info;
-            if (info.z < 0) {
-                finished = true;
-                break;
-            }
-            const int mode = info.w;
-            // tile (max, sum exp(x - max)) from the 8 warps' partials
-            // lanes 0..7 hold the warps' partials; xor steps 4, 2, 1 stay within them
-            const int wl = lane & (kWarps - 1);
-            const float mw = R.wM[wl];
-            float M = mw;
-            M = fmaxf(M, __shfl_xor_sync(kFull, M, 4));
-            M = fmaxf(M, __shfl_xor_sync(kFull, M, 2));
-            M = fmaxf(M, __shfl_xor_sync(kFull, M, 1));
-            float St = (mode != kModeArgmax && mw > kNegInf) ? R.wS[wl] * ex2((mw - M) * kLog2e) : 0.0f;
-            St += __shfl_xor_sync(kFull, St, 4);
-            St += __shfl_xor_sync(kFull, St, 2);
-            St += __shfl_xor_sync(kFull, St, 1);
-            unsigned long long key;
-            if (mode == kModeNatural) {
-                key = R.keys[lane];
-            } else {
-                key = R.wkey[wl];
-#pragma unroll
-                for (int o = 4; o > 0; o >>= 1) {
-                    const unsigned long long k2 = __shfl_xor_sync(kFull, key, o);
-                    key = k2 > key ? k2 : key;
-                }
-            }
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&sm.rempty[rslot]);
-                sm.batch[n] = make_int2(info.x, info.z);
-            }
-            const long long slot = (long long)info.x * T + info.y;
-            if (mode == kModeNatural || lane == 0) p.part_keys[slot * kKeysPerTile + lane] = key;
-            if (lane == 0) {
-                p.part_ms[slot] = make_float2(M, St);
-                atomicMax(&p.row_best[info.x], key);
-            }
-            trace(p, kTrPublish, info.x, info.y, lane == 0);
-            ++n;
-            if (++rslot == kRing) {
-                rslot = 0;
-                rphase ^= 1u;
-            }
-        } while (n < kRing && mbar_test_wait(&sm.rfull[rslot], rphase));
-        // one acquire-release increment per tile (separate lanes): the tile's results
-        // are visible to whoever counts the row's last tile
-        __syncwarp();
-        int last = 0;
-        int2 b = make_int2(0, 0);
-        int4 gd = make_int4(0, 0, 0, 0);
-        int draft = -1;
-        if (lane < n) {
-            b = sm.batch[lane];
-            last = atomic_add_acq_rel(&p.done[b.x], 1) == T - 1;
-            gd = __ldcg(&p.gdesc[b.y >> 4]);  // for the decision, loaded while the count is in flight
-            draft = __ldg(&p.drafts[b.x]);
-        }
-        unsigned lastmask = __ballot_sync(kFull, last);
-        trace(p, kTrMergeEnd, n, __popc(lastmask), lane == 0);
-        while (lastmask) {
-            const int i = __ffs(lastmask) - 1;
-            lastmask &= lastmask - 1;
-            if (lane == i) {
-                bool terminal = false;
-                decide_row(p, b.x, b.y, gd, draft, fresh_rows, &terminal);
-                if (terminal) atomicSub(&p.ctrl->outstanding, 1);
-            }
-        }
-        __syncwarp();
-        if (finished) return;
-    }
-}
-
 template <int ELT>
 __global__ void __launch_bounds__(kThreads, StageCfg<ELT>::kMinBlocks) lp_stream_kernel(Params p) {
     constexpr int S = StageCfg<ELT>::kStages;
@@ -1251,12 +1197,13 @@ __global__ void __launch_bounds__(kThreads, StageCfg<ELT>::kMinBlocks) lp_stream
             mbar_init(&sm.empty[s], kWarps);
         }
         for (int s = 0; s < kRing; ++s) {
-            mbar_init(&sm.rfull[s], kWarps);
-            mbar_init(&sm.rempty[s], 1);
-            mbar_init(&sm.rtheta[s], kWarps);
-            mbar_init(&sm.rcand[s], kWarps);
+            mbar_init(&sm.ctheta[s], kWarps);
+            mbar_init(&sm.ccand[s], kWarps);
+            mbar_init(&sm.cfree[s], 1);
+            mbar_arrive(&sm.cfree[s]);  // the slot starts free (its phase 0 is complete)
         }
         g_trace_n[0] = g_trace_n[1] = g_trace_n[2] = 0u;
+        for (int s = 0; s < S; ++s) sm.tcnt[s] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
@@ -1270,10 +1217,6 @@ __global__ void __launch_bounds__(kThreads, StageCfg<ELT>::kMinBlocks) lp_stream
     const int warp = tid >> 5;
     if (warp == kWarps) {
         if (tid == kConsumerThreads) producer_loop<ELT>(p, sm, stages, t0);
-        return;
-    }
-    if (warp == kWarps + 1) {
-        merge_loop<ELT>(p, sm, t0);
         return;
     }
     compute_loop<ELT>(p, sm, stages, t0);
@@ -1383,8 +1326,8 @@ __device__ __noinline__ void record_block(const Params& p, RecShared& sm, int ro
         sm.rec[w] = (w >= 2 && (w & 1) == 0) ? -1 : (int)kUnusedBits;
     // loads: tile partials, the chosen logit, explicit-id logits, tile key lists
     float m = kNegInf, s = 0.0f;
-    for (int t = tid; t < T; t += kConsumerThreads) {
-        const float2 ms = __ldcg(&p.part_ms[base + t]);
+    for (int t = tid; t < T * kWarps; t += kConsumerThreads) {  // one (max, exp-sum) per warp of each tile
+        const float2 ms = __ldcg(&p.part_ms[base * kWarps + t]);
         ms_merge(m, s, ms.x, ms.y);
     }
     float xc = 0.0f;

@@ -97,7 +97,7 @@ Layout layout_of(const lp_plan_desc* d) {
     L.rec_tasks = off;
     off = align_up(off + rows * sizeof(int4));
     L.part_ms = off;
-    L.part_ms_bytes = rows * T * sizeof(float2);
+    L.part_ms_bytes = rows * T * (lp::kConsumerThreads / 32) * sizeof(float2);
     off = align_up(off + L.part_ms_bytes);
     L.part_keys = off;
     L.part_keys_bytes = rows * T * lp::kKeysPerTile * sizeof(unsigned long long);
