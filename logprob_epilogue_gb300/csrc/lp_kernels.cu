@@ -1024,6 +1024,8 @@ __device__ __forceinline__ bool tile_work(const Params& p, Shared& sm, const uns
     if (om == omx && m > kNegInf) id = (uint32_t)(tbase + first_equal<ELT, FULL>(sp, tid, nv, m, cm));
     const uint32_t idmin = __reduce_min_sync(kFull, id);
     const unsigned long long wkey = ((unsigned long long)omx << 32) | (unsigned long long)(~idmin);
+    // into the row's best key now: long complete when the tile is counted below
+    if (lane == 0) atomicMax(&p.row_best[info.x], wkey);
     // pass 2: sum exp(x - m) = 2^(x*log2e - mb - mb_lo): mb_lo, the rounding
     // residual of m*log2e, is applied once, so large |m| costs no accuracy
     float s = 0.0f;
@@ -1061,9 +1063,6 @@ __device__ __forceinline__ bool tile_work(const Params& p, Shared& sm, const uns
     const float sw = warp_sum_f(sc);
     bool counted = false;
     if (lane == 0) {
-        const long long wslot = ((long long)info.x * p.T + info.y) * kWarps + warp;
-        p.part_ms[wslot] = make_float2(Mw, sw);
-        atomicMax(&p.row_best[info.x], wkey);
         if (atomic_add_acq_rel_cta_shared(&sm.tcnt[stage], 1) == kWarps - 1) {
             sm.tcnt[stage] = 0;  // the stage is not refilled before this warp releases it below
             pd.old = (unsigned)atomic_add_acq_rel(&p.done[info.x], 1);  // read back at the next resolve
@@ -1071,6 +1070,9 @@ __device__ __forceinline__ bool tile_work(const Params& p, Shared& sm, const uns
             pd.entry = info.z;
             counted = true;
         }
+        // read only by the record kernel: no ordering with the count needed
+        const long long wslot = ((long long)info.x * p.T + info.y) * kWarps + warp;
+        p.part_ms[wslot] = make_float2(Mw, sw);
     }
     pd.valid = __shfl_sync(kFull, counted, 0);
     __syncwarp();
