@@ -98,7 +98,8 @@ struct Params {
     unsigned long long* row_best;   // [max_rows] best (argmax) key over the finished tiles
     int4* gdesc;          // [max_groups] x = first row, y = k | mode << 8 | explicit << 12 |
                           // requested << 13, z = top_k or id count, w = sampled token
-    int4* rec_tasks;      // [max_rows] per row: (chosen token, queue entry, 1 = record to build, 0)
+    int4* rec_tasks;      // [max_rows] per row: (chosen token, queue entry, group descriptor word, count);
+                          // descriptor word 0: no record to build
     float2* part_ms;      // [max_rows * T * 8] (max, exp-sum) of each compute warp's share of a tile
     unsigned long long* part_keys;  // [max_rows * T * 32] tile keys, descending
     unsigned long long timeout_ns;

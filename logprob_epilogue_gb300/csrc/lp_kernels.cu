@@ -1179,7 +1179,7 @@ __device__ __noinline__ int decide_row(const Params& p, int row, int entry, unsi
     }
     if (req) {
         if (chosen >= p.V) atomicOr(p.status, kStatusBadToken);
-        p.rec_tasks[row] = make_int4(chosen, entry, 1, 0);  // built by the record kernel
+        p.rec_tasks[row] = make_int4(chosen, entry, d.y, d.z);  // built by the record kernel
     }
     *terminal = !accept;
     trace(p, kTrDecision, row, accept ? 1 : 0, true);
@@ -1316,11 +1316,11 @@ __device__ __forceinline__ void ms_merge(float& m, float& s, float m2, float s2)
 // natural alternatives (each warp merges every 8th tile list, warp 0 merges
 // the 8).  Every global load is issued before the first barrier.
 template <int ELT>
-__device__ __noinline__ void record_block(const Params& p, RecShared& sm, int row, int entry, int chosen) {
+__device__ __noinline__ void record_block(const Params& p, RecShared& sm, int row, int entry, int chosen, int dy,
+                                          int kc) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = entry >> 4;
-    const int4 d = __ldcg(&p.gdesc[g]);
-    const int mode = (d.y >> 8) & 3, ids = (d.y >> 12) & 1, kc = d.z;
+    const int mode = (dy >> 8) & 3, ids = (dy >> 12) & 1;
     const int T = p.T;
     const long long base = (long long)row * T;
     const bool natural = !ids && mode == kModeNatural && kc > 0;
@@ -1362,12 +1362,14 @@ __device__ __noinline__ void record_block(const Params& p, RecShared& sm, int ro
     if (tid == 32) sm.xchosen = xc;
     cbar();
     if (warp == 0) {
-        // lse = M + log(sum_t s_t exp(m_t - M)), rounded once to FP32
+        // lse = M + log(sum_t s_t exp(m_t - M)); S >= 1 holds the maximum's own
+        // term, so logf(S) is accurate to an ulp of a small number and the sum
+        // rounds once (FP64 is slow on this part and buys nothing here)
         float M = sm.red_f[0], S = sm.red_f2[0];
 #pragma unroll
         for (int w = 1; w < 8; ++w) ms_merge(M, S, sm.red_f[w], sm.red_f2[w]);
         float lse = 0.0f;
-        if (lane == 0) lse = __double2float_rn((double)M + log((double)S));
+        if (lane == 0) lse = M + logf(S);
         lse = __shfl_sync(kFull, lse, 0);
         if (lane == 0) {
             sm.lse = lse;
@@ -1410,8 +1412,8 @@ __global__ void __launch_bounds__(kConsumerThreads) lp_record_kernel(Params p) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (vload(&p.ctrl->abort) != 0u) return;
     for (int row = blockIdx.x; row < p.rows; row += gridDim.x) {
-        const int4 t = __ldcg(&p.rec_tasks[row]);
-        if (t.z == 1) record_block<ELT>(p, rs, row, t.y, t.x);
+        const int4 t = __ldcg(&p.rec_tasks[row]);  // (chosen, queue entry, descriptor word, count); 0 word: none
+        if (t.z != 0) record_block<ELT>(p, rs, row, t.y, t.x, t.z, t.w);
     }
 }
 
@@ -1466,8 +1468,8 @@ cudaError_t launch_epilogue(const Params& p, int dtype, const LaunchCfg& cfg, cu
     lc.numAttrs = 1;
     e = dtype == 1 ? cudaLaunchKernelEx(&lc, lp_stream_kernel<2>, p) : cudaLaunchKernelEx(&lc, lp_stream_kernel<4>, p);
     if (e != cudaSuccess) return e;
-    // records: one CTA per requesting row, at most two per SM (grid-stride)
-    int rgrid = p.rows < 2 * cfg.sms ? p.rows : 2 * cfg.sms;
+    // records: one CTA per row (rows without a record return at once)
+    int rgrid = p.rows;
     if (rgrid < 1) rgrid = 1;
     cudaLaunchConfig_t rc = {};
     rc.gridDim = dim3(rgrid);
