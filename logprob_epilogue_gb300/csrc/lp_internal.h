@@ -76,6 +76,7 @@ struct Params {
     const void* logits;
     long long V, Vp;      // elements
     int rows, G, T;       // T = tiles per row
+    int stream_grid;      // CTAs of the stream kernel (CTA b takes fresh item b first)
     int k_max, k_alt_max, max_ids;
     // inputs
     const int* indptr;

@@ -490,6 +490,22 @@ __device__ __forceinline__ unsigned long long queue_entry(int gj, int row, int m
 
 // ------------------------------------------------------------------ prepare
 
+// Inputs of one group, loaded together (one memory round trip).
+struct GroupIn {
+    int r0, r1, req, samp, cnt, K;
+};
+
+__device__ __forceinline__ GroupIn load_group(const Params& p, int g) {
+    GroupIn x;
+    x.r0 = __ldg(&p.indptr[g]);
+    x.r1 = __ldg(&p.indptr[g + 1]);
+    x.req = __ldg(&p.requested[g]);
+    x.samp = __ldg(&p.sampled[g]);
+    x.cnt = __ldg(&p.id_counts[g]);
+    x.K = __ldg(&p.top_k[g]);
+    return x;
+}
+
 __global__ void __launch_bounds__(1024) lp_prepare_kernel(Params p) {
     asm volatile("griddepcontrol.launch_dependents;");
     if (p.trace != nullptr && threadIdx.x == 0) {
@@ -502,21 +518,25 @@ __global__ void __launch_bounds__(1024) lp_prepare_kernel(Params p) {
     __shared__ int s_base;
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
-    for (int r = tid; r < p.rows; r += blockDim.x) {
+    const int G = p.G;
+    const int nthr = blockDim.x;
+    // this thread's first group: its inputs are in flight while the rows are reset
+    GroupIn in0 = {0, 1, 0, 0, 0, 0};
+    if (tid < G) in0 = load_group(p, tid);
+    for (int r = tid; r < p.rows; r += nthr) {
         p.done[r] = 0;
         p.queue[r] = ~0ull;
         p.row_best[r] = 0ull;
         p.rec_tasks[r] = make_int4(0, 0, 0, 0);
     }
     if (tid == 0) *p.status = 0u;
-    const int G = p.G;
+    // validation: indptr starts at >= 0, ends at <= rows, group sizes 1..k_max+1
     int ok = 1;
-    if (G > 0) {
-        if (tid == 0) ok = (p.indptr[0] >= 0) && (p.indptr[G] <= p.rows);
-        for (int g = tid; g < G; g += blockDim.x) {
-            const int size = p.indptr[g + 1] - p.indptr[g];
-            if (size < 1 || size - 1 > p.k_max) ok = 0;
-        }
+    for (int g = tid; g < G; g += nthr) {
+        const GroupIn x = g == tid ? in0 : load_group(p, g);
+        if (x.r1 - x.r0 < 1 || x.r1 - x.r0 - 1 > p.k_max) ok = 0;
+        if (g == 0 && x.r0 < 0) ok = 0;
+        if (g == G - 1 && x.r1 > p.rows) ok = 0;
     }
     ok = __syncthreads_and(ok);
     if (!ok) {
@@ -534,16 +554,17 @@ __global__ void __launch_bounds__(1024) lp_prepare_kernel(Params p) {
     if (tid == 0) s_base = 0;
     __syncthreads();
     unsigned st = 0;
-    for (int g0 = 0; g0 < G; g0 += blockDim.x) {
+    for (int g0 = 0; g0 < G; g0 += nthr) {
         const int g = g0 + tid;
         int need = 0, row0 = 0, mode0 = 0;
         if (g < G) {
-            const int r0 = p.indptr[g];
-            const int k = p.indptr[g + 1] - r0 - 1;
-            const int req = p.requested[g] != 0;
-            const int samp = p.sampled[g];
-            int cnt = p.id_counts[g];
-            int K = p.top_k[g];
+            const GroupIn x = g0 == 0 ? in0 : load_group(p, g);
+            const int r0 = x.r0;
+            const int k = x.r1 - r0 - 1;
+            const int req = x.req != 0;
+            const int samp = x.samp;
+            int cnt = x.cnt;
+            int K = x.K;
             int mode = kModeArgmax, kc = 0, ids = 0;
             if (req) {
                 if (cnt < 0 || cnt > p.max_ids) {
@@ -596,7 +617,7 @@ __global__ void __launch_bounds__(1024) lp_prepare_kernel(Params p) {
     }
     if (st) atomicOr(p.status, st);
     if (p.trace != nullptr) {
-        for (int i = tid; i < p.trace_ctas * 3; i += blockDim.x) p.trace_count[i] = 0u;
+        for (int i = tid; i < p.trace_ctas * 3; i += nthr) p.trace_count[i] = 0u;
     }
     if (tid == 0) {
         if (p.trace != nullptr) {
@@ -604,7 +625,8 @@ __global__ void __launch_bounds__(1024) lp_prepare_kernel(Params p) {
             e[2] = globaltimer();
             e[3] = (unsigned long long)kTrPrepEnd << 56;
         }
-        p.ctrl->fresh_next = 0u;
+        // the stream kernel's CTA b takes fresh item b first, without a claim
+        p.ctrl->fresh_next = static_cast<unsigned>(p.stream_grid);
         p.ctrl->chain_next = 0u;
         p.ctrl->chain_tail = 0u;
         p.ctrl->fresh_rows = static_cast<unsigned>(s_base);
@@ -633,12 +655,15 @@ __device__ __noinline__ void producer_loop(const Params& p, Shared& sm, unsigned
     const uint64_t policy = evict_first_policy();
     Ctrl* ctrl = p.ctrl;
     const unsigned T = (unsigned)p.T;
-    // first claims in parallel: one chained, one fresh
-    unsigned chain_claim = atomicAdd(&ctrl->chain_next, 1u);
-    unsigned fresh_ahead = atomicAdd(&ctrl->fresh_next, 1u);
+    // fresh item b is this CTA's first (the counter starts past the grid); its
+    // entry is loaded with the depth-0 row count, and the first chained claim
+    // waits until the first copy is issued
+    unsigned chain_claim = kNone;
+    unsigned fresh_ahead = blockIdx.x;
+    const unsigned first_pos = blockIdx.x / T;
+    unsigned long long fresh_entry = first_pos < (unsigned)p.rows ? vload(&p.queue[first_pos]) : ~0ull;
     const unsigned F = vload(&ctrl->fresh_rows);
     const unsigned fresh_items = F * T;
-    unsigned long long fresh_entry = fresh_ahead < fresh_items ? vload(&p.queue[fresh_ahead / T]) : ~0ull;
     bool fresh_done = fresh_ahead >= fresh_items;
     int stage = 0;
     uint32_t phase = 0;
@@ -653,12 +678,11 @@ __device__ __noinline__ void producer_loop(const Params& p, Shared& sm, unsigned
             }
             timed_out = true;
         } else {
-            if (chain_claim == kNone) chain_claim = atomicAdd(&ctrl->chain_next, 1u);
             unsigned long long e = ~0ull;
             unsigned tile = 0;
             for (;;) {
                 // the chained item, once the queue entry of its row is published
-                const unsigned cpos = F + chain_claim / T;
+                const unsigned cpos = chain_claim == kNone ? kNone : F + chain_claim / T;
                 if (cpos < (unsigned)p.rows) {
                     e = vload(&p.queue[cpos]);
                     if ((long long)e >= 0) {
@@ -679,11 +703,15 @@ __device__ __noinline__ void producer_loop(const Params& p, Shared& sm, unsigned
                     if (!fresh_done) fresh_entry = vload(&p.queue[fresh_ahead / T]);
                     continue;
                 }
+                if (chain_claim == kNone) {
+                    chain_claim = atomicAdd(&ctrl->chain_next, 1u);
+                    continue;
+                }
                 // nothing to take yet: the run is complete once no group is outstanding
                 if (vload(&ctrl->outstanding) <= 0) {
                     __threadfence();
                     // final once nothing is outstanding: a claim below it has its entry published
-                    if (chain_claim / T < vload(&ctrl->chain_tail)) continue;
+                    if (chain_claim != kNone && chain_claim / T < vload(&ctrl->chain_tail)) continue;
                     e = ~0ull;
                     break;
                 }
@@ -721,8 +749,9 @@ __device__ __noinline__ void producer_loop(const Params& p, Shared& sm, unsigned
             stage = 0;
             phase ^= 1u;
         }
-        // the next fresh item and its entry (depth-0 entries are all published),
-        // overlapping the next stage wait
+        // the next chained claim, and the next fresh item with its entry (depth-0
+        // entries are all published), overlapping the next stage wait
+        if (chain_claim == kNone) chain_claim = atomicAdd(&ctrl->chain_next, 1u);
         if (!fresh_done && fresh_ahead == kNone) {
             fresh_ahead = atomicAdd(&ctrl->fresh_next, 1u);
             fresh_done = fresh_ahead >= fresh_items;
@@ -1449,13 +1478,15 @@ cudaError_t query_launch_cfg(int dtype, LaunchCfg* cfg) {
     return cudaSuccess;
 }
 
-cudaError_t launch_epilogue(const Params& p, int dtype, const LaunchCfg& cfg, cudaStream_t stream) {
+cudaError_t launch_epilogue(const Params& p_in, int dtype, const LaunchCfg& cfg, cudaStream_t stream) {
+    long long work = (long long)p_in.rows * p_in.T;
+    int grid = cfg.grid;
+    if (work < grid) grid = work > 0 ? (int)work : 1;
+    Params p = p_in;
+    p.stream_grid = grid;
     lp_prepare_kernel<<<1, 1024, 0, stream>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    long long work = (long long)p.rows * p.T;
-    int grid = cfg.grid;
-    if (work < grid) grid = work > 0 ? (int)work : 1;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
