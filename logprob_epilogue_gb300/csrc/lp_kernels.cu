@@ -638,13 +638,14 @@ __global__ void __launch_bounds__(1024) lp_prepare_kernel(Params p) {
 // ------------------------------------------------------------------ producer
 //
 // One lane draws work items one at a time and streams each 32 KiB tile into a
-// shared-memory stage with a TMA bulk copy.  Chained items (rows appended after
-// an acceptance) come first: each producer always owns the next chained item
-// it claimed (claims run ahead of the appended rows, in order) and takes it as
-// soon as the queue entry of its row is published; otherwise it takes a fresh
-// item, claimed one ahead with its queue entry already loaded.  Rows deep in a
-// verify chain therefore start at once instead of queueing behind the depth-0
-// rows, and single-item claims spread a row's tiles over many CTAs.
+// shared-memory stage with a TMA bulk copy.  Fresh items (tiles of the depth-0
+// rows, the roots of every verify chain) come first, claimed one ahead with
+// their queue entries prefetched, so all chains start as early as the
+// bandwidth allows.  Then come chained items (rows appended after an
+// acceptance): each producer owns the next chained item it claimed (claims
+// run ahead of the appended rows, in order) and takes it as soon as the queue
+// entry of its row is published.  Single-item claims spread a row's tiles over
+// many CTAs.
 constexpr unsigned kNone = 0xFFFFFFFFu;
 
 template <int ELT>
@@ -681,6 +682,12 @@ __device__ __noinline__ void producer_loop(const Params& p, Shared& sm, unsigned
             unsigned long long e = ~0ull;
             unsigned tile = 0;
             for (;;) {
+                if (!fresh_done && fresh_ahead != kNone) {
+                    e = fresh_entry;
+                    tile = fresh_ahead % T;
+                    fresh_ahead = kNone;  // the next one is claimed once this copy is issued
+                    break;
+                }
                 // the chained item, once the queue entry of its row is published
                 const unsigned cpos = chain_claim == kNone ? kNone : F + chain_claim / T;
                 if (cpos < (unsigned)p.rows) {
@@ -690,12 +697,6 @@ __device__ __noinline__ void producer_loop(const Params& p, Shared& sm, unsigned
                         chain_claim = kNone;
                         break;
                     }
-                }
-                if (!fresh_done && fresh_ahead != kNone) {
-                    e = fresh_entry;
-                    tile = fresh_ahead % T;
-                    fresh_ahead = kNone;  // the next one is claimed once this copy is issued
-                    break;
                 }
                 if (!fresh_done) {
                     fresh_ahead = atomicAdd(&ctrl->fresh_next, 1u);
