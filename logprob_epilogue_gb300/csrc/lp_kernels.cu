@@ -721,7 +721,6 @@ __device__ __noinline__ void producer_loop(const Params& p, Shared& sm, unsigned
                     e = ~0ull;
                     break;
                 }
-                __nanosleep(32);
             }
             if ((long long)e >= 0)
                 item = make_int4((int)(e & 0x0FFFFFFFu), (int)tile, (int)(e >> 32), (int)((e >> 28) & 3u));
