@@ -16,13 +16,13 @@
  *      +0 are one value).  The group emits rows 0..a: the chosen token of row
  *      j is its argmax (equal to the draft for j < a; the correction or bonus
  *      token for j = a).  A k = 0 group emits one row whose chosen token is
- *      sampled_tokens[g] when that is >= 0, else the argmax.
- *      ("with a accepted drafts ... produces a+1 newly generated tokens")
+ *      sampled_tokens[g] when that is >= 0, else the argmax.  (mtp-design.md,
+ *      same section, step 3: a accepted drafts yield a + 1 new tokens.)
  *   2. For every emitted row of a group whose requested[g] is nonzero:
  *      lse = log sum_v exp(logits[v]) over the V unpadded lanes, accumulated
  *      in FP32; lp(v) = fl32(logits[v] - lse), -0 reported as +0.
- *      ("report logits[t] - logsumexp(logits) over the full vocabulary ...,
- *      accumulating in FP32")
+ *      (logprobs-design.md, opening paragraph: the logprob of token t is its
+ *      logit minus the logsumexp of the whole vocabulary, summed in FP32.)
  *   3. The record of that row (258 int32 words):
  *        [0] chosen token id, [1] FP32 bits of its lp,
  *        [2+2i], [3+2i] = (id, lp bits) of alternative i:
@@ -31,14 +31,23 @@
  *            created by the FP32 subtraction included;
  *          - id_counts[g] = c > 0: token_ids[g][0..c) in caller order;
  *        every other pair = (-1, 0x7FC00000).
- *      ("chosen token ID, chosen FP32 logprob bits, then pairs of alternative
- *      ID and FP32 logprob bits"; "unused alternative IDs are -1")
- *   4. Rows past a group's emitted prefix are never read; a k = 0 group with
+ *      (logprobs-design.md, packed-position paragraph: the chosen id and the
+ *      bits of its FP32 logprob come first, then one (id, FP32 bits) pair per
+ *      alternative, with -1 as the id of every unused pair.)
+ *   4. Rows past a group's emitted prefix affect no output; a k = 0 group with
  *      requested[g] == 0 and sampled_tokens[g] >= 0 reads nothing.  Records of
  *      rows that are not emitted, or whose group is not requested, are not
- *      written.  ("A packed request's columns beyond its committed prefix are
- *      never read"; "A zero request flag bypasses vocabulary reads, sorting,
- *      and payload writes")
+ *      written.  By default such rows are not read either.  With
+ *      LP_PLAN_READ_AHEAD, producers that would otherwise idle may read the
+ *      row after a row still being decided, so that a verify chain can
+ *      advance as soon as each decision is made; results are the same, and
+ *      at most the first row past each prefix is read.
+ *      (logprobs-design.md, the paragraphs on the speculative writer and on
+ *      the request flag: positions past a request's committed prefix are left
+ *      unread there, because in its packed layout they may belong to another
+ *      request; a zero request flag skips the vocabulary pass, the sort and
+ *      the record.  Here every row of the block belongs to its group, so a
+ *      read-ahead read is safe.)
  *
  * Lifetime: lp_plan_create allocates all device scratch once; lp_bind records
  * caller-owned device pointers; lp_run only enqueues kernels on the caller's
@@ -91,6 +100,7 @@ enum {
 
 /* Plan flags. */
 #define LP_PLAN_HOST_STAGING 0x1u     /* also allocate device staging so lp_run_host can be used */
+#define LP_PLAN_READ_AHEAD 0x2u       /* idle producers may read the row after one being decided */
 #define LP_PLAN_DEBUG_FORCE_TIMEOUT 0x100u /* test hook: every bounded wait runs out (no reads) */
 #define LP_PLAN_DEBUG_TRACE 0x200u    /* record a device timeline of each run (see lp_debug_trace) */
 
@@ -179,7 +189,8 @@ int lp_run_host(lp_plan_t plan, const lp_io* host_io, void* stream);
 int lp_run_host_bytes(lp_plan_t plan, const lp_io* host_io, int64_t* h2d, int64_t* d2h);
 
 /* Debug: number of vocabulary tiles the last run read for each row (0 = the
- * row was never read), copied into host_tiles[0..rows).  Synchronises the
+ * row was never read), copied into host_tiles[0..rows).  With
+ * LP_PLAN_READ_AHEAD the first row past a prefix may show read-ahead tiles.  Synchronises the
  * plan's last stream.  A tile is 32 KiB of logits: 16384 BF16 or 8192 FP32
  * elements (the last tile of a row may be shorter). */
 int lp_debug_tiles_read(lp_plan_t plan, int32_t* host_tiles, int32_t rows);
@@ -224,7 +235,7 @@ int lp_plan_tiles_per_row(lp_plan_t plan);
  *   stream  a cudaStream_t (NULL = legacy default stream).
  *
  * The scratch a run needs grows with io->rows * ceil(V / tile elements)
- * (about 320 bytes per row tile, plus 36 bytes per row and 16 per group);
+ * (about 320 bytes per row tile, plus 48 bytes per row and 16 per group);
  * a run that needs more than LP_STATIC_SCRATCH_BYTES is rejected with
  * LP_ESCRATCH before anything is enqueued.  4 MiB covers, for example, 512
  * rows of a 248,448-lane BF16 vocabulary.

@@ -28,6 +28,7 @@ STATUS_BAD_COUNT = 0x4
 STATUS_BAD_GROUP = 0x8
 STATUS_TIMEOUT = 0x10
 PLAN_HOST_STAGING = 0x1
+PLAN_READ_AHEAD = 0x2
 PLAN_DEBUG_FORCE_TIMEOUT = 0x100
 PLAN_DEBUG_TRACE = 0x200
 
@@ -127,9 +128,10 @@ def _check(rc: int, what: str) -> None:
 
 
 def make_desc(*, max_rows, max_groups, k_max, V, V_padded=None, dtype="bf16", k_alt_max=20, max_ids=128,
-              device=0, host_staging=False, timeout_ns=0, debug_force_timeout=False, trace=False) -> PlanDesc:
+              device=0, host_staging=False, timeout_ns=0, debug_force_timeout=False, trace=False,
+              read_ahead=False) -> PlanDesc:
     flags = (PLAN_HOST_STAGING if host_staging else 0) | (PLAN_DEBUG_FORCE_TIMEOUT if debug_force_timeout else 0)
-    flags |= PLAN_DEBUG_TRACE if trace else 0
+    flags |= (PLAN_DEBUG_TRACE if trace else 0) | (PLAN_READ_AHEAD if read_ahead else 0)
     return PlanDesc(int(max_rows), int(max_groups), int(k_max), int(V), int(V if V_padded is None else V_padded),
                     LP_BF16 if dtype == "bf16" else (LP_F32 if dtype == "f32" else 99), int(k_alt_max),
                     int(max_ids), int(device), flags, int(timeout_ns))

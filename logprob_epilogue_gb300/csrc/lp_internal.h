@@ -46,6 +46,13 @@ template <> struct StageCfg<4> {
     static constexpr int kMinBlocks = LP_F32_CTAS;
 };
 
+// done[row] bit set once the row's parent has accepted (depth-0 rows: by the
+// prepare kernel); the row is decided by whichever increment completes
+// T + kParentDone.
+constexpr int kParentDone = 1 << 24;
+// tclaim[row] offset that ends read-ahead claims on the row.
+constexpr unsigned kClosed = 1u << 30;
+
 // Row modes (what a read row needs).
 enum : int { kModeArgmax = 0, kModeLse = 1, kModeNatural = 2, kModeRecord = 3 };
 
@@ -56,6 +63,11 @@ enum : int { kModeArgmax = 0, kModeLse = 1, kModeNatural = 2, kModeRecord = 3 };
 // tile, handed out by fresh_next); rows appended after an acceptance take
 // positions fresh_rows + j ("chained" items c = j*T + tile, handed out by
 // chain_next, in order, before any fresh item once their row is appended).
+//
+// Read-ahead (plans with LP_PLAN_READ_AHEAD): a producer that streamed a
+// tile of a row with a successor in its group may, while it has nothing else
+// to do, stream tiles of that successor before the row is decided, claimed
+// one at a time through the successor's claim counter (tclaim).
 struct Ctrl {
     unsigned int fresh_next;  // fresh items handed out
     unsigned int pad0[31];
@@ -95,7 +107,10 @@ struct Params {
     // scratch
     Ctrl* ctrl;
     unsigned long long* queue;  // [max_rows] work queue (see queue_entry), all ones = not yet published
-    int* done;            // [max_rows] tiles finished
+    unsigned int* tclaim; // [max_rows] tiles of the row claimed by read-ahead; kClosed added once
+                          // the row's parent is decided
+    int* done;            // [max_rows] tiles finished; with read-ahead, plus kParentDone once the row
+                          // must be decided (depth-0 rows from the start, others when their parent accepts)
     unsigned long long* row_best;   // [max_rows] best (argmax) key over the finished tiles
     int4* gdesc;          // [max_groups] x = first row, y = k | mode << 8 | explicit << 12 |
                           // requested << 13, z = top_k or id count, w = sampled token
@@ -105,6 +120,9 @@ struct Params {
     unsigned long long* part_keys;  // [max_rows * T * 32] tile keys, descending
     unsigned long long timeout_ns;
     unsigned int debug_flags;
+    int read_ahead;       // 0: rows past a group's emitted prefix are never read
+    int done_last;        // done[row] before the increment that completes a row: T - 1, plus
+                          // kParentDone with read-ahead
     // optional timeline (nullptr unless the plan traces)
     unsigned long long* trace;    // [(trace_ctas * 3 + 1) * trace_cap * 2]
     unsigned int* trace_count;    // [trace_ctas * 3]

@@ -487,6 +487,14 @@ __device__ __forceinline__ float load_logit(const Params& p, int row, long long 
 __device__ __forceinline__ unsigned long long queue_entry(int gj, int row, int mode) {
     return ((unsigned long long)(uint32_t)gj << 32) | (unsigned long long)(uint32_t)(row | (mode << 28));
 }
+// Entry flags.  kEntryNext: the group has a row after this one (a read-ahead
+// candidate).  Chained entries only: kEntryShared, the row's tiles are claimed
+// through tclaim (read-ahead had started on it); kEntrySkip, read-ahead had
+// claimed all of them (nothing to take).
+constexpr unsigned long long kEntryShared = 1ull << 30;
+constexpr unsigned long long kEntrySkip = 1ull << 31;
+constexpr unsigned long long kEntryNext = 1ull << 62;
+__device__ __forceinline__ int entry_gj(unsigned long long e) { return (int)((e >> 32) & 0x3FFFFFFFu); }
 
 // ------------------------------------------------------------------ prepare
 
@@ -526,6 +534,7 @@ __global__ void __launch_bounds__(1024) lp_prepare_kernel(Params p) {
     for (int r = tid; r < p.rows; r += nthr) {
         p.done[r] = 0;
         p.queue[r] = ~0ull;
+        p.tclaim[r] = 0u;
         p.row_best[r] = 0ull;
         p.rec_tasks[r] = make_int4(0, 0, 0, 0);
     }
@@ -553,10 +562,13 @@ __global__ void __launch_bounds__(1024) lp_prepare_kernel(Params p) {
     }
     if (tid == 0) s_base = 0;
     __syncthreads();
+    // without read-ahead a row is decided when its tiles are counted; with it,
+    // also only once its parent accepted (depth-0 rows: from the start)
+    const int parent_bias = p.read_ahead ? kParentDone : 0;
     unsigned st = 0;
     for (int g0 = 0; g0 < G; g0 += nthr) {
         const int g = g0 + tid;
-        int need = 0, row0 = 0, mode0 = 0;
+        int need = 0, row0 = 0, mode0 = 0, k0 = 0;
         if (g < G) {
             const GroupIn x = g0 == 0 ? in0 : load_group(p, g);
             const int r0 = x.r0;
@@ -593,6 +605,7 @@ __global__ void __launch_bounds__(1024) lp_prepare_kernel(Params p) {
             p.gdesc[g] = make_int4(r0, k | (mode << 8) | (ids << 12) | (req << 13), kc, samp);
             row0 = r0;
             mode0 = mode;
+            k0 = k;
         }
         const unsigned bal = __ballot_sync(kFull, need);
         const int pos_in_warp = __popc(bal & ((1u << lane) - 1u));
@@ -610,7 +623,11 @@ __global__ void __launch_bounds__(1024) lp_prepare_kernel(Params p) {
             if (lane == 31) s_total = incl;
         }
         __syncthreads();
-        if (need) p.queue[s_base + s_warp[warp] + pos_in_warp] = queue_entry(g << 4, row0, mode0);
+        if (need) {
+            p.queue[s_base + s_warp[warp] + pos_in_warp] =
+                queue_entry(g << 4, row0, mode0) | (k0 >= 1 ? kEntryNext : 0ull);
+            p.done[row0] = parent_bias;
+        }
         __syncthreads();
         if (tid == 0) s_base += s_total;
         __syncthreads();
@@ -660,6 +677,7 @@ __device__ __noinline__ void producer_loop(const Params& p, Shared& sm, unsigned
     // entry is loaded with the depth-0 row count, and the first chained claim
     // waits until the first copy is issued
     unsigned chain_claim = kNone;
+    unsigned long long ra_e = ~0ull;  // read-ahead candidate: entry of the successor of the last row streamed
     unsigned fresh_ahead = blockIdx.x;
     const unsigned first_pos = blockIdx.x / T;
     unsigned long long fresh_entry = first_pos < (unsigned)p.rows ? vload(&p.queue[first_pos]) : ~0ull;
@@ -688,11 +706,27 @@ __device__ __noinline__ void producer_loop(const Params& p, Shared& sm, unsigned
                     fresh_ahead = kNone;  // the next one is claimed once this copy is issued
                     break;
                 }
-                // the chained item, once the queue entry of its row is published
+                // this poll's loads, issued together: the chained item's entry
+                // and the outstanding groups
                 const unsigned cpos = chain_claim == kNone ? kNone : F + chain_claim / T;
-                if (cpos < (unsigned)p.rows) {
-                    e = vload(&p.queue[cpos]);
-                    if ((long long)e >= 0) {
+                unsigned long long ce = ~0ull;
+                if (cpos < (unsigned)p.rows) ce = vload(&p.queue[cpos]);
+                const int out = fresh_done ? vload(&ctrl->outstanding) : 1;
+                // the chained item, once the queue entry of its row is published
+                if ((long long)ce >= 0) {
+                    e = ce;
+                    if (e & kEntrySkip) {  // read-ahead claimed every tile of the row
+                        chain_claim = kNone;
+                        e = ~0ull;
+                    } else if (e & kEntryShared) {  // read-ahead claimed some: take the next one
+                        chain_claim = kNone;
+                        const unsigned v = atomicAdd(&p.tclaim[e & 0x0FFFFFFFu], 1u);
+                        if (v < T) {
+                            tile = v;
+                            break;
+                        }
+                        e = ~0ull;
+                    } else {
                         tile = chain_claim % T;
                         chain_claim = kNone;
                         break;
@@ -708,11 +742,23 @@ __device__ __noinline__ void producer_loop(const Params& p, Shared& sm, unsigned
                     chain_claim = atomicAdd(&ctrl->chain_next, 1u);
                     continue;
                 }
-                // nothing to take yet: the run is complete once no group is outstanding
-                if (vload(&ctrl->outstanding) <= 0) {
+                // nothing to take yet: with a stage free, read ahead (a tile of
+                // the successor of the last row streamed, not decided yet)
+                if ((long long)ra_e >= 0 && mbar_test_wait(&sm.empty[stage], phase ^ 1u)) {
+                    const unsigned v = atomicAdd(&p.tclaim[ra_e & 0x0FFFFFFFu], 1u);
+                    const unsigned long long se = ra_e;
+                    if (v >= T - 1) ra_e = ~0ull;  // no tile of it left after this claim (or closed)
+                    if (v < T) {
+                        e = se;
+                        tile = v;
+                        break;
+                    }
+                }
+                // the run is complete once no group is outstanding
+                if (out <= 0) {
                     __threadfence();
                     // final once nothing is outstanding: a claim below it has its entry published
-                    if (chain_claim != kNone && chain_claim / T < vload(&ctrl->chain_tail)) continue;
+                    if (chain_claim / T < vload(&ctrl->chain_tail)) continue;
                     e = ~0ull;
                     break;
                 }
@@ -722,8 +768,13 @@ __device__ __noinline__ void producer_loop(const Params& p, Shared& sm, unsigned
                     break;
                 }
             }
-            if ((long long)e >= 0)
-                item = make_int4((int)(e & 0x0FFFFFFFu), (int)tile, (int)(e >> 32), (int)((e >> 28) & 3u));
+            if ((long long)e >= 0) {
+                const int row = (int)(e & 0x0FFFFFFFu), mode = (int)((e >> 28) & 3u);
+                item = make_int4(row, (int)tile, entry_gj(e), mode);
+                // the group's next row becomes this producer's read-ahead candidate
+                // (read-ahead entries carry no kEntryNext: one row ahead at most)
+                if (p.read_ahead && (e & kEntryNext)) ra_e = queue_entry(entry_gj(e) + 1, row + 1, mode);
+            }
         }
         if (timed_out) atomicOr(p.status, kStatusTimeout);
         if (!mbar_wait(&sm.empty[stage], phase ^ 1u, deadline)) {
@@ -996,17 +1047,17 @@ struct Pending {
     int row, entry;
 };
 
-__device__ __noinline__ int decide_row(const Params& p, int row, int entry, unsigned fresh_rows, bool* terminal);
+__device__ __noinline__ bool decide_row(const Params& p, int2* cur);
 
 // Reads the pending count (waiting for it if needed) and decides the row when
-// this warp finished it.
-__device__ __forceinline__ void resolve(const Params& p, Pending& pd, unsigned fresh_rows) {
+// this warp's increment completed it (all tiles counted, parent accepted).
+__device__ __forceinline__ void resolve(const Params& p, Pending& pd) {
     if ((threadIdx.x & 31) == 0 && pd.valid) {
-        if (pd.old == (unsigned)(p.T - 1)) {
-            bool terminal = false;
-            decide_row(p, pd.row, pd.entry, fresh_rows, &terminal);
-            // the record flag and the emitted tokens are written before the group retires
-            if (terminal) atomicSub(&p.ctrl->outstanding, 1);
+        if (pd.old == (unsigned)p.done_last) {
+            // a true result: the next row was accepted into reading and is complete already
+            int2 cur = make_int2(pd.row, pd.entry);
+            while (decide_row(p, &cur)) {
+            }
         }
     }
     pd.valid = false;
@@ -1020,7 +1071,7 @@ __device__ __forceinline__ void resolve(const Params& p, Pending& pd, unsigned f
 template <int ELT, bool FULL>
 __device__ __forceinline__ bool tile_work(const Params& p, Shared& sm, const unsigned char* sp, int nv, int tbase,
                                           const int4& info, int stage, int& ns, uint32_t& nphase, unsigned tcount,
-                                          Pending& pd, unsigned fresh_rows, unsigned long long deadline) {
+                                          Pending& pd, unsigned long long deadline) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int mode = info.w;
     const bool natural = mode == kModeNatural;
@@ -1064,7 +1115,7 @@ __device__ __forceinline__ bool tile_work(const Params& p, Shared& sm, const uns
         s = stage_expsum<ELT, FULL>(sp, tid, nv, mb) * ex2(-mb_lo);
     }
     // the previous tile's count is back by now
-    resolve(p, pd, fresh_rows);
+    resolve(p, pd);
     if (natural) {
         if (__any_sync(kFull, !mbar_wait(&sm.ctheta[ns], npar, deadline))) {
             if (lane == 0) atomicOr(p.status, kStatusTimeout);
@@ -1138,7 +1189,6 @@ __device__ void compute_loop(const Params& p, Shared& sm, unsigned char* stages,
     const int tid = threadIdx.x, lane = tid & 31;
     const unsigned long long deadline = t0 + p.timeout_ns;
     const int V = (int)p.V;
-    const unsigned fresh_rows = vload(&p.ctrl->fresh_rows);
     int stage = 0, ns = 0;
     uint32_t phase = 0, nphase = 0;   // nphase bit r: uses of candidate slot r, mod 2
     unsigned tcount = 0;              // tiles seen (picks the selecting warp)
@@ -1149,14 +1199,14 @@ __device__ void compute_loop(const Params& p, Shared& sm, unsigned char* stages,
     for (;;) {
         // a pending count is read before this warp can block: the row it may
         // complete could be what the next tile waits for
-        if (pd.valid && !mbar_test_wait(&sm.full[stage], phase)) resolve(p, pd, fresh_rows);
+        if (pd.valid && !mbar_test_wait(&sm.full[stage], phase)) resolve(p, pd);
         if (__any_sync(kFull, !mbar_wait(&sm.full[stage], phase, deadline))) {
             if (lane == 0) atomicOr(p.status, kStatusTimeout);
             return;
         }
         const int4 info = sm.info[stage];
         if (info.z < 0) {  // no more tiles
-            resolve(p, pd, fresh_rows);
+            resolve(p, pd);
             return;
         }
         const unsigned char* sp = stages + (size_t)stage * kTileBytes;
@@ -1167,9 +1217,9 @@ __device__ void compute_loop(const Params& p, Shared& sm, unsigned char* stages,
         trace(p, kTrTileStart, info.x, tile, tid == 0);
         bool ok;
         if (__builtin_expect(nv == kTE, 1)) {
-            ok = tile_work<ELT, true>(p, sm, sp, nv, tbase, info, stage, ns, nphase, tcount, pd, fresh_rows, deadline);
+            ok = tile_work<ELT, true>(p, sm, sp, nv, tbase, info, stage, ns, nphase, tcount, pd, deadline);
         } else {
-            ok = tile_work<ELT, false>(p, sm, sp, nv, tbase, info, stage, ns, nphase, tcount, pd, fresh_rows, deadline);
+            ok = tile_work<ELT, false>(p, sm, sp, nv, tbase, info, stage, ns, nphase, tcount, pd, deadline);
         }
         ++tcount;
         if (!ok) return;
@@ -1183,23 +1233,42 @@ __device__ void compute_loop(const Params& p, Shared& sm, unsigned char* stages,
 
 // ------------------------------------------------------------------ decisions
 
-// Acceptance decision of a row whose tiles are all counted (lane 0 of the
-// compute warp whose count completed it): argmax = the row's best key; on
-// acceptance the next row of the group is appended to the chained queue, else
-// the group ends (*terminal).  A requesting row is flagged for the record
-// kernel.  Returns the chosen token.
-__device__ __noinline__ int decide_row(const Params& p, int row, int entry, unsigned fresh_rows, bool* terminal) {
+// Acceptance decision of the row *cur = (row, queue entry), whose tiles are
+// all counted and whose parent accepted (lane 0 of the compute warp whose
+// increment completed it): argmax = the row's best key.  On acceptance the
+// next row of the group must be read: its queue entry is appended (flagged
+// when read-ahead has already claimed some or all of its tiles), it is marked
+// for decision, and the row after it becomes a read-ahead candidate.
+// Otherwise the group ends and read-ahead on the next row stops.  A
+// requesting row is flagged for the record kernel.  Returns true, with *cur
+// advanced to the next row, when read-ahead had already counted every tile of
+// that row: the caller decides it too.
+__device__ __noinline__ bool decide_row(const Params& p, int2* cur) {
+    const unsigned T = (unsigned)p.T;
+    const unsigned fresh_rows = vload(&p.ctrl->fresh_rows);
+    const int row = cur->x, entry = cur->y;
     const int g = entry >> 4, j = entry & 15;
     const int4 d = __ldcg(&p.gdesc[g]);
     const unsigned long long bk = __ldcg(&p.row_best[row]);
     const int draft = __ldg(&p.drafts[row]);
-    const int r0 = d.x, k = d.y & 0xFF, req = (d.y >> 13) & 1, samp = d.w;
+    const int r0 = d.x, k = d.y & 0xFF, req = (d.y >> 13) & 1, samp = d.w, mode = (d.y >> 8) & 3;
     const uint32_t amax = key_id(bk);
     const int chosen = (k == 0 && samp >= 0) ? samp : (int)amax;
     const bool accept = (j < k) && (draft == (int)amax);
+    int next_done = 0;
     if (accept) {
+        // independent round trips, issued together
         const unsigned pos = fresh_rows + atomicAdd(&p.ctrl->chain_tail, 1u);
-        vstore(&p.queue[pos], queue_entry((g << 4) | (j + 1), row + 1, (d.y >> 8) & 3));
+        unsigned long long e = queue_entry((g << 4) | (j + 1), row + 1, mode);
+        if (p.read_ahead) {
+            const unsigned claimed = atomicCAS(&p.tclaim[row + 1], 0u, kClosed);
+            next_done = atomicAdd(&p.done[row + 1], kParentDone);
+            if (j + 2 <= k) e |= kEntryNext;
+            if (claimed != 0u) e |= claimed >= T ? kEntrySkip : kEntryShared;
+        }
+        vstore(&p.queue[pos], e);
+    } else if (p.read_ahead && j < k) {
+        atomicAdd(&p.tclaim[row + 1], kClosed);  // the next row is not needed
     }
     p.emitted[row] = chosen;
     if (!accept) {
@@ -1210,9 +1279,16 @@ __device__ __noinline__ int decide_row(const Params& p, int row, int entry, unsi
         if (chosen >= p.V) atomicOr(p.status, kStatusBadToken);
         p.rec_tasks[row] = make_int4(chosen, entry, d.y, d.z);  // built by the record kernel
     }
-    *terminal = !accept;
     trace(p, kTrDecision, row, accept ? 1 : 0, true);
-    return chosen;
+    if (!accept) {
+        // the record flag and the emitted tokens are written before the group retires
+        atomicSub(&p.ctrl->outstanding, 1);
+        return false;
+    }
+    *cur = make_int2(row + 1, entry + 1);
+    if (next_done != (int)T) return false;  // decided by the increment that completes it
+    __threadfence();  // with the relaxed increment above: acquires the tile counts' releases
+    return true;
 }
 
 template <int ELT>

@@ -23,6 +23,7 @@ struct lp_plan_s {
     size_t scratch_bytes;
     lp::Ctrl* ctrl;
     unsigned long long* queue;
+    unsigned int* tclaim;
     int* done;
     unsigned long long* row_best;
     int4* gdesc;
@@ -74,7 +75,7 @@ int check_desc(const lp_plan_desc* d) {
 }
 
 struct Layout {
-    size_t ctrl, queue, row_best, done, gdesc, rec_tasks, part_ms, part_keys, total;
+    size_t ctrl, queue, tclaim, row_best, done, gdesc, rec_tasks, part_ms, part_keys, total;
     size_t part_ms_bytes, part_keys_bytes;
 };
 
@@ -88,6 +89,8 @@ Layout layout_of(const lp_plan_desc* d) {
     off = align_up(off + sizeof(lp::Ctrl));
     L.queue = off;
     off = align_up(off + rows * sizeof(unsigned long long));
+    L.tclaim = off;
+    off = align_up(off + rows * sizeof(unsigned int));
     L.row_best = off;
     off = align_up(off + rows * sizeof(unsigned long long));
     L.done = off;
@@ -190,6 +193,7 @@ lp::Params make_params(const lp_plan_s* plan, const lp_io& io) {
     p.status = io.status;
     p.ctrl = plan->ctrl;
     p.queue = plan->queue;
+    p.tclaim = plan->tclaim;
     p.row_best = plan->row_best;
     p.done = plan->done;
     p.gdesc = plan->gdesc;
@@ -198,6 +202,8 @@ lp::Params make_params(const lp_plan_s* plan, const lp_io& io) {
     p.part_keys = plan->part_keys;
     p.timeout_ns = (unsigned long long)(plan->d.timeout_ns > 0 ? plan->d.timeout_ns : kDefaultTimeoutNs);
     p.debug_flags = plan->d.flags & LP_PLAN_DEBUG_FORCE_TIMEOUT;
+    p.read_ahead = (plan->d.flags & LP_PLAN_READ_AHEAD) ? 1 : 0;
+    p.done_last = p.T - 1 + (p.read_ahead ? lp::kParentDone : 0);
     p.trace = plan->trace;
     p.trace_count = plan->trace_count;
     p.trace_cap = plan->trace_cap;
@@ -259,6 +265,7 @@ int lp_plan_create(lp_plan_t* out, const lp_plan_desc* desc) {
     plan->scratch_bytes = L.total;
     plan->ctrl = reinterpret_cast<lp::Ctrl*>(plan->scratch + L.ctrl);
     plan->queue = reinterpret_cast<unsigned long long*>(plan->scratch + L.queue);
+    plan->tclaim = reinterpret_cast<unsigned int*>(plan->scratch + L.tclaim);
     plan->row_best = reinterpret_cast<unsigned long long*>(plan->scratch + L.row_best);
     plan->done = reinterpret_cast<int*>(plan->scratch + L.done);
     plan->gdesc = reinterpret_cast<int4*>(plan->scratch + L.gdesc);
@@ -429,6 +436,7 @@ int lp_debug_tiles_read(lp_plan_t plan, int32_t* host_tiles, int32_t rows) {
     cudaError_t e = cudaStreamSynchronize(plan->last_stream);
     if (e == cudaSuccess && rows > 0) e = cudaMemcpy(host_tiles, plan->done, (size_t)rows * 4, cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return cuda_fail(e);
+    for (int32_t r = 0; r < rows; ++r) host_tiles[r] &= lp::kParentDone - 1;  // tile count only
     return LP_OK;
 }
 
@@ -553,6 +561,7 @@ extern "C" int lp_run_static(const lp_plan_desc* desc, const lp_io* io, void* st
     run.T = (int)((desc->V + lp::tile_elems_of_dtype(desc->dtype) - 1) / lp::tile_elems_of_dtype(desc->dtype));
     run.ctrl = reinterpret_cast<lp::Ctrl*>(base + L.ctrl);
     run.queue = reinterpret_cast<unsigned long long*>(base + L.queue);
+    run.tclaim = reinterpret_cast<unsigned int*>(base + L.tclaim);
     run.row_best = reinterpret_cast<unsigned long long*>(base + L.row_best);
     run.done = reinterpret_cast<int*>(base + L.done);
     run.gdesc = reinterpret_cast<int4*>(base + L.gdesc);

@@ -14,7 +14,7 @@
  *   - lse   = log(sum_v exp(x_v)) over the V unpadded lanes, in FP64, then
  *             rounded to FP32 (round to nearest even).
  *   - lp_v  = fl32(x_v - lse), an FP32 subtraction; a -0 result is reported
- *             as +0 ("signed zero is normalized").
+ *             as +0 (logprobs-design.md normalises the sign of a zero result).
  *   - natural alternatives: all v sorted by (lp_v descending, v ascending),
  *             the first min(K, V) reported.
  *   - explicit IDs: lp of each caller ID, in caller order.

@@ -188,7 +188,8 @@ def lpe_tile_elems(dtype: str) -> int:
 
 
 def expected_tiles(w: W.Workload, orc: dict) -> np.ndarray:
-    """Tiles each row must read: all tiles of rows the path reads, 0 elsewhere."""
+    """Tiles each row must read: all tiles of rows the path reads, 0 elsewhere
+    (the exact count of a plan that reads no row past a prefix)."""
     te = lpe_tile_elems(w.dtype)
     T = (w.V + te - 1) // te
     tiles = np.zeros(w.rows, np.int32)
@@ -201,3 +202,27 @@ def expected_tiles(w: W.Workload, orc: dict) -> np.ndarray:
         a = int(orc["accepted"][g])
         tiles[r0:r0 + a + 1] = T
     return tiles
+
+
+def check_tiles(w: W.Workload, orc: dict, tiles: np.ndarray, strict: bool) -> None:
+    """Tiles read per row.  Strict plans read exactly the prefix rows.  With
+    read-ahead, the prefix rows are read in full, the first row past a verify
+    group's prefix may be read in part or in full (it was the successor of a
+    row being decided), and no other row is read."""
+    want = expected_tiles(w, orc)
+    if strict:
+        assert np.array_equal(tiles, want), "tiles read per row"
+        return
+    T = int(want.max()) if want.size and want.max() > 0 else 0
+    allowed = want.copy()
+    for g in range(w.groups):
+        r0, r1 = int(w.group_indptr[g]), int(w.group_indptr[g + 1])
+        if want[r0] == 0:
+            continue
+        nxt = r0 + int(orc["accepted"][g]) + 1
+        if nxt < r1:
+            allowed[nxt] = T
+    prefix = want > 0
+    assert np.array_equal(tiles[prefix], want[prefix]), "prefix rows read in full"
+    assert ((tiles >= 0) & (tiles <= allowed)).all(), "no row read beyond the one after a prefix"
+

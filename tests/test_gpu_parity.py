@@ -11,11 +11,13 @@ pytestmark = pytest.mark.gpu
 THREADS = os.cpu_count() or 8
 
 
-def _check(w, **kw):
+def _check(w, read_ahead=False, **kw):
+    if read_ahead and "plan" not in kw:
+        kw["plan"] = PT.make_plan(w, read_ahead=True)
     gpu, plan = PT.run_gpu(w, **kw)
     orc = PT.run_oracle(w, THREADS)
     stats = PT.compare(w, gpu, orc)
-    assert np.array_equal(gpu["tiles_read"], PT.expected_tiles(w, orc)), "tiles read per row"
+    PT.check_tiles(w, orc, gpu["tiles_read"], strict=not read_ahead)
     plan.close()
     return gpu, orc, stats
 
@@ -31,9 +33,10 @@ SMALL = {
 }
 
 
+@pytest.mark.parametrize("read_ahead", [False, True], ids=["prefix_only", "read_ahead"])
 @pytest.mark.parametrize("name", list(SMALL))
-def test_workload_small(name):
-    _, orc, stats = _check(SMALL[name]())
+def test_workload_small(name, read_ahead):
+    _, orc, stats = _check(SMALL[name](), read_ahead=read_ahead)
     assert stats["rows_written"] > 0
 
 
@@ -47,11 +50,19 @@ def test_workload_full_size(name):
 
 def test_tiny_hand_checked():
     w = W.tiny()
-    gpu, _ = PT.run_gpu(w)
+    gpu, plan = PT.run_gpu(w)
+    plan.close()
     assert gpu["accepted"].tolist() == [2, 0, 0]
     assert gpu["emitted_tokens"][:3].tolist() == [int(w.draft_tokens[0]), int(w.draft_tokens[1]),
                                                   int(w.planted_argmax[2])]
     assert gpu["tiles_read"].tolist() == [1, 1, 1, 0, 1, 0]
+    # with read-ahead only row 3, the successor of the rejecting row 2, may also be read
+    gpu2, plan = PT.run_gpu(w, plan=PT.make_plan(w, read_ahead=True))
+    plan.close()
+    for key in ("records", "accepted", "emitted_tokens", "lse"):
+        assert np.array_equal(gpu[key], gpu2[key]), key
+    t = gpu2["tiles_read"].tolist()
+    assert t[:3] == [1, 1, 1] and t[3] in (0, 1) and t[4:] == [1, 0]
 
 
 def test_wide_tie_all_accepted():
@@ -146,7 +157,8 @@ def test_ragged_vocabularies(V, Vp, dtype):
 
 
 @pytest.mark.parametrize("a", [0, 1, 7, 15])
-def test_acceptance_prefixes_k15(a):
+@pytest.mark.parametrize("read_ahead", [False, True], ids=["prefix_only", "read_ahead"])
+def test_acceptance_prefixes_k15(a, read_ahead):
     rng = np.random.default_rng(100 + a)
     k, V = 15, 20_000
     rows = rng.normal(0, 1, (k + 1, V)).astype(np.float32)
@@ -157,7 +169,7 @@ def test_acceptance_prefixes_k15(a):
     if a < k:
         drafts[a] = (am[a] + 1) % V
     w = _one_group(rows, V, drafts=drafts, top_k=3)
-    gpu, _, _ = _check(w)
+    gpu, _, _ = _check(w, read_ahead=read_ahead)
     assert int(gpu["accepted"][0]) == a
 
 
@@ -187,10 +199,14 @@ def test_flags_and_unread_groups():
 
 def test_poisoned_scratch_and_repeated_runs():
     w = W.spec(groups=6)
-    gpu1, plan = PT.run_gpu(w)
+    gpu1, plan = PT.run_gpu(w, plan=PT.make_plan(w, read_ahead=True))
     gpu2, _ = PT.run_gpu(w, plan=plan, poison=True, runs=3)
-    for key in ("records", "accepted", "emitted_tokens", "lse", "tiles_read"):
+    for key in ("records", "accepted", "emitted_tokens", "lse"):
         assert np.array_equal(gpu1[key], gpu2[key]), key
+    # read-ahead may differ from run to run; the prefix rows may not
+    orc = PT.run_oracle(w, THREADS)
+    PT.check_tiles(w, orc, gpu1["tiles_read"], False)
+    PT.check_tiles(w, orc, gpu2["tiles_read"], False)
     plan.close()
 
 
