@@ -12,7 +12,7 @@ template <int ELT>
 __host__ __device__ constexpr int tile_elems() { return kTileBytes / ELT; }
 inline int tile_elems_of_dtype(int dtype) { return dtype == 1 ? kTileBytes / 2 : kTileBytes / 4; }
 constexpr int kConsumerThreads = 256;   // 8 compute warps
-constexpr int kThreads = kConsumerThreads + 32;  // + 1 producer warp
+constexpr int kThreads = kConsumerThreads + 64;  // + 1 producer warp + 1 selector warp
 #ifndef LP_RING
 #define LP_RING 4
 #endif

@@ -108,22 +108,6 @@ __device__ __forceinline__ T vload(const T* p) { return *reinterpret_cast<const 
 template <typename T>
 __device__ __forceinline__ void vstore(T* p, T v) { *reinterpret_cast<volatile T*>(p) = v; }
 
-// atomicAdd with acquire-release semantics at GPU scope: this thread's earlier
-// writes (and those ordered before it by a warp barrier) are visible to whoever
-// reads the result, and the writes released before the values it reads are
-// visible to this thread afterwards.
-__device__ __forceinline__ int atomic_add_acq_rel_cta_shared(int* p, int v) {
-    int old;
-    asm volatile("atom.acq_rel.cta.shared::cta.add.s32 %0, [%1], %2;" : "=r"(old) : "r"(smem_u32(p)), "r"(v) : "memory");
-    return old;
-}
-
-__device__ __forceinline__ int atomic_add_acq_rel(int* p, int v) {
-    int old;
-    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-    return old;
-}
-
 // ---- optional device timeline (plans created with the trace flag)
 //
 // Each CTA has three event rings (producer, compute, merge warp) of
@@ -272,9 +256,13 @@ static_assert(StageCfg<2>::kStages <= kMaxStages && StageCfg<4>::kStages <= kMax
 
 // Natural-alternative tiles: the 8 compute warps exchange their candidate
 // thresholds and candidates through a slot of this ring (one slot per tile).
+// Tiles handed from the compute warps to the helper warp, in order.
+constexpr int kDoneRing = 4;
+
 struct CandSlot {
     float wTheta[kWarps];                   // the warp's 4th largest thread maximum
     int wcnt[kWarps];                       // keys in cand[w] (<= 32)
+    long long tslot;                        // the tile's index among all row tiles (row * T + tile)
     unsigned long long cand[kWarps][32];    // the warp's keys >= theta (its best 32 if more)
 };
 
@@ -283,9 +271,12 @@ struct Shared {
     uint64_t empty[kMaxStages];      // stage released (8 compute warps)
     uint64_t ctheta[kRing];          // candidate slot: thresholds of the 8 warps written
     uint64_t ccand[kRing];           // candidate slot: candidates of the 8 warps written
-    uint64_t cfree[kRing];           // candidate slot: read by the tile's selecting warp
+    uint64_t cfree[kRing];           // candidate slot: read by the helper warp
+    uint64_t dfull[kDoneRing];       // done slot: the 8 compute warps finished the tile
+    uint64_t dfree[kDoneRing];       // done slot: read by the helper warp
+    int4 dslot[kDoneRing];           // done slot: (row, queue entry, natural, 0) of the tile
+    int sel_exit;                    // compute warps that have finished (the helper stops at 8)
     int4 info[kMaxStages];           // work item of each stage
-    int tcnt[kMaxStages];            // compute warps done with the stage's tile
     CandSlot cs[kRing];
 };
 
@@ -664,6 +655,11 @@ __global__ void __launch_bounds__(1024) lp_prepare_kernel(Params p) {
 // entry of its row is published.  Single-item claims spread a row's tiles over
 // many CTAs.
 constexpr unsigned kNone = 0xFFFFFFFFu;
+// A producer reads ahead only after waiting this long for a chained item.
+#ifndef LP_READ_AHEAD_IDLE_NS
+#define LP_READ_AHEAD_IDLE_NS 1000
+#endif
+constexpr unsigned long long kReadAheadIdleNs = LP_READ_AHEAD_IDLE_NS;
 
 template <int ELT>
 __device__ __noinline__ void producer_loop(const Params& p, Shared& sm, unsigned char* stages, unsigned long long t0) {
@@ -678,6 +674,7 @@ __device__ __noinline__ void producer_loop(const Params& p, Shared& sm, unsigned
     // waits until the first copy is issued
     unsigned chain_claim = kNone;
     unsigned long long ra_e = ~0ull;  // read-ahead candidate: entry of the successor of the last row streamed
+    unsigned long long idle_t0 = 0;   // start of the current wait for a chained item (0: not waiting)
     unsigned fresh_ahead = blockIdx.x;
     const unsigned first_pos = blockIdx.x / T;
     unsigned long long fresh_entry = first_pos < (unsigned)p.rows ? vload(&p.queue[first_pos]) : ~0ull;
@@ -742,9 +739,14 @@ __device__ __noinline__ void producer_loop(const Params& p, Shared& sm, unsigned
                     chain_claim = atomicAdd(&ctrl->chain_next, 1u);
                     continue;
                 }
-                // nothing to take yet: with a stage free, read ahead (a tile of
-                // the successor of the last row streamed, not decided yet)
-                if ((long long)ra_e >= 0 && mbar_test_wait(&sm.empty[stage], phase ^ 1u)) {
+                // nothing to take yet.  After a while without chained items
+                // (their queue has run dry, the verify chains are the work
+                // left) and with a stage free, read ahead: a tile of the
+                // successor of the last row streamed, not decided yet
+                const unsigned long long now = globaltimer();
+                if (idle_t0 == 0) idle_t0 = now;
+                if ((long long)ra_e >= 0 && now - idle_t0 > kReadAheadIdleNs &&
+                    mbar_test_wait(&sm.empty[stage], phase ^ 1u)) {
                     const unsigned v = atomicAdd(&p.tclaim[ra_e & 0x0FFFFFFFu], 1u);
                     const unsigned long long se = ra_e;
                     if (v >= T - 1) ra_e = ~0ull;  // no tile of it left after this claim (or closed)
@@ -762,12 +764,13 @@ __device__ __noinline__ void producer_loop(const Params& p, Shared& sm, unsigned
                     e = ~0ull;
                     break;
                 }
-                if (globaltimer() > deadline) {
+                if (now > deadline) {
                     timed_out = true;
                     e = ~0ull;
                     break;
                 }
             }
+            idle_t0 = 0;
             if ((long long)e >= 0) {
                 const int row = (int)(e & 0x0FFFFFFFu), mode = (int)((e >> 28) & 3u);
                 item = make_int4(row, (int)tile, entry_gj(e), mode);
@@ -1038,30 +1041,7 @@ __device__ __forceinline__ unsigned long long slot_top32(const CandSlot& R, int 
     return r;
 }
 
-// The row's done count taken by a compute warp that finished a tile last; its
-// result is read later (lane 0).  The row's decision falls to the warp whose
-// count completes the row.
-struct Pending {
-    bool valid;
-    unsigned old;     // value the counter held before this warp's increment
-    int row, entry;
-};
-
 __device__ __noinline__ bool decide_row(const Params& p, int2* cur);
-
-// Reads the pending count (waiting for it if needed) and decides the row when
-// this warp's increment completed it (all tiles counted, parent accepted).
-__device__ __forceinline__ void resolve(const Params& p, Pending& pd) {
-    if ((threadIdx.x & 31) == 0 && pd.valid) {
-        if (pd.old == (unsigned)p.done_last) {
-            // a true result: the next row was accepted into reading and is complete already
-            int2 cur = make_int2(pd.row, pd.entry);
-            while (decide_row(p, &cur)) {
-            }
-        }
-    }
-    pd.valid = false;
-}
 
 // The compute warp's share of one tile: passes, candidates (natural tiles,
 // through a candidate slot), then its partial results published to global
@@ -1070,8 +1050,8 @@ __device__ __forceinline__ void resolve(const Params& p, Pending& pd) {
 // FULL = false for the last, partial tile of a row.  False after a timeout.
 template <int ELT, bool FULL>
 __device__ __forceinline__ bool tile_work(const Params& p, Shared& sm, const unsigned char* sp, int nv, int tbase,
-                                          const int4& info, int stage, int& ns, uint32_t& nphase, unsigned tcount,
-                                          Pending& pd, unsigned long long deadline) {
+                                          const int4& info, int stage, int& ns, uint32_t& nphase,
+                                          int& ds, uint32_t& dphase, unsigned long long deadline) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int mode = info.w;
     const bool natural = mode == kModeNatural;
@@ -1104,8 +1084,10 @@ __device__ __forceinline__ bool tile_work(const Params& p, Shared& sm, const uns
     if (om == omx && m > kNegInf) id = (uint32_t)(tbase + first_equal<ELT, FULL>(sp, tid, nv, m, cm));
     const uint32_t idmin = __reduce_min_sync(kFull, id);
     const unsigned long long wkey = ((unsigned long long)omx << 32) | (unsigned long long)(~idmin);
-    // into the row's best key now: long complete when the tile is counted below
-    if (lane == 0) atomicMax(&p.row_best[info.x], wkey);
+    // into the row's best key now; its result is waited for before the tile is
+    // handed over (below), long after it returned
+    unsigned long long prev_best = 0ull;
+    if (lane == 0) prev_best = atomicMax(&p.row_best[info.x], wkey);
     // pass 2: sum exp(x - m) = 2^(x*log2e - mb - mb_lo): mb_lo, the rounding
     // residual of m*log2e, is applied once, so large |m| costs no accuracy
     float s = 0.0f;
@@ -1114,8 +1096,6 @@ __device__ __forceinline__ bool tile_work(const Params& p, Shared& sm, const uns
         const float mb_lo = fmaf(m, kLog2e, -mb);
         s = stage_expsum<ELT, FULL>(sp, tid, nv, mb) * ex2(-mb_lo);
     }
-    // the previous tile's count is back by now
-    resolve(p, pd);
     if (natural) {
         if (__any_sync(kFull, !mbar_wait(&sm.ctheta[ns], npar, deadline))) {
             if (lane == 0) atomicOr(p.status, kStatusTimeout);
@@ -1130,46 +1110,39 @@ __device__ __forceinline__ bool tile_work(const Params& p, Shared& sm, const uns
             warp_top32_exact<ELT>(sp, true, nv, tbase, tid, C.cand[warp]);  // vector layout, -inf past nv
             cw = 32;
         }
-        if (lane == 0) C.wcnt[warp] = cw;
+        if (lane == 0) {
+            C.wcnt[warp] = cw;
+            if (warp == 0) C.tslot = (long long)info.x * p.T + info.y;
+        }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.ccand[ns]);
+        if (lane == 0) mbar_arrive(&sm.ccand[ns]);  // the selector warp takes it from here
     }
-    // partial results of the warp; the last of the 8 warps to finish the tile
-    // counts it for the row (one acquire-release increment per tile, which
-    // publishes the other warps' results too: they are ordered before it by
-    // the CTA-scope count)
+    // partial results of the warp, then the tile goes to the helper warp
+    // through a done slot: once the 8 warps arrived, it counts the tile for
+    // the row
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.empty[stage]);  // no more reads of this stage by this warp
     const float Mw = unord32(omx);
     const float sc = (m > kNegInf && mode != kModeArgmax) ? s * ex2((m - Mw) * kLog2e) : 0.0f;
     const float sw = warp_sum_f(sc);
-    bool counted = false;
     if (lane == 0) {
-        if (atomic_add_acq_rel_cta_shared(&sm.tcnt[stage], 1) == kWarps - 1) {
-            sm.tcnt[stage] = 0;  // the stage is not refilled before this warp releases it below
-            pd.old = (unsigned)atomic_add_acq_rel(&p.done[info.x], 1);  // read back at the next resolve
-            pd.row = info.x;
-            pd.entry = info.z;
-            counted = true;
-        }
-        // read only by the record kernel: no ordering with the count needed
         const long long wslot = ((long long)info.x * p.T + info.y) * kWarps + warp;
         p.part_ms[wslot] = make_float2(Mw, sw);
     }
-    pd.valid = __shfl_sync(kFull, counted, 0);
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.empty[stage]);  // no more reads of this stage by this warp
+    if (__any_sync(kFull, !mbar_wait(&sm.dfree[ds], (dphase >> ds) & 1u, deadline))) {  // slot read
+        if (lane == 0) atomicOr(p.status, kStatusTimeout);
+        return false;
+    }
+    if (lane == 0) {
+        if (warp == 0) sm.dslot[ds] = make_int4(info.x, info.z, natural ? 1 : 0, 0);
+        // the best-key update has returned, so it is performed at its point of
+        // coherence before the count that follows the arrival
+        asm volatile("" ::"l"(prev_best));
+        mbar_arrive(&sm.dfull[ds]);
+    }
+    dphase ^= 1u << ds;
+    if (++ds == kDoneRing) ds = 0;
     if (natural) {
-        if (warp == (int)(tcount & (kWarps - 1))) {
-            // this tile's selecting warp (rotating): the tile's best 32 keys
-            if (__any_sync(kFull, !mbar_wait(&sm.ccand[ns], npar, deadline))) {
-                if (lane == 0) atomicOr(p.status, kStatusTimeout);
-                return false;
-            }
-            const unsigned long long key = slot_top32(C, lane);
-            const long long tslot = (long long)info.x * p.T + info.y;
-            p.part_keys[tslot * kKeysPerTile + lane] = key;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.cfree[ns]);
-        }
         nphase ^= 1u << ns;
         if (++ns == kRing) ns = 0;
     }
@@ -1189,26 +1162,16 @@ __device__ void compute_loop(const Params& p, Shared& sm, unsigned char* stages,
     const int tid = threadIdx.x, lane = tid & 31;
     const unsigned long long deadline = t0 + p.timeout_ns;
     const int V = (int)p.V;
-    int stage = 0, ns = 0;
+    int stage = 0, ns = 0, ds = 0;
     uint32_t phase = 0, nphase = 0;   // nphase bit r: uses of candidate slot r, mod 2
-    unsigned tcount = 0;              // tiles seen (picks the selecting warp)
-    Pending pd;
-    pd.valid = false;
-    pd.old = 0;
-    pd.row = pd.entry = 0;
+    uint32_t dphase = 0;              // dphase bit r: uses of done slot r, mod 2
     for (;;) {
-        // a pending count is read before this warp can block: the row it may
-        // complete could be what the next tile waits for
-        if (pd.valid && !mbar_test_wait(&sm.full[stage], phase)) resolve(p, pd);
         if (__any_sync(kFull, !mbar_wait(&sm.full[stage], phase, deadline))) {
             if (lane == 0) atomicOr(p.status, kStatusTimeout);
             return;
         }
         const int4 info = sm.info[stage];
-        if (info.z < 0) {  // no more tiles
-            resolve(p, pd);
-            return;
-        }
+        if (info.z < 0) return;  // no more tiles
         const unsigned char* sp = stages + (size_t)stage * kTileBytes;
         const int tile = info.y;
         const int tbase = tile * kTE;
@@ -1217,11 +1180,10 @@ __device__ void compute_loop(const Params& p, Shared& sm, unsigned char* stages,
         trace(p, kTrTileStart, info.x, tile, tid == 0);
         bool ok;
         if (__builtin_expect(nv == kTE, 1)) {
-            ok = tile_work<ELT, true>(p, sm, sp, nv, tbase, info, stage, ns, nphase, tcount, pd, deadline);
+            ok = tile_work<ELT, true>(p, sm, sp, nv, tbase, info, stage, ns, nphase, ds, dphase, deadline);
         } else {
-            ok = tile_work<ELT, false>(p, sm, sp, nv, tbase, info, stage, ns, nphase, tcount, pd, deadline);
+            ok = tile_work<ELT, false>(p, sm, sp, nv, tbase, info, stage, ns, nphase, ds, dphase, deadline);
         }
-        ++tcount;
         if (!ok) return;
         trace(p, kTrTileEnd, info.x, tile, tid == 0);
         if (++stage == S) {
@@ -1249,7 +1211,7 @@ __device__ __noinline__ bool decide_row(const Params& p, int2* cur) {
     const int row = cur->x, entry = cur->y;
     const int g = entry >> 4, j = entry & 15;
     const int4 d = __ldcg(&p.gdesc[g]);
-    const unsigned long long bk = __ldcg(&p.row_best[row]);
+    const unsigned long long bk = atomicMax(&p.row_best[row], 0ull);  // read at its point of coherence
     const int draft = __ldg(&p.drafts[row]);
     const int r0 = d.x, k = d.y & 0xFF, req = (d.y >> 13) & 1, samp = d.w, mode = (d.y >> 8) & 3;
     const uint32_t amax = key_id(bk);
@@ -1286,9 +1248,82 @@ __device__ __noinline__ bool decide_row(const Params& p, int2* cur) {
         return false;
     }
     *cur = make_int2(row + 1, entry + 1);
-    if (next_done != (int)T) return false;  // decided by the increment that completes it
-    __threadfence();  // with the relaxed increment above: acquires the tile counts' releases
-    return true;
+    return next_done == (int)T;  // else decided by the increment that completes it
+}
+
+// ------------------------------------------------------------------ helper warp
+//
+// Takes the compute warps' tiles through the done slots, in order: counts each
+// tile for its row, decides the row when its increment completes it, and
+// writes a natural tile's best 32 keys (descending) from its candidate slot.
+// The compute warps never wait on a count or a decision.  Stops when every
+// compute warp has finished and the next slot holds nothing.
+//
+// Ordering without fences.  A decision needs the row's best key complete:
+// every compute warp waits for the result of its best-key atomicMax before
+// its done-slot arrival, so the update has been performed at the key's
+// point of coherence (the L2 slice that owns it) before the count is issued,
+// and the decider reads the key with an atomic at that same point after its
+// own count returned.  The outputs of a decision and the tile partials are
+// read by the record kernel, after this grid has completed.  (An acquire-
+// release count gives the same order through the memory model, but its fence
+// waits for the multiprocessor's outstanding memory traffic, which made the
+// helper's per-tile counts the bottleneck.)
+__device__ __noinline__ void helper_loop(const Params& p, Shared& sm, unsigned long long deadline) {
+    const int lane = threadIdx.x & 31;
+    int ds = 0, ns = 0;
+    uint32_t dphase = 0, nphase = 0;
+    for (;;) {
+        const uint32_t par = (dphase >> ds) & 1u;
+        bool ready = false;
+        for (uint32_t i = 0;; ++i) {
+            if (mbar_test_wait(&sm.dfull[ds], par)) {  // polled: this warp has nothing else to do
+                ready = true;
+                break;
+            }
+            if (vload(&sm.sel_exit) == kWarps) {
+                __threadfence_block();  // every arrival precedes the last exit count
+                ready = mbar_test_wait(&sm.dfull[ds], par);
+                break;
+            }
+            if ((i & 63u) == 63u && globaltimer() > deadline) break;
+        }
+        if (!__all_sync(kFull, ready)) {
+            if (lane == 0 && vload(&sm.sel_exit) != kWarps) atomicOr(p.status, kStatusTimeout);
+            return;
+        }
+        const int4 d = sm.dslot[ds];
+        __syncwarp();
+        int old = 0;
+        if (lane == 0) {
+            mbar_arrive(&sm.dfree[ds]);  // the slot's contents are read
+            old = atomicAdd(&p.done[d.x], 1);
+        }
+        dphase ^= 1u << ds;
+        if (++ds == kDoneRing) ds = 0;
+        // the decision first: the tile's keys are read only by the record kernel
+        if (lane == 0 && old == p.done_last) {
+            int2 cur = make_int2(d.x, d.y);
+            while (decide_row(p, &cur)) {
+            }
+        }
+        __syncwarp();
+        if (d.z) {
+            // a natural tile: its candidates were in before its done slot
+            const uint32_t cpar = (nphase >> ns) & 1u;
+            if (__any_sync(kFull, !mbar_wait(&sm.ccand[ns], cpar, deadline))) {
+                if (lane == 0) atomicOr(p.status, kStatusTimeout);
+                return;
+            }
+            const CandSlot& C = sm.cs[ns];
+            const unsigned long long key = slot_top32(C, lane);
+            p.part_keys[C.tslot * kKeysPerTile + lane] = key;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.cfree[ns]);
+            nphase ^= 1u << ns;
+            if (++ns == kRing) ns = 0;
+        }
+    }
 }
 
 template <int ELT>
@@ -1310,7 +1345,12 @@ __global__ void __launch_bounds__(kThreads, StageCfg<ELT>::kMinBlocks) lp_stream
             mbar_arrive(&sm.cfree[s]);  // the slot starts free (its phase 0 is complete)
         }
         g_trace_n[0] = g_trace_n[1] = g_trace_n[2] = 0u;
-        for (int s = 0; s < S; ++s) sm.tcnt[s] = 0;
+        for (int s = 0; s < kDoneRing; ++s) {
+            mbar_init(&sm.dfull[s], kWarps);
+            mbar_init(&sm.dfree[s], 1);
+            mbar_arrive(&sm.dfree[s]);  // the slot starts free (its phase 0 is complete)
+        }
+        sm.sel_exit = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
@@ -1326,7 +1366,15 @@ __global__ void __launch_bounds__(kThreads, StageCfg<ELT>::kMinBlocks) lp_stream
         if (tid == kConsumerThreads) producer_loop<ELT>(p, sm, stages, t0);
         return;
     }
+    if (warp == kWarps + 1) {
+        helper_loop(p, sm, t0 + p.timeout_ns);
+        return;
+    }
     compute_loop<ELT>(p, sm, stages, t0);
+    if ((tid & 31) == 0) {
+        __threadfence_block();  // this warp's slot arrivals come first
+        atomicAdd(&sm.sel_exit, 1);
+    }
 }
 
 // ------------------------------------------------------------------ records
