@@ -1272,44 +1272,32 @@ __device__ __noinline__ bool decide_row(const Params& p, int2* cur) {
 __device__ __noinline__ void helper_loop(const Params& p, Shared& sm, unsigned long long deadline) {
     const int lane = threadIdx.x & 31;
     int ds = 0, ns = 0;
+    int selections = 0;  // natural tiles counted whose keys are not written yet
     uint32_t dphase = 0, nphase = 0;
-    for (;;) {
-        const uint32_t par = (dphase >> ds) & 1u;
-        bool ready = false;
-        for (uint32_t i = 0;; ++i) {
-            if (mbar_test_wait(&sm.dfull[ds], par)) {  // polled: this warp has nothing else to do
-                ready = true;
-                break;
+    for (uint32_t i = 0;; ++i) {
+        // counts (and decisions) first: they are on the verify chains' path
+        // polled (this warp has nothing else to wait on); lane 0's view decides for the warp
+        if (__shfl_sync(kFull, (int)mbar_test_wait(&sm.dfull[ds], (dphase >> ds) & 1u), 0)) {
+            const int4 d = sm.dslot[ds];
+            __syncwarp();
+            int old = 0;
+            if (lane == 0) {
+                mbar_arrive(&sm.dfree[ds]);  // the slot's contents are read
+                old = atomicAdd(&p.done[d.x], 1);
             }
-            if (vload(&sm.sel_exit) == kWarps) {
-                __threadfence_block();  // every arrival precedes the last exit count
-                ready = mbar_test_wait(&sm.dfull[ds], par);
-                break;
+            dphase ^= 1u << ds;
+            if (++ds == kDoneRing) ds = 0;
+            selections += d.z;
+            if (lane == 0 && old == p.done_last) {
+                int2 cur = make_int2(d.x, d.y);
+                while (decide_row(p, &cur)) {
+                }
             }
-            if ((i & 63u) == 63u && globaltimer() > deadline) break;
+            __syncwarp();
+            continue;
         }
-        if (!__all_sync(kFull, ready)) {
-            if (lane == 0 && vload(&sm.sel_exit) != kWarps) atomicOr(p.status, kStatusTimeout);
-            return;
-        }
-        const int4 d = sm.dslot[ds];
-        __syncwarp();
-        int old = 0;
-        if (lane == 0) {
-            mbar_arrive(&sm.dfree[ds]);  // the slot's contents are read
-            old = atomicAdd(&p.done[d.x], 1);
-        }
-        dphase ^= 1u << ds;
-        if (++ds == kDoneRing) ds = 0;
-        // the decision first: the tile's keys are read only by the record kernel
-        if (lane == 0 && old == p.done_last) {
-            int2 cur = make_int2(d.x, d.y);
-            while (decide_row(p, &cur)) {
-            }
-        }
-        __syncwarp();
-        if (d.z) {
-            // a natural tile: its candidates were in before its done slot
+        if (selections > 0) {
+            // the oldest natural tile counted: its candidates were in before its done slot
             const uint32_t cpar = (nphase >> ns) & 1u;
             if (__any_sync(kFull, !mbar_wait(&sm.ccand[ns], cpar, deadline))) {
                 if (lane == 0) atomicOr(p.status, kStatusTimeout);
@@ -1322,6 +1310,17 @@ __device__ __noinline__ void helper_loop(const Params& p, Shared& sm, unsigned l
             if (lane == 0) mbar_arrive(&sm.cfree[ns]);
             nphase ^= 1u << ns;
             if (++ns == kRing) ns = 0;
+            --selections;
+            continue;
+        }
+        if (vload(&sm.sel_exit) == kWarps) {
+            __threadfence_block();  // every arrival precedes the last exit count
+            if (!__any_sync(kFull, mbar_test_wait(&sm.dfull[ds], (dphase >> ds) & 1u))) return;
+            continue;
+        }
+        if ((i & 63u) == 63u && globaltimer() > deadline) {
+            if (lane == 0) atomicOr(p.status, kStatusTimeout);
+            return;
         }
     }
 }
