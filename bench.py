@@ -255,7 +255,7 @@ class Flusher:
     def __init__(self, dev):
         import torch
         self.buf = torch.empty(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
-        self.clean = torch.ones(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+        self.clean = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)  # summed without a cast
 
     def __call__(self, i):
         import torch

@@ -1,32 +1,38 @@
 // lp_kernels.cu -- sm_103a kernels of the logprob / greedy-acceptance epilogue.
 //
-// Two launches per run, both on the caller's stream:
+// Three launches per run, all on the caller's stream:
 //
-//  lp_prepare_kernel (1 CTA)
+//  lp_prepare_kernel (1 CTA of 1024 threads)
 //    validates group_indptr, resolves each group's request (natural
 //    alternatives, explicit ids or argmax only), finishes groups that need no
 //    logits, resets the per-row counters and writes the depth-0 work queue:
 //    row 0 of every group that must be read.
 //
-//  lp_stream_kernel (persistent, PDL-overlapped with the prepare kernel),
-//  warp-specialised CTAs of 10 warps:
-//    - producer warp: draws work items (queue position, tile) from one global
-//      counter and streams each 8192-element vocabulary tile into a
-//      shared-memory stage with a TMA bulk copy (cp.async.bulk, mbarrier
-//      completion, L2 evict-first);
-//    - 8 compute warps: reduce a tile to its FP32 max, exp-sum (ex2) relative
-//      to that max, argmax key and, for rows that report natural alternatives,
-//      the tile's best 32 packed sort keys
-//          key = ord32(x) << 32 | (0xFFFFFFFF - id),
-//      ord32 being the monotone float -> uint map with -0 folded into +0;
-//      results go to a shared-memory ring;
-//    - merge warp: publishes tile results to global memory, counts the row's
-//      finished tiles and, on the last one, merges the row: argmax -> greedy
-//      acceptance (on acceptance the next row of the group is appended to the
-//      queue, so rows past the accepted prefix are never read), then
-//      lse = M + log(sum s_t exp(m_t - M)), the chosen token's logprob, the
-//      top-K natural alternatives or the explicit-id gather, and the 258-word
-//      record.
+//  lp_stream_kernel (persistent, 3 CTAs per SM, launched with programmatic
+//  dependent launch so its set-up overlaps the prepare kernel), CTAs of 10
+//  specialised warps:
+//    - producer warp (one lane): takes work items (queue position, tile) --
+//      the depth-0 rows' tiles first, then rows appended after an acceptance
+//      -- and streams each 32 KiB vocabulary tile (16384 BF16 or 8192 FP32
+//      elements) into one of two shared-memory stages with a TMA bulk copy
+//      (cp.async.bulk, mbarrier completion, L2 evict-first);
+//    - 8 compute warps: each reduces its share of a tile to its FP32 max,
+//      the argmax key (atomicMax into the row's best key), the exp-sum (ex2)
+//      relative to its max and, for rows that report natural alternatives,
+//      its elements >= a tile threshold exchanged between the 8 warps (packed
+//      sort keys  key = ord32(x) << 32 | (0xFFFFFFFF - id), ord32 being the
+//      monotone float -> uint map with -0 folded into +0); the partials go to
+//      global memory and the tile to the helper warp through a done slot;
+//    - helper warp: counts every tile for its row, decides a row when its
+//      count completes it (argmax -> greedy acceptance; on acceptance the
+//      next row of the group is appended to the queue, so by default rows
+//      past the accepted prefix are never read), and writes a natural tile's
+//      best 32 keys from the 8 warps' candidates.
+//
+//  lp_record_kernel (one CTA per row, dependent launch): for every decided
+//    row of a requesting group, lse = M + log(sum s_t exp(m_t - M)) from the
+//    tile partials, the chosen token's logprob, the top-K natural
+//    alternatives or the explicit-id gather, and the 258-word record.
 //
 // Sources: "logprobs-design.md" (generation-logprob contract; the four-launch
 // reduction paragraph: FP32 tile maxima and exponential sums, a per-position
