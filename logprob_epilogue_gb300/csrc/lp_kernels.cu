@@ -246,10 +246,11 @@ __device__ __forceinline__ T warp_sort_desc(T v, int lane) {
 }
 
 // Sorts a bitonic sequence (one value per lane) in descending order.
-__device__ __forceinline__ unsigned long long warp_bitonic_clean_desc(unsigned long long v, int lane) {
+template <typename T>
+__device__ __forceinline__ T warp_bitonic_clean_desc(T v, int lane) {
 #pragma unroll
     for (int j = 16; j > 0; j >>= 1) {
-        const unsigned long long p = __shfl_xor_sync(kFull, v, j);
+        const T p = __shfl_xor_sync(kFull, v, j);
         const bool lower = (lane & j) == 0;
         v = lower ? (p > v ? p : v) : (p < v ? p : v);
     }
@@ -1012,15 +1013,46 @@ __device__ __forceinline__ int capture_candidates(const unsigned char* sp, int t
 }
 
 
-__device__ __forceinline__ unsigned long long merge_lists(unsigned long long a, unsigned long long b, int lane) {
-    const unsigned long long rev = __shfl_sync(kFull, b, 31 - lane);
+// The best 32 of two descending lists (one key per lane), descending.
+template <typename T>
+__device__ __forceinline__ T merge_lists(T a, T b, int lane) {
+    const T rev = __shfl_sync(kFull, b, 31 - lane);
     return warp_bitonic_clean_desc(rev > a ? rev : a, lane);
 }
 
 // Best 32 keys (descending, lane i holds the i-th) of a tile's candidate
 // regions: the keys are taken 64 at a time in region order, each half sorted
-// (bitonic), the halves and the running result merged.
-__device__ __forceinline__ unsigned long long slot_top32(const CandSlot& R, int lane) {
+// (bitonic), the halves and the running result merged.  For a BF16 tile the
+// sort runs on 32-bit keys, exact for its values and ids: the value's ord32
+// carries no bits in its low half (all zeros or all ones), and a tile id fits
+// in 16 bits, so  key32 = ord32 >> 16 << 16 | (0xFFFF - (id - tbase))  orders
+// like the 64-bit key, at half the shuffles.
+template <typename K>
+__device__ __forceinline__ K slot_key(unsigned long long k, uint32_t tbase) {
+    if constexpr (sizeof(K) == 8) {
+        return k;
+    } else {
+        if (k == 0ull) return 0u;
+        const uint32_t o = static_cast<uint32_t>(k >> 32), id = ~static_cast<uint32_t>(k);
+        return (o & 0xFFFF0000u) | (0xFFFFu - (id - tbase));
+    }
+}
+
+template <typename K>
+__device__ __forceinline__ unsigned long long slot_unkey(K k, uint32_t tbase) {
+    if constexpr (sizeof(K) == 8) {
+        return k;
+    } else {
+        if (k == 0u) return 0ull;
+        const uint32_t hi = k & 0xFFFF0000u;
+        const uint32_t o = hi | ((hi & 0x80000000u) ? 0u : 0xFFFFu);  // the value's ord32 low half
+        const uint32_t id = tbase + (0xFFFFu - (k & 0xFFFFu));
+        return (static_cast<unsigned long long>(o) << 32) | static_cast<unsigned long long>(~id);
+    }
+}
+
+template <typename K>
+__device__ __forceinline__ unsigned long long slot_top32(const CandSlot& R, int lane, uint32_t tbase) {
     int cw[kWarps];
     int n = 0;
 #pragma unroll
@@ -1028,7 +1060,7 @@ __device__ __forceinline__ unsigned long long slot_top32(const CandSlot& R, int 
         cw[w] = R.wcnt[w];
         n += cw[w];
     }
-    unsigned long long r = 0ull;
+    K r = 0;
     for (int q0 = 0; q0 < n; q0 += 64) {
         unsigned long long a = 0ull, b = 0ull;
         int before = 0;
@@ -1039,12 +1071,12 @@ __device__ __forceinline__ unsigned long long slot_top32(const CandSlot& R, int 
             if (ib >= 0 && ib < cw[w]) b = R.cand[w][ib];
             before += cw[w];
         }
-        a = warp_sort_desc(a, lane);
-        b = warp_sort_desc(b, lane);
-        const unsigned long long c = merge_lists(a, b, lane);
+        const K sa = warp_sort_desc(slot_key<K>(a, tbase), lane);
+        const K sb = warp_sort_desc(slot_key<K>(b, tbase), lane);
+        const K c = merge_lists(sa, sb, lane);
         r = q0 == 0 ? c : merge_lists(r, c, lane);
     }
-    return r;
+    return slot_unkey<K>(r, tbase);
 }
 
 __device__ __noinline__ bool decide_row(const Params& p, int2* cur);
@@ -1275,6 +1307,7 @@ __device__ __noinline__ bool decide_row(const Params& p, int2* cur) {
 // release count gives the same order through the memory model, but its fence
 // waits for the multiprocessor's outstanding memory traffic, which made the
 // helper's per-tile counts the bottleneck.)
+template <int ELT>
 __device__ __noinline__ void helper_loop(const Params& p, Shared& sm, unsigned long long deadline) {
     const int lane = threadIdx.x & 31;
     int ds = 0, ns = 0;
@@ -1310,7 +1343,9 @@ __device__ __noinline__ void helper_loop(const Params& p, Shared& sm, unsigned l
                 return;
             }
             const CandSlot& C = sm.cs[ns];
-            const unsigned long long key = slot_top32(C, lane);
+            const uint32_t tbase = static_cast<uint32_t>((C.tslot % p.T) * tile_elems<ELT>());
+            const unsigned long long key =
+                ELT == 2 ? slot_top32<uint32_t>(C, lane, tbase) : slot_top32<unsigned long long>(C, lane, tbase);
             p.part_keys[C.tslot * kKeysPerTile + lane] = key;
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.cfree[ns]);
@@ -1372,7 +1407,7 @@ __global__ void __launch_bounds__(kThreads, StageCfg<ELT>::kMinBlocks) lp_stream
         return;
     }
     if (warp == kWarps + 1) {
-        helper_loop(p, sm, t0 + p.timeout_ns);
+        helper_loop<ELT>(p, sm, t0 + p.timeout_ns);
         return;
     }
     compute_loop<ELT>(p, sm, stages, t0);
