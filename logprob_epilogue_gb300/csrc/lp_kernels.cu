@@ -359,31 +359,45 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 // Vector c of the calling thread (16 bytes, elements (c*256 + tid)*EPV + e).
 // In the last, partial tile of a row (FULL = false) elements at or past nv
 // read as -inf, and vectors wholly past nv are not read at all.
+// Vector c of the calling thread (16 bytes) from the stage.  A partial tile
+// (FULL = false) has had every lane past nv set to -inf in the stage first
+// (fill_partial), so both read the same way.
 template <int ELT, bool FULL>
 __device__ __forceinline__ uint4 ld_vec(const unsigned char* sp, int c, int tid, int nv) {
-    const int v = c * kConsumerThreads + tid;
-    if constexpr (FULL) {
-        return lds128(sp + (size_t)v * 16);
-    } else {
-        constexpr int EPV = 16 / ELT;
-        constexpr uint32_t kNegInfW = ELT == 2 ? 0xFF80FF80u : 0xFF800000u;
-        const int valid = nv - v * EPV;
-        if (valid <= 0) return make_uint4(kNegInfW, kNegInfW, kNegInfW, kNegInfW);
-        uint4 x = lds128(sp + (size_t)v * 16);
-        if (valid < EPV) {
-            uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    return lds128(sp + (size_t)(c * kConsumerThreads + tid) * 16);
+}
+
+// Sets the lanes past nv of the calling thread's vectors to -inf, in the stage:
+// the last tile of a row is then read like a full one.  A thread touches only
+// its own vectors, the ones it reads later, so no barrier is needed; the proxy
+// fence before the stage is released (tile_work) orders these writes before
+// the next bulk copy into the stage.
+template <int ELT>
+__device__ __forceinline__ void fill_partial(unsigned char* sp, int tid, int nv) {
+    constexpr int EPV = 16 / ELT;
+    constexpr uint32_t kNegInfW = ELT == 2 ? 0xFF80FF80u : 0xFF800000u;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                if constexpr (ELT == 2) {
-                    if (2 * i >= valid) w[i] = kNegInfW;
-                    else if (2 * i + 1 >= valid) w[i] = (w[i] & 0xFFFFu) | 0xFF800000u;
-                } else {
-                    if (i >= valid) w[i] = kNegInfW;
-                }
-            }
-            x = make_uint4(w[0], w[1], w[2], w[3]);
+    for (int c = 0; c < TileLayout<ELT>::NCH; ++c) {
+        const int v = c * kConsumerThreads + tid;
+        const int valid = nv - v * EPV;
+        if (valid >= EPV) continue;
+        uint4* dst = reinterpret_cast<uint4*>(sp + (size_t)v * 16);
+        if (valid <= 0) {
+            *dst = make_uint4(kNegInfW, kNegInfW, kNegInfW, kNegInfW);
+            continue;
         }
-        return x;
+        const uint4 x = lds128(dst);
+        uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if constexpr (ELT == 2) {
+                if (2 * i >= valid) w[i] = kNegInfW;
+                else if (2 * i + 1 >= valid) w[i] = (w[i] & 0xFFFFu) | 0xFF800000u;
+            } else {
+                if (i >= valid) w[i] = kNegInfW;
+            }
+        }
+        *dst = make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
 
@@ -1158,6 +1172,7 @@ __device__ __forceinline__ bool tile_work(const Params& p, Shared& sm, const uns
     // partial results of the warp, then the tile goes to the helper warp
     // through a done slot: once the 8 warps arrived, it counts the tile for
     // the row
+    if (!FULL) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the -inf fill, before the next copy
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.empty[stage]);  // no more reads of this stage by this warp
     const float Mw = unord32(omx);
@@ -1220,6 +1235,7 @@ __device__ void compute_loop(const Params& p, Shared& sm, unsigned char* stages,
         if (__builtin_expect(nv == kTE, 1)) {
             ok = tile_work<ELT, true>(p, sm, sp, nv, tbase, info, stage, ns, nphase, ds, dphase, deadline);
         } else {
+            fill_partial<ELT>(stages + (size_t)stage * kTileBytes, tid, nv);
             ok = tile_work<ELT, false>(p, sm, sp, nv, tbase, info, stage, ns, nphase, ds, dphase, deadline);
         }
         if (!ok) return;
