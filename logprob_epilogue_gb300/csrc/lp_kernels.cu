@@ -1036,11 +1036,12 @@ __device__ __forceinline__ T merge_lists(T a, T b, int lane) {
 
 // Best 32 keys (descending, lane i holds the i-th) of a tile's candidate
 // regions: the keys are taken 64 at a time in region order, each half sorted
-// (bitonic), the halves and the running result merged.  For a BF16 tile the
-// sort runs on 32-bit keys, exact for its values and ids: the value's ord32
-// carries no bits in its low half (all zeros or all ones), and a tile id fits
-// in 16 bits, so  key32 = ord32 >> 16 << 16 | (0xFFFF - (id - tbase))  orders
-// like the 64-bit key, at half the shuffles.
+// (bitonic), the halves and the running result merged.  When every value is
+// BF16-representable (a BF16 tile, or an FP32 tile of such values) the sort runs
+// on 32-bit keys, exact for those values and ids: the value's ord32 carries no
+// bits in its low half (all zeros or all ones), and a tile id fits in 16 bits,
+// so  key32 = ord32 >> 16 << 16 | (0xFFFF - (id - tbase))  orders like the
+// 64-bit key, at half the shuffles.
 template <typename K>
 __device__ __forceinline__ K slot_key(unsigned long long k, uint32_t tbase) {
     if constexpr (sizeof(K) == 8) {
@@ -1091,6 +1092,22 @@ __device__ __forceinline__ unsigned long long slot_top32(const CandSlot& R, int 
         r = q0 == 0 ? c : merge_lists(r, c, lane);
     }
     return slot_unkey<K>(r, tbase);
+}
+
+// True when every candidate of the slot holds a BF16-representable value (the
+// low half of its ord32 all zeros or all ones): an FP32 tile of such values
+// (logits computed in BF16, then widened) can then use the 32-bit keys.
+__device__ __forceinline__ bool slot_bf16_values(const CandSlot& R, int lane) {
+    bool ok = true;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        const int cw = R.wcnt[w];
+        if (lane < cw) {
+            const uint32_t lo = static_cast<uint32_t>(R.cand[w][lane] >> 32) & 0xFFFFu;
+            ok = ok && (lo == 0u || lo == 0xFFFFu);
+        }
+    }
+    return __all_sync(kFull, ok);
 }
 
 __device__ __noinline__ bool decide_row(const Params& p, int2* cur);
@@ -1360,8 +1377,9 @@ __device__ __noinline__ void helper_loop(const Params& p, Shared& sm, unsigned l
             }
             const CandSlot& C = sm.cs[ns];
             const uint32_t tbase = static_cast<uint32_t>((C.tslot % p.T) * tile_elems<ELT>());
+            const bool k32 = ELT == 2 || slot_bf16_values(C, lane);
             const unsigned long long key =
-                ELT == 2 ? slot_top32<uint32_t>(C, lane, tbase) : slot_top32<unsigned long long>(C, lane, tbase);
+                k32 ? slot_top32<uint32_t>(C, lane, tbase) : slot_top32<unsigned long long>(C, lane, tbase);
             p.part_keys[C.tslot * kKeysPerTile + lane] = key;
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.cfree[ns]);
