@@ -3,7 +3,7 @@
 python bench.py [--gpus N] [--steps K] [--warmup W] [--config large|spec|decode|wide|tiny]
                 [--impl reference] [--no-cpu-baseline] [--no-per-workload]
 
-One step = one lp_run (prepare + persistent stream kernel) over the whole
+One step = one lp_run (prepare, persistent stream and record kernels) over the whole
 logit block of the chosen workload, inputs resident in HBM.  L2 is flushed
 (a 256 MiB device write) before every timed step, outside the timed events.
 Rank 0 prints one JSON line.  ``--impl reference`` times the CPU oracle (the
@@ -414,7 +414,7 @@ def main():
         "rows_read_per_s": world * ab["rows_read"] / per_step,
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peak, "unit": "GB/s",
                      "frac": achieved_gbs / peak, "traffic": measured_traffic(args.config),
-                     "kernel": "lp_stream_kernel (timed with lp_prepare_kernel: one lp_run)",
+                     "kernel": "lp_stream_kernel (timed with lp_prepare_kernel and lp_record_kernel: one lp_run)",
                      "algorithmic_bytes_per_launch": ab["total"], "peak_source": peak_kind},
         "e2e": e2e,
         "gpu_launches": 2 * args.steps,
