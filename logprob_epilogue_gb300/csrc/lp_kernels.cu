@@ -219,15 +219,6 @@ __device__ __forceinline__ int warp_sum_i(int v) {
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
     return v;
 }
-__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const unsigned long long w = __shfl_xor_sync(kFull, v, o);
-        v = w > v ? w : v;
-    }
-    return v;
-}
-
 // Sorts one value per lane in descending order across the warp (bitonic).
 template <typename T>
 __device__ __forceinline__ T warp_sort_desc(T v, int lane) {
@@ -1113,10 +1104,11 @@ __device__ __forceinline__ bool slot_bf16_values(const CandSlot& R, int lane) {
 __device__ __noinline__ bool decide_row(const Params& p, int2* cur);
 
 // The compute warp's share of one tile: passes, candidates (natural tiles,
-// through a candidate slot), then its partial results published to global
-// memory: (max, exp-sum), the argmax key (atomicMax on the row's best key) and
-// one acquire-release increment of the row's done count, read back later.
-// FULL = false for the last, partial tile of a row.  False after a timeout.
+// through a candidate slot), its partial results published to global memory
+// ((max, exp-sum) and the argmax key, atomicMax on the row's best key), then
+// the tile handed to the helper warp through a done slot.  FULL = false for
+// the last, partial tile of a row (its lanes past V already -inf in the
+// stage).  False after a timeout.
 template <int ELT, bool FULL>
 __device__ __forceinline__ bool tile_work(const Params& p, Shared& sm, const unsigned char* sp, int nv, int tbase,
                                           const int4& info, int stage, int& ns, uint32_t& nphase,

@@ -126,6 +126,24 @@ def test_tie_straddles_cutoff():
     _check(_one_group(x[None, :], V))
 
 
+@pytest.mark.parametrize("off_grid", [False, True], ids=["bf16_grid", "one_off_grid"])
+def test_fp32_ties_on_the_bf16_grid(off_grid):
+    # FP32 logits that are all BF16-representable (as when computed in BF16)
+    # select each tile's best 32 on 32-bit keys; one value off the grid sends
+    # its tile back to 64-bit keys.  Heavy ties at the top, across 4 tiles.
+    rng = np.random.default_rng(7)
+    V = 30_000
+    x = np.round(rng.normal(0, 1, V) * 2.0) / 2.0  # steps of 0.5: exact in BF16
+    top = rng.choice(V, 80, replace=False)
+    x[top] = 6.0
+    x[top[:5]] = 6.5
+    if off_grid:
+        x[top[5]] = 6.0 + 2.0 ** -10  # between BF16 neighbours
+    x = x.astype(np.float32)
+    w = _one_group(np.stack([x, x[::-1].copy()]), V, drafts=[int(np.argmax(x)), -1])
+    _check(w)
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_constant_row(dtype):
     V = 30_000
