@@ -31,6 +31,8 @@ STATUS_BAD_ID = 0x1
 STATUS_BAD_TOKEN = 0x2
 STATUS_BAD_COUNT = 0x4
 STATUS_BAD_GROUP = 0x8
+SCORE_WORDS = 43
+SCORE_ALTS = 20
 
 _default = None
 
@@ -102,6 +104,11 @@ class Oracle:
                                ctypes.c_void_p, ctypes.c_void_p]
         L.orc_epilogue.restype = ctypes.c_int
         L.orc_epilogue.argtypes = [ctypes.POINTER(_IO), ctypes.c_int]
+        L.orc_rank.restype = ctypes.c_int32
+        L.orc_rank.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_float]
+        L.orc_score.restype = ctypes.c_int
+        L.orc_score.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
+                                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
         self.L = L
         self.path = path
 
@@ -132,6 +139,28 @@ class Oracle:
     def epilogue(self, *args, **kw):
         return _epilogue(self.L, *args, **kw)
 
+    def rank(self, x, lse_value, lp) -> int:
+        """1 + the number of lanes whose reported logprob is strictly greater than lp."""
+        a = _f32(x)
+        return int(self.L.orc_rank(_ptr(a), a.size, float(np.float32(lse_value)), float(np.float32(lp))))
+
+    def score(self, logits: np.ndarray, V: int, targets, *, records=None, threads: int = 1):
+        """Prompt scoring of float32 rows [rows, Vp]: dict of records [rows, 43], lse (NaN for
+        invalid rows) and status."""
+        logits = np.ascontiguousarray(logits, dtype=np.float32)
+        rows, Vp = logits.shape
+        tg = np.ascontiguousarray(targets, np.int32)
+        if records is None:
+            records = np.zeros((rows, SCORE_WORDS), np.int32)
+        records = np.ascontiguousarray(records, np.int32)
+        lse_out = np.full(max(rows, 1), np.nan, np.float32)
+        status = np.zeros(1, np.uint32)
+        rc = self.L.orc_score(_ptr(logits), rows, int(V), Vp, _ptr(tg), _ptr(records), _ptr(lse_out), _ptr(status),
+                              int(threads))
+        if rc != 0:
+            raise RuntimeError(f"orc_score failed: {rc}")
+        return {"records": records, "lse": lse_out[:rows], "status": int(status[0])}
+
 
 def load(path: str | None = None) -> Oracle:
     """The default oracle (built on first use), or the library at ``path``."""
@@ -161,6 +190,14 @@ def topk(x, K, lse_value=None):
 
 def epilogue(*args, **kw):
     return load().epilogue(*args, **kw)
+
+
+def rank(x, lse_value, lp):
+    return load().rank(x, lse_value, lp)
+
+
+def score(*args, **kw):
+    return load().score(*args, **kw)
 
 
 def _epilogue(L, logits: np.ndarray, V: int, group_indptr, draft_tokens, sampled_tokens, requested,

@@ -237,3 +237,74 @@ extern "C" int orc_epilogue(const orc_io* io, int threads) {
     if (io->rows_read) *io->rows_read = sh.rows_read.load();
     return 0;
 }
+
+// ---- prompt scoring ("logprobs-design.md", the prompt-logprobs paragraphs:
+// each scored row holds the actual token id, its raw FP32 logprob bits, its
+// rank, then twenty (id, logprob bits) alternatives in the generation order;
+// an invalid target row holds id -1, NaN, rank zero and alternative ids -1).
+
+extern "C" int32_t orc_rank(const float* x, int64_t V, float lse, float lp) {
+    // The definition: one plus the number of lanes whose reported value
+    // fl32(x_v - lse) is strictly greater than the target's.
+    int32_t greater = 0;
+    for (int64_t v = 0; v < V; ++v)
+        if (orc_logprob(x[v], lse) > lp) ++greater;
+    return 1 + greater;
+}
+
+namespace {
+
+void score_row(const float* x, int64_t V, int32_t t, int32_t* rec, float* lse_out, uint32_t* st) {
+    if (t < 0 || t >= V) {
+        if (t >= V) *st |= ORC_STATUS_BAD_TOKEN;
+        rec[0] = -1;
+        rec[1] = (int32_t)ORC_NAN_BITS;
+        rec[2] = 0;
+        for (int32_t i = 0; i < ORC_SCORE_ALTS; ++i) {
+            rec[3 + 2 * i] = -1;
+            rec[4 + 2 * i] = (int32_t)ORC_NAN_BITS;
+        }
+        return;
+    }
+    const float lse = orc_lse(x, V);
+    if (lse_out) *lse_out = lse;
+    const float lp = orc_logprob(x[t], lse);
+    rec[0] = t;
+    rec[1] = (int32_t)float_bits(lp);
+    rec[2] = orc_rank(x, V, lse, lp);
+    int32_t ids[ORC_SCORE_ALTS];
+    float lps[ORC_SCORE_ALTS];
+    const int32_t n = orc_topk(x, V, lse, ORC_SCORE_ALTS, ids, lps);
+    for (int32_t i = 0; i < ORC_SCORE_ALTS; ++i) {
+        rec[3 + 2 * i] = i < n ? ids[i] : -1;
+        rec[4 + 2 * i] = i < n ? (int32_t)float_bits(lps[i]) : (int32_t)ORC_NAN_BITS;
+    }
+}
+
+}  // namespace
+
+extern "C" int orc_score(const float* logits, int64_t rows, int64_t V, int64_t Vp, const int32_t* targets,
+                         int32_t* records, float* lse_out, uint32_t* status, int threads) {
+    if (!logits || !targets || !records || !status) return -1;
+    std::atomic<int64_t> next{0};
+    std::atomic<uint32_t> st_all{0};
+    auto worker = [&]() {
+        for (;;) {
+            const int64_t r = next.fetch_add(1);
+            if (r >= rows) break;
+            uint32_t st = 0;
+            score_row(logits + r * Vp, V, targets[r], records + r * ORC_SCORE_WORDS, lse_out ? lse_out + r : nullptr,
+                      &st);
+            st_all.fetch_or(st);
+        }
+    };
+    if (threads <= 1) {
+        worker();
+    } else {
+        std::vector<std::thread> pool;
+        for (int t = 0; t < threads; ++t) pool.emplace_back(worker);
+        for (auto& th : pool) th.join();
+    }
+    *status = st_all.load();
+    return 0;
+}

@@ -23,6 +23,12 @@
  *             +0 equal); the group emits rows 0..a.
  *   - record: int32[258] = chosen id, chosen lp bits, then (id, lp bits)
  *             pairs; unused pairs are (-1, 0x7FC00000).
+ *   - prompt scoring (logprobs-design.md, the prompt-logprobs paragraphs):
+ *             per target row, int32[43] = the actual token id, its lp bits,
+ *             its rank (1 + the number of lanes whose reported lp is strictly
+ *             greater), then the 20 natural alternatives as (id, lp bits)
+ *             pairs.  A row whose target is -1 (or any id outside [0, V))
+ *             writes id -1, NaN bits, rank 0 and alternative ids -1.
  *
  * Logits are passed as FP32 (BF16 inputs are widened exactly by the caller).
  * Inputs must be finite; the oracle is not defined for NaN or infinities.
@@ -90,6 +96,19 @@ typedef struct {
 /* Runs the epilogue; groups are split over `threads` host threads (<=1: one).
  * Returns 0, or -1 on a NULL required pointer. */
 int orc_epilogue(const orc_io* io, int threads);
+
+/* Prompt scoring record geometry: id, lp bits, rank, 20 (id, lp bits) pairs. */
+#define ORC_SCORE_WORDS 43
+#define ORC_SCORE_ALTS 20
+
+/* 1 + number of lanes v in [0, V) with fl32(x_v - lse) > lp. */
+int32_t orc_rank(const float* x, int64_t V, float lse, float lp);
+
+/* Prompt scoring of rows [0, rows): records [rows, 43]; lse_out [rows] or NULL
+ * (written for valid rows); status gets ORC_STATUS_BAD_TOKEN for a target >= V.
+ * Returns 0, or -1 on a NULL required pointer. */
+int orc_score(const float* logits, int64_t rows, int64_t V, int64_t Vp, const int32_t* targets,
+              int32_t* records, float* lse_out, uint32_t* status, int threads);
 
 #ifdef __cplusplus
 }

@@ -276,6 +276,84 @@ def pin_status_bits(orc):
     assert (r2["emitted_tokens"] == -7).all()
 
 
+# ----------------------------------------------------------------------------- prompt scoring
+#
+# "logprobs-design.md", the prompt-logprobs paragraphs: a scored row holds the
+# actual token id, its FP32 logprob bits, its rank (one plus the count of
+# strictly greater reported values), then twenty alternatives in the generation
+# order; an invalid target row holds id -1, NaN, rank zero and alternative ids -1.
+
+SCORE_WORDS = 43
+
+
+def u32(v) -> int:
+    return int(v) & 0xFFFFFFFF
+
+
+def _score_rows(rng):
+    yield rng.normal(0, 2, 500).astype(np.float32)
+    yield (np.round(rng.normal(0, 2, 500) * 4) / 4).astype(np.float32)  # heavy ties
+    x = rng.uniform(0.0, 0.01, 400).astype(np.float32)
+    x[17] = 1e4  # subtraction collapses the others into a few values
+    yield x
+
+
+def pin_score_rank_independent(orc):
+    # rank by binary search in the sorted reported values (numpy FP32), against
+    # the oracle's direct count; the record's lp and alternatives follow the
+    # generation definitions already pinned above
+    rng = np.random.default_rng(21)
+    for x in _score_rows(rng):
+        V = x.shape[0]
+        targets = rng.integers(0, V, 12).astype(np.int32)
+        targets[0] = int(np.argmax(x))
+        r = orc.score(np.repeat(x[None, :], len(targets), 0), V, targets)
+        lse = orc.lse(x)
+        lps = (x - np.float32(lse)).astype(np.float32)
+        desc = -np.sort(lps)[::-1]  # ascending copy of -lp for searchsorted
+        ids, alt = orc.topk(x, 20, lse)
+        for i, t in enumerate(targets):
+            rec = r["records"][i]
+            lpt = np.float32(x[t] - np.float32(lse))
+            rank = int(np.searchsorted(desc, -lpt, side="left")) + 1
+            assert rec[0] == t and rec[2] == rank, (int(t), int(rec[2]), rank)
+            assert u32(rec[1]) == bits(np.float32(0.0) if lpt == 0 else lpt)
+            assert list(rec[3::2][:len(ids)]) == list(ids)
+            assert [u32(b) for b in rec[4::2][:len(ids)]] == [bits(v) for v in alt]
+        assert r["records"][0][2] == 1  # the argmax has nothing strictly above it
+
+
+def pin_score_collapse_closed_form(orc):
+    # one logit of 3e7, the others in [0, 0.5]: lse rounds to 3e7 and every other
+    # logprob rounds to -3e7 (half an ulp of 3e7 is 1), so each non-maximal
+    # target has rank 2 and the alternatives after the maximum follow ascending id
+    rng = np.random.default_rng(22)
+    V = 200
+    x = rng.uniform(0.0, 0.5, V).astype(np.float32)
+    x[5] = np.float32(3e7)
+    targets = np.array([5, 0, 199, 6], np.int32)
+    r = orc.score(np.repeat(x[None, :], 4, 0), V, targets)["records"]
+    assert r[0][2] == 1 and u32(r[0][1]) == bits(np.float32(0.0))
+    for rec in r[1:]:
+        assert rec[2] == 2 and u32(rec[1]) == bits(np.float32(-3e7))
+        assert list(rec[3::2][:5]) == [5, 0, 1, 2, 3]
+
+
+def pin_score_ties_and_invalid(orc):
+    x = np.array([1.0, 4.0, 2.0, 4.0, 4.0, -0.0, 0.0], np.float32)
+    V = 7
+    targets = np.array([3, 4, 5, 6, -1, 7], np.int32)
+    r = orc.score(np.repeat(x[None, :], 6, 0), V, targets)
+    rec = r["records"]
+    assert [int(v[2]) for v in rec[:4]] == [1, 1, 6, 6]  # equal values share a rank; -0 == +0
+    assert list(rec[0][3::2][:7]) == [1, 3, 4, 2, 0, 5, 6] and list(rec[0][3::2][7:]) == [-1] * 13
+    for bad in rec[4:]:
+        assert bad[0] == -1 and bad[1] == NAN_BITS and bad[2] == 0
+        assert all(int(v) == -1 for v in bad[3::2]) and all(int(v) == NAN_BITS for v in bad[4::2])
+    assert r["status"] == 0x2  # the target 7 >= V; -1 is the ordinary invalid marker
+
+
 ALL_PINS = [pin_golden_rows, pin_golden_groups, pin_brute_force, pin_lse_independent,
             pin_two_value_closed_form, pin_sum_exp_invariant, pin_pad_exclusion, pin_id_passthrough,
-            pin_acceptance_prefixes, pin_tiny_workload, pin_status_bits]
+            pin_acceptance_prefixes, pin_tiny_workload, pin_status_bits, pin_score_rank_independent,
+            pin_score_collapse_closed_form, pin_score_ties_and_invalid]

@@ -55,6 +55,12 @@ MUTANTS = {
                           "all[(size_t)v] = Pair{x[v], (int32_t)v};"),
     "unflagged_k0_read": ("const bool must_read = flagged || k >= 1 || sampled < 0;",
                           "const bool must_read = true;"),
+    "rank_counts_ties": ("if (orc_logprob(x[v], lse) > lp) ++greater;", "if (orc_logprob(x[v], lse) >= lp) ++greater;"),
+    "rank_before_rounding": ("if (orc_logprob(x[v], lse) > lp) ++greater;",
+                             "if ((double)x[v] - (double)lse > (double)lp) ++greater;"),
+    "rank_zero_based": ("    return 1 + greater;", "    return greater;"),
+    "invalid_rank_one": ("        rec[2] = 0;", "        rec[2] = 1;"),
+    "invalid_alt_id_zero": ("            rec[3 + 2 * i] = -1;", "            rec[3 + 2 * i] = 0;"),
 }
 
 
