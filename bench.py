@@ -299,6 +299,45 @@ def bench_device(w: W.Workload, steps: int, warmup: int, device: int, staging: b
     return plan, ins, outs, flush, starts, ends, stream
 
 
+def bench_score(device: int, peak: float, steps: int = 200, warmup: int = 5) -> dict:
+    """Times prompt scoring (lp_score) of the 512 x 151,936 BF16 prompt workload
+    on device-resident inputs; algorithmic bytes = the logits of the rows with a
+    valid target + the targets + the 43-word records."""
+    import torch
+    import logprob_epilogue_gb300 as lpe
+    w = W.prompt()
+    dev = torch.device("cuda", device)
+    tg_np = np.asarray(w.meta["targets"], np.int32)
+    plan = lpe.Plan(max_rows=w.rows, max_groups=w.rows, k_max=0, V=w.V, V_padded=w.Vp, dtype=w.dtype,
+                    k_alt_max=20, max_ids=128, device=device)
+    logits = torch.from_numpy(w.logits.view(np.int16)).view(torch.bfloat16).to(dev)
+    tg = torch.from_numpy(tg_np).to(dev)
+    rec = torch.zeros((w.rows, lpe.SCORE_WORDS), dtype=torch.int32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = Flusher(dev)
+    stream = torch.cuda.current_stream(dev)
+    for i in range(warmup):
+        flush(i)
+        plan.score(logits=logits, target_tokens=tg, records=rec, status=st, stream=stream)
+    torch.cuda.synchronize(dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush(i)
+        starts[i].record(stream)
+        plan.score(logits=logits, target_tokens=tg, records=rec, status=st, stream=stream)
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    if int(st.item()) != 0:
+        raise RuntimeError(f"prompt scoring status {int(st.item()):#x}")
+    m = statistics.mean(a.elapsed_time(b) * 1e-3 for a, b in zip(starts, ends))
+    valid = int(((tg_np >= 0) & (tg_np < w.V)).sum())
+    nbytes = valid * w.V * 2 + w.rows * 4 + w.rows * lpe.SCORE_WORDS * 4
+    plan.close()
+    return {"rows_per_s": w.rows / m, "us_per_step": m * 1e6, "hbm_gbs": nbytes / m / 1e9,
+            "frac": nbytes / m / 1e9 / peak, "rows_read": valid, "dtype": w.dtype}
+
+
 def run_e2e(args, w, plan, stream, dev, pg, local, world, accepted):
     """Same metric through lp_run_host: pinned host buffers, H2D and D2H inside the timed region."""
     import torch
@@ -450,6 +489,7 @@ def main():
                          "rows_read": abn["rows_read"], "dtype": wn.dtype}
             p2.close()
             del i2, o2, fl2
+        per["prompt_score"] = bench_score(local, peak)
         line["per_workload"] = per
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -188,6 +188,44 @@ int lp_run_host(lp_plan_t plan, const lp_io* host_io, void* stream);
 /* Bytes lp_run_host copies host->device and device->host for host_io. */
 int lp_run_host_bytes(lp_plan_t plan, const lp_io* host_io, int64_t* h2d, int64_t* d2h);
 
+/* ---- Prompt scoring ("logprobs-design.md", the prompt-logprobs paragraphs)
+ *
+ * Scores target tokens against rows of logits: row j carries the logits that
+ * predict target_tokens[j].  For a valid target t (0 <= t < V) the record holds
+ *   [0] t, [1] FP32 bits of lp(t) = fl32(x_t - lse) (-0 reported as +0),
+ *   [2] rank = 1 + the number of lanes v < V whose lp(v) is strictly greater,
+ *   [3+2i], [4+2i] = (id, lp bits) of the 20 natural alternatives in the
+ *       generation order (lp descending, id ascending), (-1, 0x7FC00000) past V;
+ * for any other target (-1 marks the prompt end or an image position) the row
+ * is not read and its record is id -1, 0x7FC00000, rank 0, every alternative
+ * (-1, 0x7FC00000); a target >= V also sets LP_STATUS_BAD_TOKEN.  (The page:
+ * each scored row holds the actual token id, its raw FP32 logprob bits, its
+ * rank, then twenty alternatives; an invalid target row holds id -1, NaN,
+ * rank zero and alternative ids -1.)
+ *
+ *   records      int32 [rows, 43]   (output; every row written)
+ *   lse_out      float [rows] or NULL (output: lse of the rows read)
+ *
+ * The rank counts strictly greater *reported* values, so lanes whose logit is
+ * above the target's but whose lp rounds to the same value do not count.
+ * Uses the plan's scratch: rows <= max_rows and rows <= max_groups (each row
+ * is scored on its own).  Device pointers; enqueues only, like lp_run.  The
+ * bound lp_io buffers are neither used nor changed.
+ * Errors: LP_EINVAL, LP_ESHAPE, LP_EALIGN, LP_ECUDA. */
+#define LP_SCORE_WORDS 43
+#define LP_SCORE_ALTS 20
+
+typedef struct {
+    const void* logits;            /* [rows, V_padded] of the plan's dtype, 16-byte aligned */
+    const int32_t* target_tokens;  /* [rows] */
+    int32_t* records;              /* [rows, 43] */
+    float* lse_out;                /* [rows] or NULL */
+    uint32_t* status;              /* [1] */
+    int32_t rows;
+} lp_score_io;
+
+int lp_score(lp_plan_t plan, const lp_score_io* io, void* stream);
+
 /* Debug: number of vocabulary tiles the last run read for each row (0 = the
  * row was never read), copied into host_tiles[0..rows).  With
  * LP_PLAN_READ_AHEAD the first row past a prefix may show read-ahead tiles.  Synchronises the
@@ -235,7 +273,7 @@ int lp_plan_tiles_per_row(lp_plan_t plan);
  *   stream  a cudaStream_t (NULL = legacy default stream).
  *
  * The scratch a run needs grows with io->rows * ceil(V / tile elements)
- * (about 320 bytes per row tile, plus 48 bytes per row and 16 per group);
+ * (about 384 bytes per row tile, plus 48 bytes per row and 16 per group);
  * a run that needs more than LP_STATIC_SCRATCH_BYTES is rejected with
  * LP_ESCRATCH before anything is enqueued.  4 MiB covers, for example, 512
  * rows of a 248,448-lane BF16 vocabulary.

@@ -17,6 +17,8 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "liblp_epilogue.so")
 
 RECORD_WORDS = 258
+SCORE_WORDS = 43  # prompt-scoring record: target id, lp bits, rank, 20 (id, lp bits) pairs
+SCORE_ALTS = 20
 MAX_IDS = 128
 UNUSED_LP_BITS = 0x7FC00000
 TILE_BYTES = 32768  # vocabulary tile: 16384 BF16 or 8192 FP32 logits
@@ -39,7 +41,7 @@ STATIC_SCRATCH_BYTES = 4 << 20  # fixed device scratch of run_static
 # Every symbol include/lp_epilogue.h declares.
 EXPORTS = ("lp_plan_create", "lp_plan_destroy", "lp_plan_scratch_bytes", "lp_bind", "lp_run", "lp_run_host",
            "lp_run_host_bytes", "lp_debug_tiles_read", "lp_debug_poison_scratch", "lp_debug_trace",
-           "lp_plan_tiles_per_row", "lp_run_static",
+           "lp_plan_tiles_per_row", "lp_run_static", "lp_score",
            "lp_strerror", "lp_last_cuda_error")
 
 
@@ -79,6 +81,17 @@ class IO(ctypes.Structure):
     ]
 
 
+class ScoreIO(ctypes.Structure):
+    _fields_ = [
+        ("logits", ctypes.c_void_p),
+        ("target_tokens", ctypes.c_void_p),
+        ("records", ctypes.c_void_p),
+        ("lse_out", ctypes.c_void_p),
+        ("status", ctypes.c_void_p),
+        ("rows", ctypes.c_int32),
+    ]
+
+
 _lib = None
 
 
@@ -112,6 +125,7 @@ def lib() -> ctypes.CDLL:
         L.lp_plan_tiles_per_row.argtypes = [P]
         L.lp_debug_trace.argtypes = [P, P, P, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]
         L.lp_run_static.argtypes = [ctypes.POINTER(PlanDesc), ctypes.POINTER(IO), P]
+        L.lp_score.argtypes = [P, ctypes.POINTER(ScoreIO), P]
         L.lp_strerror.argtypes = [ctypes.c_int]
         L.lp_strerror.restype = ctypes.c_char_p
         L.lp_last_cuda_error.argtypes = []
@@ -229,6 +243,41 @@ class Plan:
             stream = torch.cuda.current_stream(self.device)
         handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
         _check(lib().lp_run(self._h, ctypes.c_void_p(handle)), "lp_run")
+
+    def score(self, *, logits, target_tokens, records, status, lse_out=None, stream=None) -> None:
+        """Enqueues prompt scoring of ``target_tokens`` (int32 [rows]) against
+        ``logits`` [rows, V_padded]: ``records`` (int32 [rows, 43]) receives per row
+        the target id, the FP32 bits of its logprob, its rank and the 20 natural
+        alternatives; an invalid target (-1, or >= V) gives the invalid record.
+        The bound tensors are not used."""
+        import torch
+        want_logit = torch.bfloat16 if self.dtype == "bf16" else torch.float32
+        t = dict(logits=logits, target_tokens=target_tokens, records=records, status=status, lse_out=lse_out)
+        for name, x in t.items():
+            if x is None:
+                continue
+            if not isinstance(x, torch.Tensor) or not x.is_cuda or x.device.index != self.device:
+                raise ValueError(f"{name}: expected a CUDA tensor on device {self.device}")
+            if not x.is_contiguous():
+                raise ValueError(f"{name}: must be contiguous")
+        if logits.dtype != want_logit or logits.dim() != 2 or logits.shape[1] != self.desc.V_padded:
+            raise ValueError(f"logits: expected {want_logit} [rows, {self.desc.V_padded}]")
+        rows = int(logits.shape[0])
+        if target_tokens.dtype != torch.int32 or target_tokens.numel() < rows:
+            raise ValueError("target_tokens: expected int32 [rows]")
+        if records.dtype != torch.int32 or records.numel() < rows * SCORE_WORDS:
+            raise ValueError("records: expected int32 [rows, 43]")
+        if status.element_size() != 4 or status.numel() < 1:
+            raise ValueError("status: expected one 32-bit word")
+        if lse_out is not None and (lse_out.dtype != torch.float32 or lse_out.numel() < rows):
+            raise ValueError("lse_out: expected float32 [rows]")
+        io = ScoreIO(logits.data_ptr(), target_tokens.data_ptr(), records.data_ptr(),
+                     None if lse_out is None else lse_out.data_ptr(), status.data_ptr(), rows)
+        if stream is None:
+            stream = torch.cuda.current_stream(self.device)
+        handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+        self._keep_score = t
+        _check(lib().lp_score(self._h, ctypes.byref(io), ctypes.c_void_p(handle)), "lp_score")
 
     def host_io(self, arrays: dict) -> IO:
         rows = int(arrays["logits"].shape[0])

@@ -19,6 +19,8 @@ constexpr int kThreads = kConsumerThreads + 64;  // + 1 producer warp + 1 select
 constexpr int kRing = LP_RING;          // tile results in flight between compute and merge warps
 constexpr int kKeysPerTile = 32;        // retained sort keys per tile
 constexpr int kRecordWords = 258;
+constexpr int kScoreWords = 43;        // prompt-scoring record: id, lp bits, rank, 20 pairs
+constexpr int kScoreAlts = 20;
 constexpr int kMaxIds = 128;
 constexpr int kCandCap = 256;           // tile candidate buffer (keys)
 
@@ -117,10 +119,16 @@ struct Params {
     int4* rec_tasks;      // [max_rows] per row: (chosen token, queue entry, group descriptor word, count);
                           // descriptor word 0: no record to build
     float2* part_ms;      // [max_rows * T * 8] (max, exp-sum) of each compute warp's share of a tile
+    int2* part_rank;      // [max_rows * T * 8] prompt scoring: (lanes above the target's logit, the
+                          // smallest such logit's bits) of each compute warp's share of a tile
     unsigned long long* part_keys;  // [max_rows * T * 32] tile keys, descending
     unsigned long long timeout_ns;
     unsigned int debug_flags;
     int read_ahead;       // 0: rows past a group's emitted prefix are never read
+    // prompt scoring (targets != nullptr): group g is row g alone, k = 0, 20
+    // natural alternatives, chosen token targets[g]; records go to score_records
+    const int* targets;
+    int* score_records;   // [rows, 43]
     int done_last;        // done[row] before the increment that completes a row: T - 1, plus
                           // kParentDone with read-ahead
     // optional timeline (nullptr unless the plan traces)

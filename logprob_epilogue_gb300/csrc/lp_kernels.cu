@@ -204,6 +204,12 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gmem_src, 
 
 // ---- warp / block reductions (block = the 256 compute threads)
 
+__device__ __forceinline__ float warp_min_f(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fminf(v, __shfl_xor_sync(kFull, v, o));
+    return v;
+}
+
 __device__ __forceinline__ float warp_max_f(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
@@ -283,8 +289,11 @@ struct RecShared {
     unsigned long long lists[kWarps][32];   // per-warp partial top-32 lists
     float red_f[kWarps];
     float red_f2[kWarps];
+    int red_i[kWarps];
     float lse;
     float xchosen;
+    float xlim;                             // prompt scoring: largest logit whose lp is the target's
+    int corr;                               // prompt scoring: logits in (target's, xlim]
     int rec[kRecordWords + 2];              // record being assembled
 };
 
@@ -347,9 +356,6 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     return d;
 }
 
-// Vector c of the calling thread (16 bytes, elements (c*256 + tid)*EPV + e).
-// In the last, partial tile of a row (FULL = false) elements at or past nv
-// read as -inf, and vectors wholly past nv are not read at all.
 // Vector c of the calling thread (16 bytes) from the stage.  A partial tile
 // (FULL = false) has had every lane past nv set to -inf in the stage first
 // (fill_partial), so both read the same way.
@@ -508,6 +514,15 @@ struct GroupIn {
 
 __device__ __forceinline__ GroupIn load_group(const Params& p, int g) {
     GroupIn x;
+    if (p.targets != nullptr) {  // prompt scoring: row g alone, 20 natural alternatives, chosen = target
+        x.r0 = g;
+        x.r1 = g + 1;
+        x.req = 1;
+        x.samp = __ldg(&p.targets[g]);
+        x.cnt = 0;
+        x.K = kScoreAlts;
+        return x;
+    }
     x.r0 = __ldg(&p.indptr[g]);
     x.r1 = __ldg(&p.indptr[g + 1]);
     x.req = __ldg(&p.requested[g]);
@@ -591,7 +606,7 @@ __global__ void __launch_bounds__(1024) lp_prepare_kernel(Params p) {
                     kc = cnt;
                     mode = kModeLse;
                 } else {
-                    if (K < 0 || K > p.k_alt_max) {
+                    if ((K < 0 || K > p.k_alt_max) && p.targets == nullptr) {
                         st |= kStatusBadCount;
                         K = K < 0 ? 0 : p.k_alt_max;
                     }
@@ -600,7 +615,22 @@ __global__ void __launch_bounds__(1024) lp_prepare_kernel(Params p) {
                 }
             }
             need = req || k >= 1 || samp < 0;
-            if (!need) {
+            if (p.targets != nullptr) {
+                // prompt scoring: a row without a valid target is not read; its
+                // record is the invalid one (id -1, NaN, rank 0, ids -1)
+                need = samp >= 0 && samp < p.V;
+                if (!need) {
+                    if (samp >= p.V) st |= kStatusBadToken;
+                    int* rec = p.score_records + (long long)r0 * kScoreWords;
+                    rec[0] = -1;
+                    rec[1] = (int)kUnusedBits;
+                    rec[2] = 0;
+                    for (int i = 0; i < kScoreAlts; ++i) {
+                        rec[3 + 2 * i] = -1;
+                        rec[4 + 2 * i] = (int)kUnusedBits;
+                    }
+                }
+            } else if (!need) {
                 if (samp >= p.V) st |= kStatusBadToken;
                 p.emitted[r0] = samp;
                 p.accepted[g] = 0;
@@ -1116,6 +1146,9 @@ __device__ __forceinline__ bool tile_work(const Params& p, Shared& sm, const uns
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int mode = info.w;
     const bool natural = mode == kModeNatural;
+    // prompt scoring: the target's logit, loaded now and used after the passes
+    float xt = 0.0f;
+    if (p.targets != nullptr && lane == 0) xt = load_logit<ELT>(p, info.x, __ldg(&p.targets[info.x]));
     // pass 1: maxima (per vector for a full tile)
     uint32_t cm[TileLayout<ELT>::NCH];
     const float m = stage_max<ELT, FULL>(sp, tid, nv, cm);
@@ -1176,7 +1209,37 @@ __device__ __forceinline__ bool tile_work(const Params& p, Shared& sm, const uns
             if (warp == 0) C.tslot = (long long)info.x * p.T + info.y;
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.ccand[ns]);  // the selector warp takes it from here
+        if (lane == 0) mbar_arrive(&sm.ccand[ns]);  // the helper warp takes it from here
+        if (p.targets != nullptr) {
+            // prompt scoring: this warp's lanes whose logit is above the target's,
+            // and the smallest of those logits (the rank is finished in the record
+            // kernel, once lse is known); vectors whose maximum is not above it
+            // are skipped
+            const float t = __shfl_sync(kFull, xt, 0);
+            int cnt = 0;
+            float mn = kPosInf;
+#pragma unroll
+            for (int c = 0; c < TileLayout<ELT>::NCH; ++c) {
+                if (!(vec_max<ELT>(cm[c]) > t)) continue;
+                const uint4 v = ld_vec<ELT, FULL>(sp, c, tid, nv);
+                const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int e = 0; e < TileLayout<ELT>::EPV; ++e) {
+                    const float x = (ELT == 2) ? ((e & 1) ? bf16_hi(w4[e >> 1]) : bf16_lo(w4[e >> 1]))
+                                               : __uint_as_float(w4[e]);
+                    if (x > t) {
+                        ++cnt;
+                        mn = fminf(mn, x);
+                    }
+                }
+            }
+            cnt = (int)__reduce_add_sync(kFull, (unsigned)cnt);
+            mn = warp_min_f(mn);
+            if (lane == 0) {
+                const long long wslot = ((long long)info.x * p.T + info.y) * kWarps + warp;
+                p.part_rank[wslot] = make_int2(cnt, (int)__float_as_uint(mn));
+            }
+        }
     }
     // partial results of the warp, then the tile goes to the helper warp
     // through a done slot: once the 8 warps arrived, it counts the tile for
@@ -1275,7 +1338,7 @@ __device__ __noinline__ bool decide_row(const Params& p, int2* cur) {
     const int g = entry >> 4, j = entry & 15;
     const int4 d = __ldcg(&p.gdesc[g]);
     const unsigned long long bk = atomicMax(&p.row_best[row], 0ull);  // read at its point of coherence
-    const int draft = __ldg(&p.drafts[row]);
+    const int draft = p.drafts != nullptr ? __ldg(&p.drafts[row]) : -1;  // none when scoring
     const int r0 = d.x, k = d.y & 0xFF, req = (d.y >> 13) & 1, samp = d.w, mode = (d.y >> 8) & 3;
     const uint32_t amax = key_id(bk);
     const int chosen = (k == 0 && samp >= 0) ? samp : (int)amax;
@@ -1295,10 +1358,12 @@ __device__ __noinline__ bool decide_row(const Params& p, int2* cur) {
     } else if (p.read_ahead && j < k) {
         atomicAdd(&p.tclaim[row + 1], kClosed);  // the next row is not needed
     }
-    p.emitted[row] = chosen;
-    if (!accept) {
-        p.accepted[g] = j;
-        for (int jj = j + 1; jj <= k; ++jj) p.emitted[r0 + jj] = -1;
+    if (p.emitted != nullptr) {  // generation outputs (none when scoring)
+        p.emitted[row] = chosen;
+        if (!accept) {
+            p.accepted[g] = j;
+            for (int jj = j + 1; jj <= k; ++jj) p.emitted[r0 + jj] = -1;
+        }
     }
     if (req) {
         if (chosen >= p.V) atomicOr(p.status, kStatusBadToken);
@@ -1522,6 +1587,28 @@ __device__ __noinline__ void natural_from_top32(const Params& p, int* rec, int r
     }
 }
 
+// Prompt scoring: the largest float X with fl32(X - lse) <= lp, where lp =
+// fl32(xt - lse) is the target's logprob.  x -> fl32(x - lse) is monotone, so a
+// logit is reported strictly above the target exactly when it is above X, and
+// the logits in (xt, X] are the ones whose logprob rounds to the target's.  A
+// warp search over the ordered bit patterns in [xt, +inf]: each round the 32
+// lanes test 32 points spread over the interval, and the interval shrinks to
+// the gap between the last point that holds and the first that does not.
+__device__ __forceinline__ float score_limit(float xt, float lse, float lp, int lane) {
+    uint32_t lo = ord32(xt), hi = ord32(kPosInf);  // the predicate holds at lo
+    if (__fsub_rn(kPosInf, lse) <= lp) return kPosInf;
+    while (hi - lo > 1u) {
+        const uint32_t q = lo + (uint32_t)(((unsigned long long)(hi - lo) * (unsigned)(lane + 1)) / 33ull);
+        const bool ok = __fsub_rn(unord32(q), lse) <= lp;
+        const int n = __popc(__ballot_sync(kFull, ok));  // the points that hold are a prefix
+        const uint32_t nlo = __shfl_sync(kFull, q, n > 0 ? n - 1 : 0);
+        const uint32_t nhi = __shfl_sync(kFull, q, n < 32 ? n : 31);
+        lo = n > 0 ? nlo : lo;
+        hi = n < 32 ? nhi : hi;
+    }
+    return unord32(lo);
+}
+
 // Merges two (max, sum exp(x - max)) pairs.
 __device__ __forceinline__ void ms_merge(float& m, float& s, float m2, float s2) {
     const float M = fmaxf(m, m2);
@@ -1543,14 +1630,19 @@ __device__ __noinline__ void record_block(const Params& p, RecShared& sm, int ro
     const int T = p.T;
     const long long base = (long long)row * T;
     const bool natural = !ids && mode == kModeNatural && kc > 0;
+    const bool score = p.targets != nullptr;
     for (int w = tid; w < kRecordWords; w += kConsumerThreads)
         sm.rec[w] = (w >= 2 && (w & 1) == 0) ? -1 : (int)kUnusedBits;
+    if (tid == 0) sm.corr = 0;
     // loads: tile partials, the chosen logit, explicit-id logits, tile key lists
     float m = kNegInf, s = 0.0f;
+    int above = 0;  // prompt scoring: logits above the target's
     for (int t = tid; t < T * kWarps; t += kConsumerThreads) {  // one (max, exp-sum) per warp of each tile
         const float2 ms = __ldcg(&p.part_ms[base * kWarps + t]);
         ms_merge(m, s, ms.x, ms.y);
+        if (score) above += __ldcg(&p.part_rank[base * kWarps + t]).x;
     }
+    if (score) above = (int)__reduce_add_sync(kFull, (unsigned)above);
     float xc = 0.0f;
     if (tid == 32 && chosen >= 0 && chosen < p.V) xc = load_logit<ELT>(p, row, chosen);
     int id = -1;
@@ -1577,6 +1669,7 @@ __device__ __noinline__ void record_block(const Params& p, RecShared& sm, int ro
     if (lane == 0) {
         sm.red_f[warp] = m;
         sm.red_f2[warp] = s;
+        sm.red_i[warp] = above;
     }
     if (tid == 32) sm.xchosen = xc;
     cbar();
@@ -1596,6 +1689,10 @@ __device__ __noinline__ void record_block(const Params& p, RecShared& sm, int ro
             sm.rec[1] = (chosen >= 0 && chosen < p.V) ? (int)__float_as_uint(logprob(sm.xchosen, lse))
                                                       : (int)kUnusedBits;
             if (p.lse_out) p.lse_out[row] = lse;
+        }
+        if (score) {
+            const float lp = logprob(sm.xchosen, lse);
+            sm.xlim = lp == lp ? score_limit(sm.xchosen, lse, lp, lane) : sm.xchosen;  // NaN: nothing is above
         }
         if (natural) {
             const unsigned long long b0 = merge_lists(sm.lists[0][lane], sm.lists[1][lane], lane);
@@ -1617,9 +1714,39 @@ __device__ __noinline__ void record_block(const Params& p, RecShared& sm, int ro
         sm.rec[2 + 2 * tid] = id;
         sm.rec[3 + 2 * tid] = bits;
     }
+    if (score) {
+        // logits in (xt, X]: above the target's but reported equal to it.  Only
+        // a tile whose smallest logit above the target's is <= X holds any.
+        const float xt = sm.xchosen, X = sm.xlim;
+        int corr = 0;
+        for (int t = warp; t < T; t += kWarps) {
+            const float mn = lane < kWarps ? __uint_as_float((uint32_t)__ldcg(&p.part_rank[(base + t) * kWarps + lane]).y)
+                                           : kPosInf;
+            if (!__any_sync(kFull, mn <= X)) continue;
+            const long long t0e = (long long)t * tile_elems<ELT>();
+            const long long remv = p.V - t0e;
+            const int nvt = remv < tile_elems<ELT>() ? (int)remv : tile_elems<ELT>();
+            for (int e = lane; e < nvt; e += 32) {
+                const float x = load_logit<ELT>(p, row, t0e + e);
+                corr += (x > xt && x <= X) ? 1 : 0;
+            }
+        }
+        corr = (int)__reduce_add_sync(kFull, (unsigned)corr);
+        if (lane == 0 && corr != 0) atomicAdd(&sm.corr, corr);
+    }
     cbar();
-    int* out = p.records + (long long)row * kRecordWords;
-    for (int w = tid; w < kRecordWords; w += kConsumerThreads) out[w] = sm.rec[w];
+    if (score) {
+        // record: target, its lp, rank, then the 20 alternatives
+        int above_all = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) above_all += sm.red_i[w];
+        int* out = p.score_records + (long long)row * kScoreWords;
+        for (int w = tid; w < kScoreWords; w += kConsumerThreads)
+            out[w] = w < 2 ? sm.rec[w] : w == 2 ? 1 + above_all - sm.corr : sm.rec[w - 1];
+    } else {
+        int* out = p.records + (long long)row * kRecordWords;
+        for (int w = tid; w < kRecordWords; w += kConsumerThreads) out[w] = sm.rec[w];
+    }
     cbar();
 }
 

@@ -29,6 +29,7 @@ struct lp_plan_s {
     int4* gdesc;
     int4* rec_tasks;
     float2* part_ms;
+    int2* part_rank;
     unsigned long long* part_keys;
     size_t part_ms_bytes, part_keys_bytes;
     bool bound;
@@ -75,7 +76,7 @@ int check_desc(const lp_plan_desc* d) {
 }
 
 struct Layout {
-    size_t ctrl, queue, tclaim, row_best, done, gdesc, rec_tasks, part_ms, part_keys, total;
+    size_t ctrl, queue, tclaim, row_best, done, gdesc, rec_tasks, part_ms, part_rank, part_keys, total;
     size_t part_ms_bytes, part_keys_bytes;
 };
 
@@ -102,6 +103,8 @@ Layout layout_of(const lp_plan_desc* d) {
     L.part_ms = off;
     L.part_ms_bytes = rows * T * (lp::kConsumerThreads / 32) * sizeof(float2);
     off = align_up(off + L.part_ms_bytes);
+    L.part_rank = off;
+    off = align_up(off + rows * T * (lp::kConsumerThreads / 32) * sizeof(int2));
     L.part_keys = off;
     L.part_keys_bytes = rows * T * lp::kKeysPerTile * sizeof(unsigned long long);
     off = align_up(off + L.part_keys_bytes);
@@ -199,6 +202,7 @@ lp::Params make_params(const lp_plan_s* plan, const lp_io& io) {
     p.gdesc = plan->gdesc;
     p.rec_tasks = plan->rec_tasks;
     p.part_ms = plan->part_ms;
+    p.part_rank = plan->part_rank;
     p.part_keys = plan->part_keys;
     p.timeout_ns = (unsigned long long)(plan->d.timeout_ns > 0 ? plan->d.timeout_ns : kDefaultTimeoutNs);
     p.debug_flags = plan->d.flags & LP_PLAN_DEBUG_FORCE_TIMEOUT;
@@ -271,6 +275,7 @@ int lp_plan_create(lp_plan_t* out, const lp_plan_desc* desc) {
     plan->gdesc = reinterpret_cast<int4*>(plan->scratch + L.gdesc);
     plan->rec_tasks = reinterpret_cast<int4*>(plan->scratch + L.rec_tasks);
     plan->part_ms = reinterpret_cast<float2*>(plan->scratch + L.part_ms);
+    plan->part_rank = reinterpret_cast<int2*>(plan->scratch + L.part_rank);
     plan->part_keys = reinterpret_cast<unsigned long long*>(plan->scratch + L.part_keys);
     plan->part_ms_bytes = L.part_ms_bytes;
     plan->part_keys_bytes = L.part_keys_bytes;
@@ -430,6 +435,41 @@ int lp_run_host(lp_plan_t plan, const lp_io* h, void* stream) {
     return LP_OK;
 }
 
+int lp_score(lp_plan_t plan, const lp_score_io* io, void* stream) {
+    if (!plan || !io) return LP_EINVAL;
+    if (io->rows < 0 || io->rows > plan->d.max_rows || io->rows > plan->d.max_groups) return LP_ESHAPE;
+    if (io->rows > 0 && (!io->logits || !io->target_tokens || !io->records)) return LP_EINVAL;
+    if (!io->status) return LP_EINVAL;
+    if (!aligned(io->logits, 16)) return LP_EALIGN;
+    if (!aligned(io->target_tokens, 4) || !aligned(io->records, 4) || !aligned(io->status, 4)) return LP_EALIGN;
+    if (io->lse_out && !aligned(io->lse_out, 4)) return LP_EALIGN;
+    DeviceGuard guard(plan->d.device);
+    if (!guard.ok) return cuda_fail(cudaGetLastError());
+    if (io->rows == 0) {  // nothing to score: status only
+        const cudaError_t e0 = cudaMemsetAsync(io->status, 0, sizeof(uint32_t), static_cast<cudaStream_t>(stream));
+        if (e0 != cudaSuccess) return cuda_fail(e0);
+        plan->last_stream = static_cast<cudaStream_t>(stream);
+        return LP_OK;
+    }
+    // the epilogue's machinery with one group per row (k = 0): no group vectors,
+    // drafts or generation outputs
+    lp_io g{};
+    g.logits = io->logits;
+    g.lse_out = io->lse_out;
+    g.status = io->status;
+    g.rows = io->rows;
+    g.groups = io->rows;
+    lp::Params p = make_params(plan, g);
+    p.k_max = 0;
+    p.targets = io->target_tokens;
+    p.score_records = io->records;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const cudaError_t e = lp::launch_epilogue(p, plan->d.dtype, plan->cfg, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    plan->last_stream = s;
+    return LP_OK;
+}
+
 int lp_debug_tiles_read(lp_plan_t plan, int32_t* host_tiles, int32_t rows) {
     if (!plan || !host_tiles || rows < 0 || rows > plan->d.max_rows) return LP_EINVAL;
     DeviceGuard guard(plan->d.device);
@@ -446,6 +486,8 @@ int lp_debug_poison_scratch(lp_plan_t plan, void* stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaMemsetAsync(plan->part_ms, 0xFF, plan->part_ms_bytes, s);
     if (e == cudaSuccess) e = cudaMemsetAsync(plan->part_keys, 0xFF, plan->part_keys_bytes, s);
+    // the scoring partials: one int2 per warp of a tile, the size of part_ms
+    if (e == cudaSuccess) e = cudaMemsetAsync(plan->part_rank, 0xFF, plan->part_ms_bytes, s);
     if (e != cudaSuccess) return cuda_fail(e);
     return LP_OK;
 }
@@ -567,6 +609,7 @@ extern "C" int lp_run_static(const lp_plan_desc* desc, const lp_io* io, void* st
     run.gdesc = reinterpret_cast<int4*>(base + L.gdesc);
     run.rec_tasks = reinterpret_cast<int4*>(base + L.rec_tasks);
     run.part_ms = reinterpret_cast<float2*>(base + L.part_ms);
+    run.part_rank = reinterpret_cast<int2*>(base + L.part_rank);
     run.part_keys = reinterpret_cast<unsigned long long*>(base + L.part_keys);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // The array keeps the previous call's contents.  The control block must

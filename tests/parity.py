@@ -226,3 +226,78 @@ def check_tiles(w: W.Workload, orc: dict, tiles: np.ndarray, strict: bool) -> No
     assert np.array_equal(tiles[prefix], want[prefix]), "prefix rows read in full"
     assert ((tiles >= 0) & (tiles <= allowed)).all(), "no row read beyond the one after a prefix"
 
+
+
+# ----------------------------------------------------------------- prompt scoring
+
+SCORE_WORDS = 43
+
+
+def run_gpu_score(w: W.Workload, targets, plan=None, poison=False, runs=1):
+    """Prompt scoring on the CUDA path: numpy records [rows, 43], lse, status."""
+    import torch
+    if plan is None:
+        plan = make_plan(w)
+    dev = torch.device("cuda", 0)
+    d = to_device(w)
+    rows = w.rows
+    tg = torch.from_numpy(np.ascontiguousarray(targets, np.int32)).to(dev)
+    rec = torch.full((max(rows, 1), SCORE_WORDS), SENTINEL, dtype=torch.int32, device=dev)
+    lse = torch.full((max(rows, 1),), LSE_SENTINEL, dtype=torch.float32, device=dev)
+    st = torch.full((1,), -1, dtype=torch.int32, device=dev)
+    for _ in range(runs):
+        if poison:
+            plan.poison_scratch()
+        plan.score(logits=d["logits"], target_tokens=tg, records=rec, status=st, lse_out=lse)
+    torch.cuda.synchronize()
+    res = dict(records=rec.cpu().numpy()[:rows], lse=lse.cpu().numpy()[:rows],
+               status=int(st.cpu().numpy().view(np.uint32)[0]), tiles_read=plan.tiles_read(rows))
+    return res, plan
+
+
+def run_oracle_score(w: W.Workload, targets, threads: int = 8):
+    return oracle.score(w.logits_f32(), w.V, np.asarray(targets, np.int32), threads=threads)
+
+
+def compare_score(w: W.Workload, targets, gpu: dict, orc: dict) -> dict:
+    """Parity of prompt-scoring records.  The integer words are bit-exact; the
+    ones FP32 decides (the target's lp bits, its rank, the alternatives and
+    their order) are decided on both sides with the CUDA path's lse, which must
+    itself be within the tolerance of the oracle's."""
+    stats = {"scored": 0, "strict_rows": 0, "max_lse_err": 0.0, "max_lp_err": 0.0, "ranks_above_1": 0}
+    assert gpu["status"] == orc["status"], (hex(gpu["status"]), hex(orc["status"]))
+    for r in range(w.rows):
+        t = int(targets[r])
+        grec, orec = gpu["records"][r], orc["records"][r]
+        if not (0 <= t < w.V):
+            assert np.array_equal(grec, orec), f"row {r}: invalid-target record"
+            assert gpu["lse"][r] == np.float32(LSE_SENTINEL), f"row {r}: lse written for an unread row"
+            continue
+        stats["scored"] += 1
+        olse, glse = np.float32(orc["lse"][r]), np.float32(gpu["lse"][r])
+        tol = row_tol(olse)
+        err = abs(float(olse) - float(glse))
+        stats["max_lse_err"] = max(stats["max_lse_err"], err)
+        assert err <= tol, f"row {r}: lse {glse} vs {olse}"
+        if olse.view(np.uint32) == glse.view(np.uint32):
+            stats["strict_rows"] += 1
+            assert np.array_equal(grec, orec), f"row {r}: lse identical but records differ at " \
+                f"{np.flatnonzero(grec != orec)[:8]}"
+            continue
+        x = w.logits_f32(r)[:w.V]
+        assert grec[0] == t, f"row {r}: target id"
+        lp = oracle.logprob(x[t], glse)
+        assert (int(grec[1]) & 0xFFFFFFFF) == int(np.float32(lp).view(np.uint32)), f"row {r}: lp bits"
+        _cmp_lp(r, "target", grec[1], orec[1], stats, tol)
+        assert grec[2] == oracle.rank(x, glse, lp), f"row {r}: rank {grec[2]} vs {oracle.rank(x, glse, lp)}"
+        ids, lps = oracle.topk(x, 20, glse)
+        n = ids.size
+        assert np.array_equal(grec[3::2][:n], ids), f"row {r}: alternative ids"
+        assert np.array_equal(grec[4::2][:n].view(np.uint32), lps.view(np.uint32)), f"row {r}: alternative lps"
+        assert (grec[3::2][n:] == -1).all() and (grec[4::2][n:] == NAN_BITS).all(), f"row {r}: unused pairs"
+        for i in range(n):
+            _cmp_lp(r, f"alt[{i}]", grec[4 + 2 * i], orec[4 + 2 * i], stats, tol)
+    for r in range(w.rows):
+        if 0 <= int(targets[r]) < w.V and gpu["records"][r][2] > 1:
+            stats["ranks_above_1"] += 1
+    return stats

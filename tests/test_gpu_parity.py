@@ -300,3 +300,114 @@ def test_host_buffers_match_device_run():
     assert np.array_equal(arrays["accepted"].numpy(), ref["accepted"])
     assert np.array_equal(arrays["emitted_tokens"].numpy(), ref["emitted_tokens"])
     plan.close()
+
+
+# ----------------------------------------------------------------- prompt scoring
+
+def _score(w, targets, plan=None, **kw):
+    gpu, plan = PT.run_gpu_score(w, targets, plan=plan, **kw)
+    orc = PT.run_oracle_score(w, targets, THREADS)
+    stats = PT.compare_score(w, targets, gpu, orc)
+    te = PT.lpe_tile_elems(w.dtype)
+    T = (w.V + te - 1) // te
+    valid = (np.asarray(targets) >= 0) & (np.asarray(targets) < w.V)
+    assert np.array_equal(gpu["tiles_read"], np.where(valid, T, 0)), "rows read: exactly the valid targets'"
+    plan.close()
+    return gpu, orc, stats
+
+
+def _score_rows(rows_f32, V, *, dtype="f32", Vp=None):
+    n = np.asarray(rows_f32).shape[0]
+    return W.custom(rows_f32, V, [1] * n, dtype=dtype, Vp=Vp, k_max=0)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_score_prompt_workload(dtype):
+    w = W.prompt(rows=48, dtype=dtype)
+    _, _, st = _score(w, w.meta["targets"])
+    assert st["scored"] >= 40 and st["ranks_above_1"] >= 20
+
+
+def test_score_prompt_full_size():
+    w = W.prompt()
+    _, _, st = _score(w, w.meta["targets"])
+    assert st["scored"] >= 480
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_score_collapse_rescans_every_tile(dtype):
+    # one logit of 3e7, the others in [0, 0.5] over several tiles: every other
+    # logprob rounds to the maximum's negated, so each non-maximal target has
+    # rank 2 and every tile holds logits reported equal to the target's
+    rng = np.random.default_rng(31)
+    V = 40_000
+    x = rng.uniform(0.0, 0.5, (6, V)).astype(np.float32)
+    x[:, 17] = np.float32(3e7)
+    targets = np.array([17, 0, V - 1, 20_000, 16_384, 8_191], np.int32)
+    gpu, _, _ = _score(_score_rows(x, V, dtype=dtype), targets)
+    assert gpu["records"][0][2] == 1 and (gpu["records"][1:, 2] == 2).all()
+
+
+def test_score_fp32_subtraction_collisions():
+    # FP32 logits near 0 under an lse near 1000: the ulp of the difference
+    # (6e-5) merges many distinct logits with the target's
+    rng = np.random.default_rng(32)
+    V = 30_000
+    x = rng.standard_normal((8, V)).astype(np.float32) * np.float32(1e-3)
+    x[:, 5] = np.float32(1000.0)
+    targets = np.array([0, 1, 2, 3, 4, 6, 29_999, 5], np.int32)
+    gpu, _, _ = _score(_score_rows(x, V), targets)
+    assert (gpu["records"][:7, 2] > 1).all() and gpu["records"][7][2] == 1
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_score_ties_invalid_and_masked(dtype):
+    rng = np.random.default_rng(33)
+    V = 20_000
+    x = (np.round(rng.standard_normal((8, V)) * 4) / 4).astype(np.float32)
+    x[2, ::3] = -np.inf                      # a masked vocabulary
+    x[5, 1:] = -np.inf                       # a single live lane
+    x[6, :100] = np.float32(-0.0)
+    targets = np.array([int(np.argmax(x[0])), 7, 3, -1, V, 0, 50, V + 7], np.int32)
+    gpu, orc, _ = _score(_score_rows(x, V, dtype=dtype), targets)
+    assert gpu["status"] == 0x2
+    assert gpu["records"][0][2] == 1
+    assert gpu["records"][2][2] == 1 + int(np.isfinite(x[2]).sum())  # a masked target: below every live lane
+
+
+@pytest.mark.parametrize("V,Vp,dtype", [(7, 8, "bf16"), (19, 20, "f32"), (1, 4, "f32"), (10_001, 10_008, "bf16"),
+                                        (16_385, 16_388, "f32"), (8192, 8192, "f32")])
+def test_score_ragged_vocabularies(V, Vp, dtype):
+    rng = np.random.default_rng(V + 1)
+    x = rng.normal(0, 2, (4, V)).astype(np.float32)
+    targets = rng.integers(0, V, 4).astype(np.int32)
+    _score(_score_rows(x, V, dtype=dtype, Vp=Vp), targets)
+
+
+def test_score_and_generation_share_a_plan():
+    # scoring on a plan between generation runs: poisoned scratch, no state left behind
+    w = W.decode(rows=12)
+    plan = PT.make_plan(w)
+    _check(w, plan=plan, poison=True)
+    plan = PT.make_plan(w)
+    ws = W.prompt(rows=12)
+    gpu, _ = PT.run_gpu_score(ws, ws.meta["targets"], plan=plan, poison=True)
+    PT.compare_score(ws, ws.meta["targets"], gpu, PT.run_oracle_score(ws, ws.meta["targets"], THREADS))
+    gen, _ = PT.run_gpu(w, plan=plan, poison=True)
+    PT.compare(w, gen, PT.run_oracle(w, THREADS))
+    plan.close()
+
+
+def test_score_no_rows():
+    w = W.prompt(rows=4)
+    import torch
+    import logprob_epilogue_gb300 as lpe
+    plan = PT.make_plan(w)
+    dev = torch.device("cuda", 0)
+    st = torch.full((1,), -1, dtype=torch.int32, device=dev)
+    plan.score(logits=torch.zeros((0, w.Vp), dtype=torch.bfloat16, device=dev),
+               target_tokens=torch.zeros(1, dtype=torch.int32, device=dev),
+               records=torch.zeros((1, lpe.SCORE_WORDS), dtype=torch.int32, device=dev), status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    plan.close()

@@ -15,6 +15,11 @@ K natural alternatives or up to 128 explicit ids):
   wide   4 x 1,048,576 (stride 1,048,704) BF16, N(0,1), 1% of lanes +8,
          a 64-way exact tie at the maximum, one group of k=3
 
+and, for prompt scoring, one target token per row:
+
+  prompt 512 x 151,936 (stride 152,064) BF16, N(0,2.5) + 3 spikes, targets
+         30% spike ids, 3% -1, the rest uniform
+
 Pad lanes (between V and the row stride) hold +1e30 so that any leak into a
 result is visible.  Where a draft must equal its row's argmax, the generator
 plants that argmax: it writes a value above every other lane of the row (the
@@ -31,7 +36,7 @@ import numpy as np
 MAX_IDS = 128
 PAD_VALUE = 1e30
 
-SEEDS = {"tiny": 0, "decode": 1, "spec": 2, "large": 3, "wide": 4}
+SEEDS = {"tiny": 0, "decode": 1, "spec": 2, "large": 3, "wide": 4, "prompt": 5}
 NAMES = ("tiny", "decode", "spec", "large", "wide")
 
 
@@ -272,8 +277,38 @@ def wide(seed: int = SEEDS["wide"]) -> Workload:
                   meta={"tie_value": float(tie_value)})
 
 
+def prompt(seed: int = SEEDS["prompt"], rows: int = 512, V: int = 151_936, Vp: int = 152_064,
+           dtype: str = "bf16") -> Workload:
+    """Prompt scoring: one row per prompt position, N(0,2.5) + 3 spikes of
+    +U[12,18]; meta["targets"] holds the scored tokens: a spike id for 30% of
+    the rows (a well-predicted token), -1 for 3% (the prompt-end marker), a
+    uniform id otherwise."""
+    rng = np.random.default_rng(seed)
+    vals = np.empty((rows, Vp), np.float32)
+    targets = np.empty(rows, np.int32)
+    kind = rng.random(rows)
+    for r0 in range(0, rows, 64):
+        n = min(64, rows - r0)
+        vals[r0:r0 + n, :V] = rng.standard_normal((n, V), dtype=np.float32) * np.float32(2.5)
+    for r in range(rows):
+        ids = _distinct_ids(rng, V, 3)
+        vals[r, ids] += rng.uniform(12.0, 18.0, size=3).astype(np.float32)
+        targets[r] = ids[int(rng.integers(0, 3))] if kind[r] < 0.3 else (-1 if kind[r] < 0.33
+                                                                           else int(rng.integers(0, V)))
+    gi = np.arange(rows + 1)
+    drafts = np.full(rows, -1, np.int32)
+    req = np.ones(rows)
+    topk = np.full(rows, 20)
+    tids = np.full((rows, MAX_IDS), -1, np.int32)
+    cnts = np.zeros(rows)
+    planted = np.full(rows, -1, np.int32)
+    return _store("prompt", dtype, V, Vp, 0, vals, gi, drafts, targets, req, topk, tids, cnts, planted,
+                  meta={"targets": targets})
+
+
 def make(name: str, **kw) -> Workload:
-    return {"tiny": tiny, "decode": decode, "spec": spec, "large": large, "wide": wide}[name](**kw)
+    return {"tiny": tiny, "decode": decode, "spec": spec, "large": large, "wide": wide,
+            "prompt": prompt}[name](**kw)
 
 
 def custom(rows_f32: np.ndarray, V: int, group_sizes, *, dtype: str = "f32", Vp: int | None = None,
