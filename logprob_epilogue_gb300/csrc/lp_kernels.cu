@@ -210,11 +210,6 @@ __device__ __forceinline__ float warp_min_f(float v) {
     return v;
 }
 
-__device__ __forceinline__ float warp_max_f(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
-    return v;
-}
 __device__ __forceinline__ float warp_sum_f(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
@@ -299,23 +294,16 @@ struct RecShared {
 
 // ---- tile element access
 //
-// Full tiles: thread i owns the 16-byte vectors c*256 + i (c = 0..NCH-1), so
-// element k = c*EPV + s of the thread is tile element (c*256 + i)*EPV + s.
-// Partial tiles (the last tile of a row): element k of thread i is tile element
-// k*256 + i, masked beyond the valid count.  Both orders are ascending in k.
+// Thread i owns the 16-byte vectors c*256 + i (c = 0..NCH-1), so element
+// k = c*EPV + s of the thread is tile element (c*256 + i)*EPV + s.  The last,
+// partial tile of a row is read the same way once its lanes past V are set to
+// -inf in the stage (fill_partial).
 
 template <int ELT>
 struct TileLayout {
     static constexpr int EPV = 16 / ELT;          // elements per 16-byte vector
     static constexpr int NCH = kTileBytes / 16 / kConsumerThreads;  // vectors per thread (8)
-    static constexpr int EPT = EPV * NCH;         // elements per thread (64 BF16, 32 FP32)
 };
-
-template <int ELT>
-__device__ __forceinline__ int tile_elem_id(bool full, int k, int tid) {
-    using L = TileLayout<ELT>;
-    return full ? ((k / L::EPV) * kConsumerThreads + tid) * L::EPV + (k % L::EPV) : k * kConsumerThreads + tid;
-}
 
 // 16-byte shared-memory load through an explicit shared-space address.
 __device__ __forceinline__ uint4 lds128(const void* p) {
@@ -859,17 +847,6 @@ __device__ __noinline__ void producer_loop(const Params& p, Shared& sm, unsigned
 // ------------------------------------------------------------------ tile: candidate selection
 
 // Element k of the calling thread (tile layout), read from the stage; -inf past nv.
-template <int ELT>
-__device__ __forceinline__ float stage_elem(const unsigned char* sp, bool full, int nv, int k, int tid) {
-    const int e = tile_elem_id<ELT>(full, k, tid);
-    if (e >= nv) return kNegInf;
-    if constexpr (ELT == 4) {
-        return reinterpret_cast<const float*>(sp)[e];
-    } else {
-        return __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const unsigned short*>(sp)[e]) << 16);
-    }
-}
-
 __device__ __forceinline__ int warp_excl_scan_i(int v, int lane, int* total) {
     int incl = v;
 #pragma unroll
@@ -879,69 +856,6 @@ __device__ __forceinline__ int warp_excl_scan_i(int v, int lane, int* total) {
     }
     *total = __shfl_sync(kFull, incl, 31);
     return incl - v;
-}
-
-// Exact best 32 keys (value descending, id ascending) of the warp's share of a
-// tile, for the rare warp with more than 32 elements >= theta (large runs of
-// equal values): the 32nd largest value v is found by walking distinct values
-// down from the warp's maximum; the result is every element above v, then the
-// smallest ids equal to v, written to region[0..32) in no particular order.
-// Reads the stage element by element.
-template <int ELT>
-__device__ __forceinline__ void warp_top32_exact(const unsigned char* sp, bool full, int nv, int tbase, int tid,
-                                              unsigned long long* region) {
-    using L = TileLayout<ELT>;
-    const int lane = tid & 31;
-    float v = kPosInf;
-    for (int it = 0; it < 33; ++it) {
-        float loc = kNegInf;
-        for (int k = 0; k < L::EPT; ++k) {
-            const float x = stage_elem<ELT>(sp, full, nv, k, tid);
-            loc = (x < v && x > loc) ? x : loc;
-        }
-        const float vn = warp_max_f(loc);
-        if (!(vn > kNegInf)) break;  // nothing left below v
-        v = vn;
-        int c = 0;
-        for (int k = 0; k < L::EPT; ++k) {
-            const float x = stage_elem<ELT>(sp, full, nv, k, tid);
-            c += (x >= v && x > kNegInf) ? 1 : 0;
-        }
-        if (warp_sum_i(c) >= 32) break;
-    }
-    int gt = 0;
-    for (int k = 0; k < L::EPT; ++k) {
-        const float x = stage_elem<ELT>(sp, full, nv, k, tid);
-        gt += (x > v && x > kNegInf) ? 1 : 0;
-    }
-    int got = 0;
-    int pos = warp_excl_scan_i(gt, lane, &got);  // got < 32: v is the 32nd largest value
-    for (int k = 0; k < L::EPT; ++k) {
-        const float x = stage_elem<ELT>(sp, full, nv, k, tid);
-        if (x > v && x > kNegInf) region[pos++] = make_key(x, (uint32_t)(tbase + tile_elem_id<ELT>(full, k, tid)));
-    }
-    // elements equal to v in ascending id order: vector by vector (full tiles) or
-    // element by element (partial tiles), lanes in order within each
-    const int NQ = full ? L::NCH : L::EPT;
-    const int SPQ = full ? L::EPV : 1;
-    for (int q = 0; q < NQ && got < 32; ++q) {
-        int mine = 0;
-        for (int e = 0; e < SPQ; ++e) {
-            const float x = stage_elem<ELT>(sp, full, nv, q * SPQ + e, tid);
-            mine += (x == v && x > kNegInf) ? 1 : 0;
-        }
-        int total = 0;
-        int before = warp_excl_scan_i(mine, lane, &total);
-        for (int e = 0; e < SPQ; ++e) {
-            const int k = q * SPQ + e;
-            const float x = stage_elem<ELT>(sp, full, nv, k, tid);
-            if (x == v && x > kNegInf) {
-                if (got + before < 32) region[got + before] = make_key(x, (uint32_t)(tbase + tile_elem_id<ELT>(full, k, tid)));
-                ++before;
-            }
-        }
-        got += total;
-    }
 }
 
 // Warp-level top-4 extraction on ord32 values: returns the 4th largest
@@ -977,6 +891,115 @@ __device__ __forceinline__ int first_equal(const unsigned char* sp, int tid, int
         ef = (x == m) ? e : ef;
     }
     return (cf * kConsumerThreads + tid) * L::EPV + ef;
+}
+
+// Exact best 32 keys (value descending, id ascending) of the warp's share of a
+// tile, for the rare warp with more than 32 elements >= theta (long runs of
+// equal or close values).  The warp's 32nd largest value v is found by
+// bisection over the ordered bit patterns in [theta, warp maximum] (BF16: over
+// the 16-bit patterns of BF16 values only); each probe counts, warp-wide, the
+// elements >= it in the thread's vectors whose maximum reaches theta (pass),
+// since no other vector holds one.  Then every element above v (fewer than 32)
+// and the smallest ids equal to v are written to region[0..32), in no
+// particular order.  The -inf lanes of a partial tile are never taken.
+template <int ELT, bool FULL>
+__device__ __noinline__ void warp_top32_select(const unsigned char* sp, int tid, unsigned pass, float theta,
+                                               uint32_t omx, int tbase, unsigned long long* region) {
+    using L = TileLayout<ELT>;
+    const int lane = tid & 31;
+    auto elem = [](const uint32_t (&w)[4], int e) {
+        return (ELT == 2) ? ((e & 1) ? bf16_hi(w[e >> 1]) : bf16_lo(w[e >> 1])) : __uint_as_float(w[e]);
+    };
+    auto count_ge = [&](float x) {
+        int c = 0;
+        for (unsigned q = pass; q; q &= q - 1u) {
+            const uint4 v = ld_vec<ELT, FULL>(sp, __ffs(q) - 1, tid, 0);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < L::EPV; ++e) {
+                const float y = elem(w, e);
+                c += (y >= x && (FULL || y > kNegInf)) ? 1 : 0;
+            }
+        }
+        return warp_sum_i(c);
+    };
+    // v: the largest pattern whose value still has >= 32 elements at or above
+    // it (true at theta, whose count is the warp's candidate count)
+    float v;
+    if constexpr (ELT == 2) {
+        auto val = [](uint32_t k) { return unord32((k << 16) | ((k & 0x8000u) ? 0u : 0xFFFFu)); };
+        uint32_t lo = ord32(theta) >> 16, hi = omx >> 16;
+        while (lo < hi) {
+            const uint32_t mid = lo + ((hi - lo + 1u) >> 1);
+            if (count_ge(val(mid)) >= 32) lo = mid;
+            else hi = mid - 1u;
+        }
+        v = val(lo);
+    } else {
+        uint32_t lo = ord32(theta), hi = omx;
+        while (lo < hi) {
+            const uint32_t d = hi - lo;
+            const uint32_t mid = lo + (d >> 1) + (d & 1u);
+            if (count_ge(unord32(mid)) >= 32) lo = mid;
+            else hi = mid - 1u;
+        }
+        v = unord32(lo);
+    }
+    // every element above v
+    int gt = 0;
+    for (unsigned q = pass; q; q &= q - 1u) {
+        const uint4 x = ld_vec<ELT, FULL>(sp, __ffs(q) - 1, tid, 0);
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int e = 0; e < L::EPV; ++e) {
+            const float y = elem(w, e);
+            gt += (y > v && (FULL || y > kNegInf)) ? 1 : 0;
+        }
+    }
+    int got = 0;
+    int pos = warp_excl_scan_i(gt, lane, &got);  // got < 32
+    for (unsigned q = pass; q; q &= q - 1u) {
+        const int c = __ffs(q) - 1;
+        const uint4 x = ld_vec<ELT, FULL>(sp, c, tid, 0);
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int e = 0; e < L::EPV; ++e) {
+            const float y = elem(w, e);
+            if (y > v && (FULL || y > kNegInf))
+                region[pos++] = make_key(y, (uint32_t)(tbase + (c * kConsumerThreads + tid) * L::EPV + e));
+        }
+    }
+    // elements equal to v in ascending id order: vector by vector, lanes in
+    // order within each
+    for (int c = 0; c < L::NCH && got < 32; ++c) {
+        const bool mine_c = (pass >> c) & 1u;
+        if (!__any_sync(kFull, mine_c)) continue;
+        uint32_t w[4] = {0u, 0u, 0u, 0u};
+        int mine = 0;
+        if (mine_c) {
+            const uint4 x = ld_vec<ELT, FULL>(sp, c, tid, 0);
+            w[0] = x.x; w[1] = x.y; w[2] = x.z; w[3] = x.w;
+#pragma unroll
+            for (int e = 0; e < L::EPV; ++e) {
+                const float y = elem(w, e);
+                mine += (y == v && (FULL || y > kNegInf)) ? 1 : 0;
+            }
+        }
+        int total = 0;
+        int before = warp_excl_scan_i(mine, lane, &total);
+        if (mine_c) {
+#pragma unroll
+            for (int e = 0; e < L::EPV; ++e) {
+                const float y = elem(w, e);
+                if (y == v && (FULL || y > kNegInf)) {
+                    if (got + before < 32)
+                        region[got + before] = make_key(y, (uint32_t)(tbase + (c * kConsumerThreads + tid) * L::EPV + e));
+                    ++before;
+                }
+            }
+        }
+        got += total;
+    }
 }
 
 // Writes the keys of the warp's elements >= theta (full tile) into its region
@@ -1138,8 +1161,10 @@ __device__ __noinline__ bool decide_row(const Params& p, int2* cur);
 // ((max, exp-sum) and the argmax key, atomicMax on the row's best key), then
 // the tile handed to the helper warp through a done slot.  FULL = false for
 // the last, partial tile of a row (its lanes past V already -inf in the
-// stage).  False after a timeout.
-template <int ELT, bool FULL>
+// stage).  SCORE: prompt scoring (the count of logits above the target's is
+// kept too; a separate instance, so generation runs carry none of it).  False
+// after a timeout.
+template <int ELT, bool FULL, bool SCORE>
 __device__ __forceinline__ bool tile_work(const Params& p, Shared& sm, const unsigned char* sp, int nv, int tbase,
                                           const int4& info, int stage, int& ns, uint32_t& nphase,
                                           int& ds, uint32_t& dphase, unsigned long long deadline) {
@@ -1148,7 +1173,7 @@ __device__ __forceinline__ bool tile_work(const Params& p, Shared& sm, const uns
     const bool natural = mode == kModeNatural;
     // prompt scoring: the target's logit, loaded now and used after the passes
     float xt = 0.0f;
-    if (p.targets != nullptr && lane == 0) xt = load_logit<ELT>(p, info.x, __ldg(&p.targets[info.x]));
+    if (SCORE && lane == 0) xt = load_logit<ELT>(p, info.x, __ldg(&p.targets[info.x]));
     // pass 1: maxima (per vector for a full tile)
     uint32_t cm[TileLayout<ELT>::NCH];
     const float m = stage_max<ELT, FULL>(sp, tid, nv, cm);
@@ -1201,7 +1226,11 @@ __device__ __forceinline__ bool tile_work(const Params& p, Shared& sm, const uns
         const float th = m > kNegInf ? theta : kPosInf;
         int cw = capture_candidates<ELT, FULL>(sp, tid, nv, th, tbase, cm, C.cand[warp]);
         if (cw > 32) {
-            warp_top32_exact<ELT>(sp, true, nv, tbase, tid, C.cand[warp]);  // vector layout, -inf past nv
+            // more than 32 at or above theta in this warp (rare): its exact best 32
+            unsigned pass = 0u;
+#pragma unroll
+            for (int c = 0; c < TileLayout<ELT>::NCH; ++c) pass |= (vec_max<ELT>(cm[c]) >= th ? 1u : 0u) << c;
+            warp_top32_select<ELT, FULL>(sp, tid, pass, theta, omx, tbase, C.cand[warp]);
             cw = 32;
         }
         if (lane == 0) {
@@ -1210,7 +1239,7 @@ __device__ __forceinline__ bool tile_work(const Params& p, Shared& sm, const uns
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.ccand[ns]);  // the helper warp takes it from here
-        if (p.targets != nullptr) {
+        if constexpr (SCORE) {
             // prompt scoring: this warp's lanes whose logit is above the target's,
             // and the smallest of those logits (the rank is finished in the record
             // kernel, once lse is known); vectors whose maximum is not above it
@@ -1280,7 +1309,7 @@ __device__ __forceinline__ bool tile_work(const Params& p, Shared& sm, const uns
 // its partial results itself: the warps never wait for one another, except on
 // natural-alternative tiles, where the 8 warp thresholds and candidates are
 // exchanged through a candidate slot (bounded mbarrier waits).
-template <int ELT>
+template <int ELT, bool SCORE>
 __device__ void compute_loop(const Params& p, Shared& sm, unsigned char* stages, unsigned long long t0) {
     constexpr int S = StageCfg<ELT>::kStages;
     constexpr int kTE = tile_elems<ELT>();
@@ -1305,10 +1334,10 @@ __device__ void compute_loop(const Params& p, Shared& sm, unsigned char* stages,
         trace(p, kTrTileStart, info.x, tile, tid == 0);
         bool ok;
         if (__builtin_expect(nv == kTE, 1)) {
-            ok = tile_work<ELT, true>(p, sm, sp, nv, tbase, info, stage, ns, nphase, ds, dphase, deadline);
+            ok = tile_work<ELT, true, SCORE>(p, sm, sp, nv, tbase, info, stage, ns, nphase, ds, dphase, deadline);
         } else {
             fill_partial<ELT>(stages + (size_t)stage * kTileBytes, tid, nv);
-            ok = tile_work<ELT, false>(p, sm, sp, nv, tbase, info, stage, ns, nphase, ds, dphase, deadline);
+            ok = tile_work<ELT, false, SCORE>(p, sm, sp, nv, tbase, info, stage, ns, nphase, ds, dphase, deadline);
         }
         if (!ok) return;
         trace(p, kTrTileEnd, info.x, tile, tid == 0);
@@ -1457,7 +1486,7 @@ __device__ __noinline__ void helper_loop(const Params& p, Shared& sm, unsigned l
     }
 }
 
-template <int ELT>
+template <int ELT, bool SCORE>
 __global__ void __launch_bounds__(kThreads, StageCfg<ELT>::kMinBlocks) lp_stream_kernel(Params p) {
     constexpr int S = StageCfg<ELT>::kStages;
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -1501,7 +1530,7 @@ __global__ void __launch_bounds__(kThreads, StageCfg<ELT>::kMinBlocks) lp_stream
         helper_loop<ELT>(p, sm, t0 + p.timeout_ns);
         return;
     }
-    compute_loop<ELT>(p, sm, stages, t0);
+    compute_loop<ELT, SCORE>(p, sm, stages, t0);
     if ((tid & 31) == 0) {
         __threadfence_block();  // this warp's slot arrivals come first
         atomicAdd(&sm.sel_exit, 1);
@@ -1620,8 +1649,9 @@ __device__ __forceinline__ void ms_merge(float& m, float& s, float m2, float s2)
 // Record of a requested, emitted row, built by one CTA of 256 threads: lse from
 // the tile partials, the chosen pair, then the explicit-id gather or the
 // natural alternatives (each warp merges every 8th tile list, warp 0 merges
-// the 8).  Every global load is issued before the first barrier.
-template <int ELT>
+// the 8).  Every global load is issued before the first barrier.  SCORE: the
+// prompt-scoring record (rank, 43 words) instead of the 258-word one.
+template <int ELT, bool SCORE>
 __device__ __noinline__ void record_block(const Params& p, RecShared& sm, int row, int entry, int chosen, int dy,
                                           int kc) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -1630,7 +1660,7 @@ __device__ __noinline__ void record_block(const Params& p, RecShared& sm, int ro
     const int T = p.T;
     const long long base = (long long)row * T;
     const bool natural = !ids && mode == kModeNatural && kc > 0;
-    const bool score = p.targets != nullptr;
+    constexpr bool score = SCORE;
     for (int w = tid; w < kRecordWords; w += kConsumerThreads)
         sm.rec[w] = (w >= 2 && (w & 1) == 0) ? -1 : (int)kUnusedBits;
     if (tid == 0) sm.corr = 0;
@@ -1690,7 +1720,7 @@ __device__ __noinline__ void record_block(const Params& p, RecShared& sm, int ro
                                                       : (int)kUnusedBits;
             if (p.lse_out) p.lse_out[row] = lse;
         }
-        if (score) {
+        if constexpr (SCORE) {
             const float lp = logprob(sm.xchosen, lse);
             sm.xlim = lp == lp ? score_limit(sm.xchosen, lse, lp, lane) : sm.xchosen;  // NaN: nothing is above
         }
@@ -1714,7 +1744,7 @@ __device__ __noinline__ void record_block(const Params& p, RecShared& sm, int ro
         sm.rec[2 + 2 * tid] = id;
         sm.rec[3 + 2 * tid] = bits;
     }
-    if (score) {
+    if constexpr (SCORE) {
         // logits in (xt, X]: above the target's but reported equal to it.  Only
         // a tile whose smallest logit above the target's is <= X holds any.
         const float xt = sm.xchosen, X = sm.xlim;
@@ -1735,7 +1765,7 @@ __device__ __noinline__ void record_block(const Params& p, RecShared& sm, int ro
         if (lane == 0 && corr != 0) atomicAdd(&sm.corr, corr);
     }
     cbar();
-    if (score) {
+    if constexpr (SCORE) {
         // record: target, its lp, rank, then the 20 alternatives
         int above_all = 0;
 #pragma unroll
@@ -1752,14 +1782,14 @@ __device__ __noinline__ void record_block(const Params& p, RecShared& sm, int ro
 
 // Builds the records of the rows the stream kernel flagged (launched after it
 // with programmatic dependent launch: it waits for the stream grid to finish).
-template <int ELT>
+template <int ELT, bool SCORE>
 __global__ void __launch_bounds__(kConsumerThreads) lp_record_kernel(Params p) {
     __shared__ RecShared rs;
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (vload(&p.ctrl->abort) != 0u) return;
     for (int row = blockIdx.x; row < p.rows; row += gridDim.x) {
         const int4 t = __ldcg(&p.rec_tasks[row]);  // (chosen, queue entry, descriptor word, count); 0 word: none
-        if (t.z != 0) record_block<ELT>(p, rs, row, t.y, t.x, t.z, t.w);
+        if (t.z != 0) record_block<ELT, SCORE>(p, rs, row, t.y, t.x, t.z, t.w);
     }
 }
 
@@ -1776,17 +1806,22 @@ cudaError_t query_launch_cfg(int dtype, LaunchCfg* cfg) {
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
+    // both instances (generation, prompt scoring) have the same launch shape
     if (dtype == 1) {
         const int smem = stream_smem_bytes<2>();
-        e = cudaFuncSetAttribute(lp_stream_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        e = cudaFuncSetAttribute(lp_stream_kernel<2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(lp_stream_kernel<2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, lp_stream_kernel<2>, kThreads, smem);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, lp_stream_kernel<2, false>, kThreads, smem);
         cfg->smem_bytes = smem;
     } else {
         const int smem = stream_smem_bytes<4>();
-        e = cudaFuncSetAttribute(lp_stream_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        e = cudaFuncSetAttribute(lp_stream_kernel<4, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(lp_stream_kernel<4, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, lp_stream_kernel<4>, kThreads, smem);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, lp_stream_kernel<4, false>, kThreads, smem);
         cfg->smem_bytes = smem;
     }
     if (e != cudaSuccess) return e;
@@ -1814,7 +1849,12 @@ cudaError_t launch_epilogue(const Params& p_in, int dtype, const LaunchCfg& cfg,
     lc.stream = stream;
     lc.attrs = attr;
     lc.numAttrs = 1;
-    e = dtype == 1 ? cudaLaunchKernelEx(&lc, lp_stream_kernel<2>, p) : cudaLaunchKernelEx(&lc, lp_stream_kernel<4>, p);
+    const bool score = p.targets != nullptr;
+    if (dtype == 1) {
+        e = score ? cudaLaunchKernelEx(&lc, lp_stream_kernel<2, true>, p) : cudaLaunchKernelEx(&lc, lp_stream_kernel<2, false>, p);
+    } else {
+        e = score ? cudaLaunchKernelEx(&lc, lp_stream_kernel<4, true>, p) : cudaLaunchKernelEx(&lc, lp_stream_kernel<4, false>, p);
+    }
     if (e != cudaSuccess) return e;
     // records: one CTA per row (rows without a record return at once)
     int rgrid = p.rows;
@@ -1826,7 +1866,10 @@ cudaError_t launch_epilogue(const Params& p_in, int dtype, const LaunchCfg& cfg,
     rc.stream = stream;
     rc.attrs = attr;
     rc.numAttrs = 1;
-    return dtype == 1 ? cudaLaunchKernelEx(&rc, lp_record_kernel<2>, p) : cudaLaunchKernelEx(&rc, lp_record_kernel<4>, p);
+    if (dtype == 1) {
+        return score ? cudaLaunchKernelEx(&rc, lp_record_kernel<2, true>, p) : cudaLaunchKernelEx(&rc, lp_record_kernel<2, false>, p);
+    }
+    return score ? cudaLaunchKernelEx(&rc, lp_record_kernel<4, true>, p) : cudaLaunchKernelEx(&rc, lp_record_kernel<4, false>, p);
 }
 
 }  // namespace lp

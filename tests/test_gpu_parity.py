@@ -411,3 +411,37 @@ def test_score_no_rows():
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     plan.close()
+
+
+def _warp_share_ids(tile, V, dtype, warp):
+    """Vocabulary ids of one compute warp's share of a 32 KiB tile (thread i reads
+    the 16-byte vectors c*256 + i)."""
+    epv = 8 if dtype == "bf16" else 4
+    te = PT.lpe_tile_elems(dtype)
+    tid = np.arange(32 * warp, 32 * warp + 32)
+    c = np.arange(te // epv // 256)
+    e = np.arange(epv)
+    ids = ((c[:, None, None] * 256 + tid[None, :, None]) * epv + e[None, None, :]).reshape(-1)
+    ids = tile * te + ids
+    return ids[ids < V]
+
+
+@pytest.mark.parametrize("dtype,ragged", [("bf16", False), ("bf16", True), ("f32", False), ("f32", True)])
+def test_one_low_warp_forces_exact_select(dtype, ragged):
+    # one warp's share of every tile far below the rest: the tile threshold (the
+    # smallest warp's 4th-largest thread maximum) drops, so every other warp has
+    # far more than 32 candidates and takes the exact per-warp selection
+    te = PT.lpe_tile_elems(dtype)
+    V = 3 * te + (777 if ragged else 0)
+    rng = np.random.default_rng(41)
+    x = rng.standard_normal((2, V)).astype(np.float32)
+    for t in range((V + te - 1) // te):
+        ids = _warp_share_ids(t, V, dtype, 7)
+        x[:, ids] = np.float32(-10.0) + rng.standard_normal((2, ids.size)).astype(np.float32) * np.float32(0.01)
+    x[1] = np.round(x[1] * 2) / 2  # heavy exact ties as well
+    epv = 8 if dtype == "bf16" else 4
+    Vp = (V + epv - 1) // epv * epv + (epv if ragged else 0)  # rows 16-byte aligned, plus one pad vector
+    x0 = W.bf16_to_f32(W.bf16_bits(x[0])) if dtype == "bf16" else x[0]
+    w = _one_group(x, V, dtype=dtype, Vp=Vp, k=1, drafts=[int(np.argmax(x0)), -1])
+    gpu, _, _ = _check(w)
+    assert gpu["accepted"].tolist() == [1]  # both rows carry records
