@@ -456,7 +456,7 @@ def main():
                      "kernel": "lp_stream_kernel (timed with lp_prepare_kernel and lp_record_kernel: one lp_run)",
                      "algorithmic_bytes_per_launch": ab["total"], "peak_source": peak_kind},
         "e2e": e2e,
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": 3 * args.steps,  # lp_prepare_kernel, lp_stream_kernel, lp_record_kernel per lp_run
         "clocks": clocks,
         "status": status,
         "median_launch_us": statistics.median(durs) * 1e6,
