@@ -74,6 +74,8 @@ class _IO(ctypes.Structure):
         ("lse_out", ctypes.c_void_p),
         ("status", ctypes.c_void_p),
         ("rows_read", ctypes.c_void_p),
+        ("eos_tokens", ctypes.c_void_p),
+        ("budgets", ctypes.c_void_p),
     ]
 
 
@@ -202,13 +204,15 @@ def score(*args, **kw):
 
 def _epilogue(L, logits: np.ndarray, V: int, group_indptr, draft_tokens, sampled_tokens, requested,
              top_k, token_ids, id_counts, *, k_max: int = 15, k_alt_max: int = 20,
-             max_ids: int = 128, records=None, threads: int = 1):
+             max_ids: int = 128, records=None, threads: int = 1, eos_tokens=None, budgets=None):
     """Runs the whole epilogue on host arrays.
 
     ``logits`` is float32 [rows, Vp] (BF16 data widened exactly).  ``records``
     may be passed pre-filled (e.g. with a sentinel) to check that rows not
     emitted are left untouched.  Returns a dict with records, accepted,
     emitted_tokens, lse (NaN where not computed), status and rows_read.
+    ``eos_tokens`` and ``budgets`` ([groups] each, optional) clip the emitted
+    prefix.
     """
     logits = np.ascontiguousarray(logits, dtype=np.float32)
     rows, Vp = logits.shape
@@ -228,10 +232,13 @@ def _epilogue(L, logits: np.ndarray, V: int, group_indptr, draft_tokens, sampled
     lse_out = np.full(max(rows, 1), np.nan, np.float32)
     status = np.zeros(1, np.uint32)
     rows_read = np.zeros(1, np.int64)
+    eo = None if eos_tokens is None else np.ascontiguousarray(eos_tokens, np.int32)
+    bu = None if budgets is None else np.ascontiguousarray(budgets, np.int32)
     io = _IO(
         _ptr(logits), rows, int(V), Vp, G, _ptr(ip), _ptr(dr), _ptr(sa), _ptr(rq), _ptr(tk),
         _ptr(ti), _ptr(ic), int(k_max), int(k_alt_max), int(max_ids), _ptr(records), _ptr(accepted),
         _ptr(emitted), _ptr(lse_out), _ptr(status), _ptr(rows_read),
+        None if eo is None else _ptr(eo), None if bu is None else _ptr(bu),
     )
     rc = L.orc_epilogue(ctypes.byref(io), int(threads))
     if rc != 0:

@@ -124,6 +124,20 @@ void run_group(Shared& sh, int32_t g) {
         }
     }
 
+    // Commit clipping ("mtp-design.md", a speculative round, step 4): the
+    // emitted prefix of length t (1 <= t <= a+1) ends at the first emitted EOS
+    // token (which is emitted) and holds at most `budget` tokens.  A request
+    // already at its limit (budget <= 0) takes no step: nothing is emitted,
+    // read or written, and accepted is -1.
+    const int32_t eos = io.eos_tokens ? io.eos_tokens[g] : -1;
+    const int32_t budget = io.budgets ? io.budgets[g] : INT32_MAX;
+    if (budget <= 0) {
+        io.accepted[g] = -1;
+        for (int32_t j = 0; j <= k; ++j) io.emitted_tokens[(int64_t)r0 + j] = -1;
+        sh.status.fetch_or(st);
+        return;
+    }
+
     // A k=0 request with a caller-sampled token and no flag needs no logits.
     const bool must_read = flagged || k >= 1 || sampled < 0;
     if (!must_read) {
@@ -181,9 +195,13 @@ void run_group(Shared& sh, int32_t g) {
         }
 
         // Row j < k accepts its draft when the draft equals the row's argmax;
-        // the first mismatch (or the bonus row j == k) ends the group.
+        // the first mismatch (or the bonus row j == k) ends the group.  The
+        // clip ends it too, at an emitted EOS or once `budget` tokens are
+        // emitted, so t = min(a + 1, budget, position of the first EOS + 1)
+        // and no row past the clipped prefix is read.
         const bool accept = j < k && io.draft_tokens[row] == amax;
-        if (!accept) {
+        const bool clipped = (eos >= 0 && chosen == eos) || j + 1 >= budget;
+        if (!accept || clipped) {
             io.accepted[g] = j;
             for (int32_t jj = j + 1; jj <= k; ++jj) io.emitted_tokens[(int64_t)r0 + jj] = -1;
             break;

@@ -91,6 +91,10 @@ typedef struct {
     float* lse_out;                /* [rows] or NULL; written for rows whose lse is computed */
     uint32_t* status;              /* out: status bits */
     int64_t* rows_read;            /* out (optional): logit rows the path had to read */
+    /* Commit clipping ("mtp-design.md", a speculative round, step 4 and the
+     * paragraph after it), both optional (NULL = none): */
+    const int32_t* eos_tokens;     /* [groups]; the emitted prefix ends at this token (< 0 = none) */
+    const int32_t* budgets;        /* [groups]; at most this many tokens emitted; <= 0 = at the limit */
 } orc_io;
 
 /* Runs the epilogue; groups are split over `threads` host threads (<=1: one).

@@ -353,7 +353,71 @@ def pin_score_ties_and_invalid(orc):
     assert r["status"] == 0x2  # the target 7 >= V; -1 is the ordinary invalid marker
 
 
+# ----------------------------------------------------------------------------- commit clipping
+#
+# "mtp-design.md", a speculative round, step 4 and the paragraph after it: the
+# emitted prefix of t tokens (1 <= t <= a+1) is clipped at an emitted EOS token
+# (which stays emitted) and at the request's output budget; a request already at
+# its limit takes no step.  The logprob writer reads only the emitted prefix.
+
+CLIP_SENTINEL = 0x5EED5EED
+
+
+def _clip_block():
+    # four groups of k = 3 over a 40-lane vocabulary; every row has one planted
+    # maximum (5.0), the rest in [0, 1)
+    rng = np.random.default_rng(61)
+    V = 40
+    amax = [[7, 11, 13, 17], [7, 11, 13, 17], [21, 22, 23, 24], [30, 31, 32, 33]]
+    x = rng.uniform(0.0, 1.0, (16, V)).astype(np.float32)
+    for g in range(4):
+        for j in range(4):
+            x[4 * g + j, amax[g][j]] = 5.0
+    drafts = np.full(16, -1, np.int32)
+    drafts[0:3] = [7, 11, 13]       # group 0: every draft matches
+    drafts[4:7] = [7, 12, 13]       # group 1: draft 1 misses (row 1's argmax is 11)
+    drafts[8:11] = [21, 22, 23]     # group 2: every draft matches
+    drafts[12:15] = [30, 31, 32]    # group 3: every draft matches
+    return W.custom(x, V, [4, 4, 4, 4], drafts=drafts, top_k=[3, 3, 3, 3], k_max=3)
+
+
+def pin_commit_clipping(orc):
+    w = _clip_block()
+    def run(eos, budget):
+        rec = np.full((16, 258), CLIP_SENTINEL, np.int32)
+        return orc.epilogue(w.logits_f32(), w.V, **w.inputs(), k_max=3, records=rec,
+                            eos_tokens=None if eos is None else np.array(eos, np.int32),
+                            budgets=None if budget is None else np.array(budget, np.int32))
+    base = run(None, None)
+    assert base["accepted"].tolist() == [3, 1, 3, 3] and base["rows_read"] == 4 + 2 + 4 + 4
+    # budgets: at most that many tokens; 0 = at the limit (no step at all)
+    r = run(None, [2, 1, 0, 9])
+    assert r["accepted"].tolist() == [1, 0, -1, 3]
+    assert r["emitted_tokens"].tolist() == [7, 11, -1, -1, 7, -1, -1, -1, -1, -1, -1, -1, 30, 31, 32, 33]
+    assert r["rows_read"] == 2 + 1 + 0 + 4
+    written = [not (row == CLIP_SENTINEL).all() for row in r["records"]]
+    assert written == [True, True, False, False, True, False, False, False,
+                       False, False, False, False, True, True, True, True]
+    assert np.isnan(r["lse"][8:12]).all()
+    # EOS: the emitted prefix ends at (and keeps) the first emitted EOS token,
+    # whether it is an accepted draft, the correction or the bonus token
+    r = run([11, 11, 24, 99], None)
+    assert r["accepted"].tolist() == [1, 1, 3, 3]
+    assert r["emitted_tokens"].tolist() == [7, 11, -1, -1, 7, 11, -1, -1, 21, 22, 23, 24, 30, 31, 32, 33]
+    r = run([7, 12, 22, -1], [3, 9, 9, 2])
+    # group 1: 12 is the rejected draft, never emitted; group 3: no EOS, budget 2
+    assert r["accepted"].tolist() == [0, 1, 1, 1]
+    assert r["emitted_tokens"].tolist() == [7, -1, -1, -1, 7, 11, -1, -1, 21, 22, -1, -1, 30, 31, -1, -1]
+    assert r["rows_read"] == 1 + 2 + 2 + 2
+    # k = 0 requests: a caller-sampled token is emitted as is (one token), not read
+    x = np.zeros((2, 8), np.float32)
+    w0 = W.custom(x, 8, [1, 1], sampled=[5, 5], requested=[0, 0], k_max=0)
+    r0 = orc.epilogue(w0.logits_f32(), 8, **w0.inputs(), k_max=0, eos_tokens=np.array([5, 5], np.int32),
+                      budgets=np.array([1, 0], np.int32))
+    assert r0["accepted"].tolist() == [0, -1] and r0["emitted_tokens"].tolist() == [5, -1] and r0["rows_read"] == 0
+
+
 ALL_PINS = [pin_golden_rows, pin_golden_groups, pin_brute_force, pin_lse_independent,
             pin_two_value_closed_form, pin_sum_exp_invariant, pin_pad_exclusion, pin_id_passthrough,
             pin_acceptance_prefixes, pin_tiny_workload, pin_status_bits, pin_score_rank_independent,
-            pin_score_collapse_closed_form, pin_score_ties_and_invalid]
+            pin_score_collapse_closed_form, pin_score_ties_and_invalid, pin_commit_clipping]

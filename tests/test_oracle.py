@@ -61,6 +61,12 @@ MUTANTS = {
     "rank_zero_based": ("    return 1 + greater;", "    return greater;"),
     "invalid_rank_one": ("        rec[2] = 0;", "        rec[2] = 1;"),
     "invalid_alt_id_zero": ("            rec[3 + 2 * i] = -1;", "            rec[3 + 2 * i] = 0;"),
+    "budget_off_by_one": ("|| j + 1 >= budget;", "|| j >= budget;"),
+    "eos_ignored": ("const bool clipped = (eos >= 0 && chosen == eos) || j + 1 >= budget;",
+                    "const bool clipped = j + 1 >= budget;"),
+    "at_limit_still_steps": ("    if (budget <= 0) {", "    if (budget < 0) {"),
+    "eos_not_emitted": ("        io.emitted_tokens[row] = chosen;\n",
+                        "        io.emitted_tokens[row] = (eos >= 0 && chosen == eos) ? -1 : chosen;\n"),
 }
 
 
