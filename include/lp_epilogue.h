@@ -170,6 +170,24 @@ size_t lp_plan_scratch_bytes(const lp_plan_desc* desc);
  * device (status bits).  Errors: LP_EINVAL, LP_ESHAPE, LP_EALIGN. */
 int lp_bind(lp_plan_t plan, const lp_io* io);
 
+/* ---- Commit clipping ("mtp-design.md", a speculative round, step 4 and the
+ * paragraph after it)
+ *
+ * Attaches optional per-group clipping inputs to the bound buffers, for the
+ * following lp_run calls (lp_bind clears them; lp_run_host, lp_run_static and
+ * lp_score never clip).  Device pointers, or NULL for none:
+ *   eos_tokens  int32 [groups]  the emitted prefix ends at the first emitted
+ *                               token equal to it, which is kept (< 0 = none)
+ *   budgets     int32 [groups]  at most this many tokens are emitted; <= 0 =
+ *                               the request is at its limit and takes no step
+ * With a accepted drafts the unclipped prefix holds a+1 tokens; the clipped
+ * one holds t = min(a+1, budget, position of the first EOS + 1).  accepted[g]
+ * then reports t - 1 and emitted_tokens holds -1 past the t tokens, so
+ * records are written, and rows read, for the t emitted rows only.  A group
+ * at its limit reports accepted -1, emits nothing and reads nothing.
+ * Errors: LP_EINVAL (no plan), LP_ESTATE (nothing bound), LP_EALIGN. */
+int lp_bind_clip(lp_plan_t plan, const int32_t* eos_tokens, const int32_t* budgets);
+
 /* Enqueues the epilogue over the bound buffers on `stream` (a cudaStream_t;
  * NULL = legacy default stream).  Returns after enqueueing.  Errors:
  * LP_ESTATE (nothing bound), LP_ECUDA (launch failed). */

@@ -41,7 +41,7 @@ STATIC_SCRATCH_BYTES = 4 << 20  # fixed device scratch of run_static
 # Every symbol include/lp_epilogue.h declares.
 EXPORTS = ("lp_plan_create", "lp_plan_destroy", "lp_plan_scratch_bytes", "lp_bind", "lp_run", "lp_run_host",
            "lp_run_host_bytes", "lp_debug_tiles_read", "lp_debug_poison_scratch", "lp_debug_trace",
-           "lp_plan_tiles_per_row", "lp_run_static", "lp_score",
+           "lp_plan_tiles_per_row", "lp_run_static", "lp_score", "lp_bind_clip",
            "lp_strerror", "lp_last_cuda_error")
 
 
@@ -126,6 +126,7 @@ def lib() -> ctypes.CDLL:
         L.lp_debug_trace.argtypes = [P, P, P, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]
         L.lp_run_static.argtypes = [ctypes.POINTER(PlanDesc), ctypes.POINTER(IO), P]
         L.lp_score.argtypes = [P, ctypes.POINTER(ScoreIO), P]
+        L.lp_bind_clip.argtypes = [P, P, P]
         L.lp_strerror.argtypes = [ctypes.c_int]
         L.lp_strerror.restype = ctypes.c_char_p
         L.lp_last_cuda_error.argtypes = []
@@ -235,6 +236,23 @@ class Plan:
         _check(lib().lp_bind(self._h, ctypes.byref(io)), "lp_bind")
         self._keep = t
         self.rows, self.groups = rows, groups
+
+    def bind_clip(self, *, eos_tokens=None, budgets=None) -> None:
+        """Attaches per-group commit clipping (int32 CUDA tensors of [groups], or
+        None) to the bound buffers for the following runs: the emitted prefix
+        ends at an emitted EOS token (kept) and holds at most ``budgets[g]``
+        tokens (<= 0: the group takes no step).  ``bind`` clears it."""
+        import torch
+        for name, x in (("eos_tokens", eos_tokens), ("budgets", budgets)):
+            if x is None:
+                continue
+            if not isinstance(x, torch.Tensor) or not x.is_cuda or x.device.index != self.device:
+                raise ValueError(f"{name}: expected a CUDA tensor on device {self.device}")
+            if x.dtype != torch.int32 or not x.is_contiguous() or x.numel() < self.groups:
+                raise ValueError(f"{name}: expected contiguous int32 [groups]")
+        ptr = lambda x: None if x is None else x.data_ptr()  # noqa: E731
+        _check(lib().lp_bind_clip(self._h, ptr(eos_tokens), ptr(budgets)), "lp_bind_clip")
+        self._keep_clip = (eos_tokens, budgets)
 
     def run(self, stream=None) -> None:
         """Enqueues the epilogue on ``stream`` (default: torch's current stream)."""

@@ -127,6 +127,8 @@ struct Params {
     int read_ahead;       // 0: rows past a group's emitted prefix are never read
     // prompt scoring (targets != nullptr): group g is row g alone, k = 0, 20
     // natural alternatives, chosen token targets[g]; records go to score_records
+    const int* eos;       // [G] or null: commit clipping at an emitted EOS token
+    const int* budget;    // [G] or null: commit clipping at the output budget
     const int* targets;
     int* score_records;   // [rows, 43]
     int done_last;        // done[row] before the increment that completes a row: T - 1, plus

@@ -578,9 +578,19 @@ __global__ void __launch_bounds__(1024) lp_prepare_kernel(Params p) {
         if (g < G) {
             const GroupIn x = g0 == 0 ? in0 : load_group(p, g);
             const int r0 = x.r0;
-            const int k = x.r1 - r0 - 1;
+            int k = x.r1 - r0 - 1;
             const int req = x.req != 0;
-            const int samp = x.samp;
+            int samp = x.samp;
+            // commit clipping at the output budget: at most `budget` tokens, so
+            // rows past budget - 1 are never read; <= 0: the request is at its
+            // limit and takes no step
+            const int budget = p.budget != nullptr ? __ldg(&p.budget[g]) : 0x7FFFFFFF;
+            const bool at_limit = budget <= 0;
+            if (!at_limit && k > budget - 1) {
+                for (int jj = budget; jj <= k; ++jj) p.emitted[r0 + jj] = -1;
+                k = budget - 1;
+                samp = -1;  // a verify group's target row stays greedy when clipped to it
+            }
             int cnt = x.cnt;
             int K = x.K;
             int mode = kModeArgmax, kc = 0, ids = 0;
@@ -603,7 +613,11 @@ __global__ void __launch_bounds__(1024) lp_prepare_kernel(Params p) {
                 }
             }
             need = req || k >= 1 || samp < 0;
-            if (p.targets != nullptr) {
+            if (at_limit) {
+                need = 0;
+                for (int jj = 0; jj <= k; ++jj) p.emitted[r0 + jj] = -1;
+                p.accepted[g] = -1;
+            } else if (p.targets != nullptr) {
                 // prompt scoring: a row without a valid target is not read; its
                 // record is the invalid one (id -1, NaN, rank 0, ids -1)
                 need = samp >= 0 && samp < p.V;
@@ -1368,10 +1382,12 @@ __device__ __noinline__ bool decide_row(const Params& p, int2* cur) {
     const int4 d = __ldcg(&p.gdesc[g]);
     const unsigned long long bk = atomicMax(&p.row_best[row], 0ull);  // read at its point of coherence
     const int draft = p.drafts != nullptr ? __ldg(&p.drafts[row]) : -1;  // none when scoring
+    const int eos = p.eos != nullptr ? __ldg(&p.eos[g]) : -1;
     const int r0 = d.x, k = d.y & 0xFF, req = (d.y >> 13) & 1, samp = d.w, mode = (d.y >> 8) & 3;
     const uint32_t amax = key_id(bk);
     const int chosen = (k == 0 && samp >= 0) ? samp : (int)amax;
-    const bool accept = (j < k) && (draft == (int)amax);
+    // commit clipping: an emitted EOS token ends the group (it stays emitted)
+    const bool accept = (j < k) && (draft == (int)amax) && !(eos >= 0 && chosen == eos);
     int next_done = 0;
     if (accept) {
         // independent round trips, issued together

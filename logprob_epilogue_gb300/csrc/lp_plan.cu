@@ -34,6 +34,8 @@ struct lp_plan_s {
     size_t part_ms_bytes, part_keys_bytes;
     bool bound;
     lp_io io;
+    const int32_t* clip_eos;     // lp_bind_clip inputs for lp_run (null: none)
+    const int32_t* clip_budget;
     // optional host staging (LP_PLAN_HOST_STAGING)
     unsigned char* staging;
     size_t staging_bytes;
@@ -343,6 +345,17 @@ int lp_bind(lp_plan_t plan, const lp_io* io) {
     if (rc != LP_OK) return rc;
     plan->io = *io;
     plan->bound = true;
+    plan->clip_eos = nullptr;
+    plan->clip_budget = nullptr;
+    return LP_OK;
+}
+
+int lp_bind_clip(lp_plan_t plan, const int32_t* eos_tokens, const int32_t* budgets) {
+    if (!plan) return LP_EINVAL;
+    if (!plan->bound) return LP_ESTATE;
+    if ((eos_tokens && !aligned(eos_tokens, 4)) || (budgets && !aligned(budgets, 4))) return LP_EALIGN;
+    plan->clip_eos = eos_tokens;
+    plan->clip_budget = budgets;
     return LP_OK;
 }
 
@@ -351,7 +364,9 @@ int lp_run(lp_plan_t plan, void* stream) {
     if (!plan->bound) return LP_ESTATE;
     DeviceGuard guard(plan->d.device);
     if (!guard.ok) return cuda_fail(cudaGetLastError());
-    const lp::Params p = make_params(plan, plan->io);
+    lp::Params p = make_params(plan, plan->io);
+    p.eos = plan->clip_eos;
+    p.budget = plan->clip_budget;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const cudaError_t e = lp::launch_epilogue(p, plan->d.dtype, plan->cfg, s);
     if (e != cudaSuccess) return cuda_fail(e);

@@ -56,8 +56,9 @@ def make_plan(w: W.Workload, **kw):
     return lpe.Plan(**args)
 
 
-def run_gpu(w: W.Workload, plan=None, dev_inputs=None, poison=False, runs=1):
-    """Runs the CUDA path; returns numpy outputs and the plan."""
+def run_gpu(w: W.Workload, plan=None, dev_inputs=None, poison=False, runs=1, eos_tokens=None, budgets=None):
+    """Runs the CUDA path; returns numpy outputs and the plan.  ``eos_tokens`` /
+    ``budgets`` ([groups] int32, optional) attach commit clipping."""
     import torch
     if plan is None:
         plan = make_plan(w)
@@ -72,6 +73,10 @@ def run_gpu(w: W.Workload, plan=None, dev_inputs=None, poison=False, runs=1):
         status=torch.full((1,), -1, dtype=torch.int32, device=dev),
     )
     plan.bind(**d, **out)
+    if eos_tokens is not None or budgets is not None:
+        ti = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a, np.int32)).to(dev)  # noqa: E731
+        clip = (ti(eos_tokens), ti(budgets))
+        plan.bind_clip(eos_tokens=clip[0], budgets=clip[1])
     for _ in range(runs):
         if poison:
             plan.poison_scratch()
@@ -87,9 +92,10 @@ def run_gpu(w: W.Workload, plan=None, dev_inputs=None, poison=False, runs=1):
     return res, plan
 
 
-def run_oracle(w: W.Workload, threads: int = 8):
+def run_oracle(w: W.Workload, threads: int = 8, eos_tokens=None, budgets=None):
     sentinel = np.full((w.rows, 258), SENTINEL, np.int32)
-    return oracle.epilogue(w.logits_f32(), w.V, **w.inputs(), k_max=w.k_max, records=sentinel, threads=threads)
+    return oracle.epilogue(w.logits_f32(), w.V, **w.inputs(), k_max=w.k_max, records=sentinel, threads=threads,
+                           eos_tokens=eos_tokens, budgets=budgets)
 
 
 def _f(bits) -> np.float32:
