@@ -266,8 +266,9 @@ class Flusher:
             self.last = self.clean.sum()
 
 
-def bench_device(w: W.Workload, steps: int, warmup: int, device: int, staging: bool = True):
-    """Times lp_run on device-resident inputs; returns per-step durations (s) and outputs."""
+def bench_device(w: W.Workload, steps: int, warmup: int, device: int, staging: bool = True, clip=None):
+    """Times lp_run on device-resident inputs; returns per-step durations (s) and outputs.
+    ``clip``: optional (eos_tokens, budgets) commit-clipping inputs."""
     import torch
     import logprob_epilogue_gb300 as lpe
     sys.path.insert(0, os.path.join(ROOT, "tests"))
@@ -288,6 +289,9 @@ def bench_device(w: W.Workload, steps: int, warmup: int, device: int, staging: b
                 lse_out=torch.zeros(w.rows, dtype=torch.float32, device=dev),
                 status=torch.zeros(1, dtype=torch.int32, device=dev))
     plan.bind(**ins, **outs)
+    if clip is not None:
+        ins["eos_tokens"], ins["budgets"] = ti(clip[0]), ti(clip[1])
+        plan.bind_clip(eos_tokens=ins["eos_tokens"], budgets=ins["budgets"])
     flush = Flusher(dev)
     stream = torch.cuda.current_stream(dev)
     for _ in range(warmup):
@@ -470,11 +474,14 @@ def main():
     del ins, outs
     if rank == 0 and not args.no_per_workload:
         per = {}
-        for name in DESCRIPTIONS:
-            if name == args.config:
-                continue
-            wn = W.make(name)
-            p2, i2, o2, fl2, st2, en2, s2 = bench_device(wn, 200, 5, local, staging=False)
+        # the other workloads, and the spec block with commit clipping (seeded
+        # EOS tokens and output budgets, every case of the rule)
+        cases = [(name, name, None) for name in DESCRIPTIONS if name != args.config]
+        cases.append(("spec_clipped", "spec", 5))
+        for name, base, clip_seed in cases:
+            wn = W.make(base)
+            clip = None if clip_seed is None else W.commit_clip(wn, clip_seed)
+            p2, i2, o2, fl2, st2, en2, s2 = bench_device(wn, 200, 5, local, staging=False, clip=clip)
             for i in range(200):
                 fl2(i)
                 st2[i].record(s2)

@@ -449,42 +449,11 @@ def test_one_low_warp_forces_exact_select(dtype, ragged):
 
 # ----------------------------------------------------------------- commit clipping
 
-def _clip_inputs(w, seed):
-    """Per-group EOS tokens and budgets, cycling through every case: at the limit
-    (budget 0); EOS on a draft; an EOS id drawn at random with a budget of one
-    token; a budget inside the group; EOS on a planted row maximum (an accepted
-    draft, or the correction or bonus token)."""
-    rng = np.random.default_rng(seed)
-    gi = np.asarray(w.group_indptr)
-    G = w.groups
-    eos = np.full(G, -1, np.int32)
-    budgets = np.empty(G, np.int32)
-    for g in range(G):
-        r0, r1 = int(gi[g]), int(gi[g + 1])
-        k = r1 - r0 - 1
-        kind = g % 5
-        budgets[g] = k + 2
-        if kind == 0:
-            budgets[g] = 0
-        elif kind == 1 and k >= 1:
-            eos[g] = int(w.draft_tokens[r0 + int(rng.integers(0, k))])
-        elif kind == 2:
-            eos[g] = int(rng.integers(0, w.V))
-            budgets[g] = 1
-        elif kind == 3:
-            budgets[g] = int(rng.integers(1, k + 2))
-        elif kind == 4:
-            planted = [int(v) for v in w.planted_argmax[r0:r1] if v >= 0]
-            if planted:
-                eos[g] = planted[int(rng.integers(0, len(planted)))]
-    return eos, budgets
-
-
 @pytest.mark.parametrize("read_ahead", [False, True], ids=["prefix_only", "read_ahead"])
 @pytest.mark.parametrize("name", ["spec", "large", "tiny"])
 def test_commit_clipping(name, read_ahead):
     w = {"spec": lambda: W.spec(groups=16), "large": lambda: W.large(groups=12), "tiny": W.tiny}[name]()
-    eos, budgets = _clip_inputs(w, 70 + len(name))
+    eos, budgets = W.commit_clip(w, 70 + len(name))
     plan = PT.make_plan(w, read_ahead=read_ahead)
     gpu, plan = PT.run_gpu(w, plan=plan, eos_tokens=eos, budgets=budgets)
     orc = PT.run_oracle(w, THREADS, eos_tokens=eos, budgets=budgets)

@@ -306,6 +306,38 @@ def prompt(seed: int = SEEDS["prompt"], rows: int = 512, V: int = 151_936, Vp: i
                   meta={"targets": targets})
 
 
+def commit_clip(w: Workload, seed: int):
+    """Per-group commit-clipping inputs (EOS token, output budget) for a block,
+    cycling through every case: at the limit (budget 0); EOS on a draft; an EOS
+    id drawn at random with a budget of one token; a budget inside the group;
+    EOS on a planted row maximum (an accepted draft, or the correction or bonus
+    token).  Returns (eos_tokens, budgets), int32 [groups] each."""
+    rng = np.random.default_rng(seed)
+    gi = np.asarray(w.group_indptr)
+    G = w.groups
+    eos = np.full(G, -1, np.int32)
+    budgets = np.empty(G, np.int32)
+    for g in range(G):
+        r0, r1 = int(gi[g]), int(gi[g + 1])
+        k = r1 - r0 - 1
+        kind = g % 5
+        budgets[g] = k + 2
+        if kind == 0:
+            budgets[g] = 0
+        elif kind == 1 and k >= 1:
+            eos[g] = int(w.draft_tokens[r0 + int(rng.integers(0, k))])
+        elif kind == 2:
+            eos[g] = int(rng.integers(0, w.V))
+            budgets[g] = 1
+        elif kind == 3:
+            budgets[g] = int(rng.integers(1, k + 2))
+        elif kind == 4:
+            planted = [int(v) for v in w.planted_argmax[r0:r1] if v >= 0]
+            if planted:
+                eos[g] = planted[int(rng.integers(0, len(planted)))]
+    return eos, budgets
+
+
 def make(name: str, **kw) -> Workload:
     return {"tiny": tiny, "decode": decode, "spec": spec, "large": large, "wide": wide,
             "prompt": prompt}[name](**kw)
