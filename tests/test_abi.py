@@ -85,6 +85,8 @@ def test_null_arguments(L):
     assert L.lp_run(None, None) == -1
     assert L.lp_plan_destroy(None) == -1
     assert L.lp_plan_create(None, None) == -1
+    assert L.lp_bind_clip(None, None, None) == -1
+    assert L.lp_score(None, None, None) == -1
 
 
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):

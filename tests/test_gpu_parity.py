@@ -483,3 +483,27 @@ def test_bind_clears_clipping():
     gpu, _ = PT.run_gpu(w, plan=plan)  # a new bind: unclipped
     PT.compare(w, gpu, PT.run_oracle(w, THREADS))
     plan.close()
+
+
+def test_score_and_clip_argument_errors():
+    # host-side checks only: each call returns before anything is enqueued
+    import ctypes
+    import torch
+    import logprob_epilogue_gb300 as lpe
+    L = lpe.lib()
+    w = W.prompt(rows=4, V=1000, Vp=1000)
+    plan = PT.make_plan(w, max_rows=4, max_groups=4)
+    assert L.lp_bind_clip(plan._h, None, None) == -7          # nothing bound yet
+    dev = torch.device("cuda", 0)
+    buf = torch.zeros(64, dtype=torch.int32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    io = lpe.ScoreIO(buf.data_ptr(), buf.data_ptr(), buf.data_ptr(), None, st.data_ptr(), 5)
+    assert L.lp_score(plan._h, ctypes.byref(io), None) == -2   # rows > max_rows
+    io = lpe.ScoreIO(buf.data_ptr() + 4, buf.data_ptr(), buf.data_ptr(), None, st.data_ptr(), 2)
+    assert L.lp_score(plan._h, ctypes.byref(io), None) == -3   # logits not 16-byte aligned
+    io = lpe.ScoreIO(None, buf.data_ptr(), buf.data_ptr(), None, st.data_ptr(), 2)
+    assert L.lp_score(plan._h, ctypes.byref(io), None) == -1   # NULL logits
+    plan.close()
+    gpu, plan = PT.run_gpu(W.spec(groups=2, V=1000, Vp=1000), plan=PT.make_plan(W.spec(groups=2, V=1000, Vp=1000)))
+    assert L.lp_bind_clip(plan._h, ctypes.c_void_p(buf.data_ptr() + 2), None) == -3  # misaligned
+    plan.close()
