@@ -1,9 +1,10 @@
-// lp_plan.cu -- host side of the C ABI (plan / bind / run).
+// lp_plan.cu -- host side of the C ABI (plan / bind / clip / run / score).
 //
 // The plan owns one device allocation holding the run's control block, work
 // queue, per-row counters, group descriptors and per-tile partial results, sized
-// once from the plan descriptor.  lp_run only enqueues the two kernels; nothing
-// is allocated or synchronised on the hot path.
+// once from the plan descriptor.  lp_run and lp_score only enqueue the three
+// kernels (prepare, stream, records); nothing is allocated or synchronised on
+// the hot path.
 #include <cuda_runtime.h>
 
 #include <cstdint>
