@@ -108,6 +108,9 @@ class Oracle:
         L.orc_epilogue.argtypes = [ctypes.POINTER(_IO), ctypes.c_int]
         L.orc_rank.restype = ctypes.c_int32
         L.orc_rank.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_float]
+        L.orc_chain_verify.restype = ctypes.c_int
+        L.orc_chain_verify.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                       ctypes.c_int32] + [ctypes.c_void_p] * 8
         L.orc_score.restype = ctypes.c_int
         L.orc_score.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
                                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
@@ -163,6 +166,29 @@ class Oracle:
             raise RuntimeError(f"orc_score failed: {rc}")
         return {"records": records, "lse": lse_out[:rows], "status": int(status[0])}
 
+    def chain_verify(self, logits: np.ndarray, V: int, group_indptr, draft_tokens, draft_probs, temperature,
+                     u, r):
+        """Stochastic chain verification of float32 rows [rows, Vp] with draft laws
+        draft_probs [rows, Vp] and the uniforms u [rows], r [groups]: dict of
+        accepted [groups] and emitted_tokens [rows]."""
+        logits = np.ascontiguousarray(logits, dtype=np.float32)
+        rows, Vp = logits.shape
+        q = np.ascontiguousarray(draft_probs, np.float32)
+        assert q.shape == logits.shape
+        ip = np.ascontiguousarray(group_indptr, np.int32)
+        G = ip.size - 1
+        dr = np.ascontiguousarray(draft_tokens, np.int32)
+        tt = np.ascontiguousarray(temperature, np.float32)
+        uu = np.ascontiguousarray(u, np.float32)
+        rr = np.ascontiguousarray(r, np.float32)
+        accepted = np.full(max(G, 1), -7, np.int32)
+        emitted = np.full(max(rows, 1), -7, np.int32)
+        rc = self.L.orc_chain_verify(_ptr(logits), rows, int(V), Vp, G, _ptr(ip), _ptr(dr), _ptr(q), _ptr(tt),
+                                     _ptr(uu), _ptr(rr), _ptr(accepted), _ptr(emitted))
+        if rc != 0:
+            raise RuntimeError(f"orc_chain_verify failed: {rc}")
+        return {"accepted": accepted[:G], "emitted_tokens": emitted[:rows]}
+
 
 def load(path: str | None = None) -> Oracle:
     """The default oracle (built on first use), or the library at ``path``."""
@@ -200,6 +226,10 @@ def rank(x, lse_value, lp):
 
 def score(*args, **kw):
     return load().score(*args, **kw)
+
+
+def chain_verify(*args, **kw):
+    return load().chain_verify(*args, **kw)
 
 
 def _epilogue(L, logits: np.ndarray, V: int, group_indptr, draft_tokens, sampled_tokens, requested,

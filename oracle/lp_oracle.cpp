@@ -326,3 +326,88 @@ extern "C" int orc_score(const float* logits, int64_t rows, int64_t V, int64_t V
     *status = st_all.load();
     return 0;
 }
+
+// ---- stochastic chain verification ("mtp-design.md", "Sampling correctness":
+// accept with probability min(1, p/q), on rejection draw the normalised
+// positive residual, after full acceptance draw the bonus from the target law).
+
+namespace {
+
+// Target law of one row at temperature t: p(v) = exp(x_v/t - lse(x/t)), FP64.
+void target_law(const float* x, int64_t V, double t, std::vector<double>& p) {
+    p.assign((size_t)V, 0.0);
+    double m = -INFINITY;
+    for (int64_t v = 0; v < V; ++v) m = std::max(m, (double)x[v] / t);
+    double s = 0.0;
+    for (int64_t v = 0; v < V; ++v) s += std::exp((double)x[v] / t - m);
+    const double log_z = m + std::log(s);  // log of the normaliser
+    for (int64_t v = 0; v < V; ++v) p[(size_t)v] = std::exp((double)x[v] / t - log_z);
+}
+
+// Inverse CDF over ids in ascending order: the smallest v whose running sum of
+// w exceeds r * sum(w).  Zero-weight lanes are never drawn.
+int32_t draw(const std::vector<double>& w, double r) {
+    double total = 0.0;
+    for (double x : w) total += x;
+    const double target = r * total;
+    double c = 0.0;
+    int32_t last = -1;
+    for (size_t v = 0; v < w.size(); ++v) {
+        if (w[v] <= 0.0) continue;
+        c += w[v];
+        last = (int32_t)v;
+        if (c > target) return (int32_t)v;
+    }
+    return last;  // rounding left the target at the total: the last lane with mass
+}
+
+}  // namespace
+
+extern "C" int orc_chain_verify(const float* logits, int64_t rows, int64_t V, int64_t Vp, int32_t groups,
+                                const int32_t* group_indptr, const int32_t* draft_tokens,
+                                const float* draft_probs, const float* temperature, const float* u,
+                                const float* r, int32_t* accepted, int32_t* emitted) {
+    if (!logits || !group_indptr || !draft_tokens || !draft_probs || !temperature || !u || !r || !accepted ||
+        !emitted)
+        return -1;
+    (void)rows;
+    std::vector<double> p, w;
+    for (int32_t g = 0; g < groups; ++g) {
+        const double t = temperature[g];
+        if (!(t > 0.0)) return -1;
+        const int32_t r0 = group_indptr[g];
+        const int32_t k = group_indptr[g + 1] - r0 - 1;
+        int32_t a = 0;
+        int32_t last = -1;
+        for (int32_t j = 0; j <= k; ++j) {
+            const int64_t row = (int64_t)r0 + j;
+            target_law(logits + row * Vp, V, t, p);
+            if (j == k) {  // every draft accepted: the bonus token from the target law
+                last = draw(p, (double)r[g]);
+                break;
+            }
+            const int32_t d = draft_tokens[row];
+            const float* q = draft_probs + row * Vp;
+            const double pd = (d >= 0 && d < V) ? p[(size_t)d] : 0.0;
+            const double qd = (d >= 0 && d < V) ? (double)q[d] : 0.0;
+            if ((double)u[row] * qd < pd) {  // u < p/q: draft j accepted
+                emitted[row] = d;
+                ++a;
+                continue;
+            }
+            // the first rejection: draw from max(p - q, 0), normalised
+            w.assign((size_t)V, 0.0);
+            double mass = 0.0;
+            for (int64_t v = 0; v < V; ++v) {
+                w[(size_t)v] = std::max(p[(size_t)v] - (double)q[v], 0.0);
+                mass += w[(size_t)v];
+            }
+            last = draw(mass > 0.0 ? w : p, (double)r[g]);
+            break;
+        }
+        accepted[g] = a;
+        emitted[(int64_t)r0 + a] = last;
+        for (int32_t j = a + 1; j <= k; ++j) emitted[(int64_t)r0 + j] = -1;
+    }
+    return 0;
+}

@@ -30,8 +30,12 @@
  *             pairs.  A row whose target is -1 (or any id outside [0, V))
  *             writes id -1, NaN bits, rank 0 and alternative ids -1.
  *
+ *   - stochastic chain verification (mtp-design.md, "Sampling correctness"):
+ *             see orc_chain_verify.
+ *
  * Logits are passed as FP32 (BF16 inputs are widened exactly by the caller).
- * Inputs must be finite; the oracle is not defined for NaN or infinities.
+ * -Inf lanes (a masked vocabulary) are allowed where a row keeps a finite lane;
+ * the oracle is not defined for NaN or +Inf.
  */
 #ifndef LP_ORACLE_H
 #define LP_ORACLE_H
@@ -113,6 +117,28 @@ int32_t orc_rank(const float* x, int64_t V, float lse, float lp);
  * Returns 0, or -1 on a NULL required pointer. */
 int orc_score(const float* logits, int64_t rows, int64_t V, int64_t Vp, const int32_t* targets,
               int32_t* records, float* lse_out, uint32_t* status, int threads);
+
+/* Stochastic chain verification ("mtp-design.md", "Sampling correctness":
+ * accept each draft with probability min(1, p/q); on the first rejection draw
+ * from the normalised positive residual max(p - q, 0); after full acceptance
+ * draw the bonus token from the target law).  Groups as in orc_io: group g
+ * holds k drafts on rows r0..r0+k-1 and its bonus row r0+k.  For row j:
+ *   p_j(v) = exp(x_j(v)/t - lse(x_j/t)) over the V lanes, t = temperature[g]
+ *            (FP64 throughout);
+ *   q_j    = draft_probs row r0+j: the law that drew draft d_j (j < k);
+ *   draft j is accepted iff u[r0+j] * q_j(d_j) < p_j(d_j), i.e. u < p/q;
+ *   a      = the number of leading accepted drafts;
+ *   the last token is drawn with r[g] in [0, 1) by inverse CDF over ids in
+ *   ascending order: the smallest v whose running sum of weights exceeds
+ *   r[g] * (total weight), the weights being max(p_a - q_a, 0) when a < k
+ *   (p_a itself if that residual has no mass) and p_k when a == k.
+ * Outputs: accepted[g] = a; emitted[r0+j] = d_j for j < a, the drawn token at
+ * j = a, -1 after.  The random numbers are inputs.  Returns 0, or -1 on a NULL
+ * pointer or a temperature that is not > 0. */
+int orc_chain_verify(const float* logits, int64_t rows, int64_t V, int64_t Vp, int32_t groups,
+                     const int32_t* group_indptr, const int32_t* draft_tokens, const float* draft_probs,
+                     const float* temperature, const float* u, const float* r, int32_t* accepted,
+                     int32_t* emitted);
 
 #ifdef __cplusplus
 }

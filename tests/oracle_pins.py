@@ -417,7 +417,94 @@ def pin_commit_clipping(orc):
     assert r0["accepted"].tolist() == [0, -1] and r0["emitted_tokens"].tolist() == [5, -1] and r0["rows_read"] == 0
 
 
+# ----------------------------------------------------------------------------- stochastic chain verification
+#
+# "mtp-design.md", "Sampling correctness": accept a draft with probability
+# min(1, p/q); on rejection draw the normalised positive residual max(p - q, 0);
+# after full acceptance draw the bonus token from the target law.  The random
+# numbers are inputs.
+
+
+def _log_law(probs):
+    return np.log(np.asarray(probs, np.float64)).astype(np.float32)
+
+
+def pin_chain_closed_form(orc):
+    # target rows with known laws at temperature 1, draft law q on row 0
+    x = np.stack([_log_law([0.5, 0.3, 0.2]), _log_law([0.1, 0.1, 0.8])])
+    q = np.array([[0.2, 0.6, 0.2], [0, 0, 0]], np.float32)
+    def run(u0, r0, qq=q, d0=1):
+        return orc.chain_verify(x, 3, [0, 2], [d0, -1], qq, [1.0], [u0, 0.0], [r0])
+    r = run(0.4, 0.15)                      # 0.4 * 0.6 < 0.3: accepted; bonus from [.1, .1, .8]: 0.15 -> id 1
+    assert r["accepted"].tolist() == [1] and r["emitted_tokens"].tolist() == [1, 1]
+    r = run(0.4, 0.25)                      # bonus: 0.25 -> id 2
+    assert r["emitted_tokens"].tolist() == [1, 2]
+    r = run(0.6, 0.9)                       # 0.36 >= 0.3: rejected; residual [0.3, 0, 0] -> id 0
+    assert r["accepted"].tolist() == [0] and r["emitted_tokens"].tolist() == [0, -1]
+    q2 = np.array([[0.1, 0.8, 0.1], [0, 0, 0]], np.float32)  # residual [0.4, 0, 0.1], mass 0.5
+    assert run(0.5, 0.7, q2)["emitted_tokens"].tolist() == [0, -1]    # 0.35 of 0.5 falls in lane 0
+    assert run(0.5, 0.85, q2)["emitted_tokens"].tolist() == [2, -1]   # 0.425: past 0.4, lane 1 has none
+    # temperature: logits (0, ln 3) at t = 0.5 give the law (0.1, 0.9)
+    xt = np.array([[0.0, np.log(3.0)], [0.0, 0.0]], np.float32)
+    qt = np.array([[0.5, 0.5], [0, 0]], np.float32)
+    a = orc.chain_verify(xt, 2, [0, 2], [0, -1], qt, [0.5], [0.19, 0.0], [0.5])  # 0.19 * 0.5 < 0.1
+    b = orc.chain_verify(xt, 2, [0, 2], [0, -1], qt, [0.5], [0.21, 0.0], [0.0])  # rejected: residual (0, 0.4)
+    assert a["accepted"].tolist() == [1] and b["emitted_tokens"].tolist() == [1, -1]
+    # two drafts: the first accepted, the second rejected
+    x3 = np.stack([_log_law([0.5, 0.3, 0.2]), _log_law([0.2, 0.2, 0.6]), _log_law([1 / 3] * 3)])
+    q3 = np.array([[0.2, 0.6, 0.2], [0.1, 0.1, 0.8], [0, 0, 0]], np.float32)
+    r3 = orc.chain_verify(x3, 3, [0, 3], [1, 2, -1], q3, [1.0], [0.1, 0.9, 0.0], [0.25])
+    assert r3["accepted"].tolist() == [1] and r3["emitted_tokens"].tolist() == [1, 0, -1]  # residual (.1, .1, 0)
+    r3 = orc.chain_verify(x3, 3, [0, 3], [1, 2, -1], q3, [1.0], [0.1, 0.9, 0.0], [0.75])
+    assert r3["emitted_tokens"].tolist() == [1, 1, -1]
+    try:
+        orc.chain_verify(xt, 2, [0, 2], [0, -1], qt, [0.0], [0.5, 0.0], [0.5])
+    except RuntimeError:
+        pass
+    else:
+        raise AssertionError("a temperature of 0 must be refused")
+
+
+def pin_chain_preserves_target_law(orc):
+    # The defining property: with d ~ q and u, r uniform, the first emitted
+    # token follows p exactly, and the bonus token after an acceptance follows
+    # the bonus row's law.  Every draft id is enumerated with weight q(d), u and
+    # r run over midpoint grids of N points, so the frequencies must match the
+    # laws to within about 1/N.
+    V, N, t = 5, 160, 0.7
+    rng = np.random.default_rng(81)
+    x0 = rng.normal(0.0, 1.5, V).astype(np.float32)
+    x1 = rng.normal(0.0, 1.5, V).astype(np.float32)
+    q = rng.dirichlet(np.ones(V)).astype(np.float32)
+    law = lambda x: np.exp(x / t - np.log(np.exp(x.astype(np.float64) / t).sum()))  # noqa: E731
+    grid = (np.arange(N) + 0.5) / N
+    d, ui, ri = np.meshgrid(np.arange(V), np.arange(N), np.arange(N), indexing="ij")
+    d, ui, ri = d.ravel(), ui.ravel(), ri.ravel()
+    G = d.size
+    logits = np.empty((2 * G, V), np.float32)
+    logits[0::2], logits[1::2] = x0, x1
+    qq = np.zeros((2 * G, V), np.float32)
+    qq[0::2] = q
+    drafts = np.full(2 * G, -1, np.int32)
+    drafts[0::2] = d
+    u = np.zeros(2 * G, np.float32)
+    u[0::2] = grid[ui]
+    res = orc.chain_verify(logits, V, np.arange(G + 1) * 2, drafts, qq, np.full(G, t, np.float32), u,
+                           grid[ri].astype(np.float32))
+    wgt = q[d].astype(np.float64) / (N * N)
+    first = res["emitted_tokens"][0::2]
+    freq = np.bincount(first, weights=wgt, minlength=V)
+    assert np.abs(freq - law(x0)).max() < 3.0 / N, (freq, law(x0))
+    acc = res["accepted"] == 1
+    bonus = np.bincount(res["emitted_tokens"][1::2][acc], weights=wgt[acc], minlength=V) / wgt[acc].sum()
+    assert np.abs(bonus - law(x1)).max() < 3.0 / N, (bonus, law(x1))
+    # the acceptance rate itself: sum over d of q(d) min(1, p(d)/q(d))
+    rate = float(np.minimum(q.astype(np.float64), law(x0)).sum())
+    assert abs(float(wgt[acc].sum()) - rate) < 2.0 / N
+
+
 ALL_PINS = [pin_golden_rows, pin_golden_groups, pin_brute_force, pin_lse_independent,
             pin_two_value_closed_form, pin_sum_exp_invariant, pin_pad_exclusion, pin_id_passthrough,
             pin_acceptance_prefixes, pin_tiny_workload, pin_status_bits, pin_score_rank_independent,
-            pin_score_collapse_closed_form, pin_score_ties_and_invalid, pin_commit_clipping]
+            pin_score_collapse_closed_form, pin_score_ties_and_invalid, pin_commit_clipping,
+            pin_chain_closed_form, pin_chain_preserves_target_law]

@@ -65,6 +65,11 @@ MUTANTS = {
     "eos_ignored": ("const bool clipped = (eos >= 0 && chosen == eos) || j + 1 >= budget;",
                     "const bool clipped = j + 1 >= budget;"),
     "at_limit_still_steps": ("    if (budget <= 0) {", "    if (budget < 0) {"),
+    "chain_accept_ratio_inverted": ("if ((double)u[row] * qd < pd) {", "if ((double)u[row] * pd < qd) {"),
+    "chain_residual_abs": ("w[(size_t)v] = std::max(p[(size_t)v] - (double)q[v], 0.0);",
+                           "w[(size_t)v] = std::fabs(p[(size_t)v] - (double)q[v]);"),
+    "chain_reject_draws_target": ("last = draw(mass > 0.0 ? w : p, (double)r[g]);", "last = draw(p, (double)r[g]);"),
+    "chain_temperature_ignored": ("target_law(logits + row * Vp, V, t, p);", "target_law(logits + row * Vp, V, 1.0, p);"),
     "eos_not_emitted": ("        io.emitted_tokens[row] = chosen;\n",
                         "        io.emitted_tokens[row] = (eos >= 0 && chosen == eos) ? -1 : chosen;\n"),
 }
