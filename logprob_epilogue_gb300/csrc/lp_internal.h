@@ -13,16 +13,11 @@ __host__ __device__ constexpr int tile_elems() { return kTileBytes / ELT; }
 inline int tile_elems_of_dtype(int dtype) { return dtype == 1 ? kTileBytes / 2 : kTileBytes / 4; }
 constexpr int kConsumerThreads = 256;   // 8 compute warps
 constexpr int kThreads = kConsumerThreads + 64;  // + 1 producer warp + 1 selector warp
-#ifndef LP_RING
-#define LP_RING 4
-#endif
-constexpr int kRing = LP_RING;          // tile results in flight between compute and merge warps
-constexpr int kKeysPerTile = 32;        // retained sort keys per tile
+constexpr int kKeysPerTile = 32;        // natural-alternative summary entries per tile (4 per compute warp)
 constexpr int kRecordWords = 258;
 constexpr int kScoreWords = 43;        // prompt-scoring record: id, lp bits, rank, 20 pairs
 constexpr int kScoreAlts = 20;
 constexpr int kMaxIds = 128;
-constexpr int kCandCap = 256;           // tile candidate buffer (keys)
 
 // Pipeline stages per CTA and CTAs per SM, per element type: three CTAs of two
 // 32 KiB stages fill the SM's shared memory and give 24 compute warps per SM.
@@ -121,7 +116,8 @@ struct Params {
     float2* part_ms;      // [max_rows * T * 8] (max, exp-sum) of each compute warp's share of a tile
     int2* part_rank;      // [max_rows * T * 8] prompt scoring: (lanes above the target's logit, the
                           // smallest such logit's bits) of each compute warp's share of a tile
-    unsigned long long* part_keys;  // [max_rows * T * 32] tile keys, descending
+    unsigned long long* part_keys;  // [max_rows * T * 32] natural tiles: each compute warp's 4 largest
+                                    // thread maxima, (ord32 << 32) | (tile << 8) | thread; 0 = none
     unsigned long long timeout_ns;
     unsigned int debug_flags;
     int read_ahead;       // 0: rows past a group's emitted prefix are never read

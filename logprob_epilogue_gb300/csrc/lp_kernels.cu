@@ -90,10 +90,6 @@ __device__ __forceinline__ float unord32(uint32_t o) {
     return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
 }
 
-__device__ __forceinline__ unsigned long long make_key(float x, uint32_t id) {
-    x = __fadd_rn(x, 0.0f);  // -0 -> +0
-    return (static_cast<unsigned long long>(ord32(x)) << 32) | static_cast<unsigned long long>(~id);
-}
 
 __device__ __forceinline__ float key_value(unsigned long long k) { return unord32(static_cast<uint32_t>(k >> 32)); }
 __device__ __forceinline__ uint32_t key_id(unsigned long long k) { return ~static_cast<uint32_t>(k); }
@@ -120,7 +116,7 @@ __device__ __forceinline__ void vstore(T* p, T v) { *reinterpret_cast<volatile T
 // p.trace_cap events; an event is (globaltimer ns, type << 56 | row << 24 | tile).
 enum : unsigned { kTrKernel = 1, kTrClaim, kTrIssue, kTrTileStart, kTrTileEnd, kTrPublish, kTrMergeStart,
                   kTrDecision, kTrMergeEnd, kTrPrepStart, kTrPrepEnd, kTrExit, kTrTileB1, kTrTileB2,
-                  kTrWarpAppend, kTrWarpDone };
+                  kTrWarpAppend, kTrWarpDone, kTrRecStart, kTrRecEnd };
 
 __shared__ unsigned g_trace_n[3];  // per-CTA event counts (producer, compute, merge)
 
@@ -215,11 +211,6 @@ __device__ __forceinline__ float warp_sum_f(float v) {
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
     return v;
 }
-__device__ __forceinline__ int warp_sum_i(int v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-    return v;
-}
 // Sorts one value per lane in descending order across the warp (bitonic).
 template <typename T>
 __device__ __forceinline__ T warp_sort_desc(T v, int lane) {
@@ -253,31 +244,24 @@ constexpr int kMaxStages = 8;
 constexpr int kWarps = kConsumerThreads / 32;  // compute warps
 static_assert(StageCfg<2>::kStages <= kMaxStages && StageCfg<4>::kStages <= kMaxStages, "stage count");
 
-// Natural-alternative tiles: the 8 compute warps exchange their candidate
-// thresholds and candidates through a slot of this ring (one slot per tile).
 // Tiles handed from the compute warps to the helper warp, in order.
 constexpr int kDoneRing = 4;
-
-struct CandSlot {
-    float wTheta[kWarps];                   // the warp's 4th largest thread maximum
-    int wcnt[kWarps];                       // keys in cand[w] (<= 32)
-    long long tslot;                        // the tile's index among all row tiles (row * T + tile)
-    unsigned long long cand[kWarps][32];    // the warp's keys >= theta (its best 32 if more)
-};
 
 struct Shared {
     uint64_t full[kMaxStages];       // stage filled (producer + TMA)
     uint64_t empty[kMaxStages];      // stage released (8 compute warps)
-    uint64_t ctheta[kRing];          // candidate slot: thresholds of the 8 warps written
-    uint64_t ccand[kRing];           // candidate slot: candidates of the 8 warps written
-    uint64_t cfree[kRing];           // candidate slot: read by the helper warp
     uint64_t dfull[kDoneRing];       // done slot: the 8 compute warps finished the tile
     uint64_t dfree[kDoneRing];       // done slot: read by the helper warp
-    int4 dslot[kDoneRing];           // done slot: (row, queue entry, natural, 0) of the tile
+    int4 dslot[kDoneRing];           // done slot: (row, queue entry, 0, 0) of the tile
     int sel_exit;                    // compute warps that have finished (the helper stops at 8)
+    unsigned long long wbest[kWarps];  // each warp's last best-key atomic result (an issue dependency)
     int4 info[kMaxStages];           // work item of each stage
-    CandSlot cs[kRing];
 };
+
+// Natural alternatives in the record stage (see natural_record).
+constexpr int kCandThreads = 512;    // candidate thread slots (tile << 8 | thread)
+constexpr int kCandShares = 16;      // warp shares re-read whole (their 4th summary entry reaches theta)
+constexpr int kCandKeys = 1024;      // candidate logprob keys
 
 // Shared memory of the record kernel.
 struct RecShared {
@@ -285,11 +269,17 @@ struct RecShared {
     float red_f[kWarps];
     float red_f2[kWarps];
     int red_i[kWarps];
+    int red_x[kWarps];                      // natural_exact: counts
     float lse;
     float xchosen;
     float xlim;                             // prompt scoring: largest logit whose lp is the target's
     int corr;                               // prompt scoring: logits in (target's, xlim]
+    uint32_t theta_o;                       // natural: ord32 of the candidate threshold (0: none)
+    int n_thr, n_sh, n_keys;                // natural: candidate threads, shares and keys
     int rec[kRecordWords + 2];              // record being assembled
+    uint32_t cthr[kCandThreads];
+    uint32_t csh[kCandShares];
+    unsigned long long ckeys[kCandKeys];
 };
 
 // ---- tile element access
@@ -526,6 +516,10 @@ __global__ void __launch_bounds__(1024) lp_prepare_kernel(Params p) {
         unsigned long long* e = p.trace + ((size_t)p.trace_ctas * 3) * p.trace_cap * 2;
         e[0] = globaltimer();
         e[1] = (unsigned long long)kTrPrepStart << 56;
+        e[4] = ~0ull;  // first record-kernel start (atomicMin)
+        e[5] = (unsigned long long)kTrRecStart << 56;
+        e[6] = 0ull;   // last record-kernel end (atomicMax)
+        e[7] = (unsigned long long)kTrRecEnd << 56;
     }
     __shared__ int s_warp[32];
     __shared__ int s_total;
@@ -858,32 +852,30 @@ __device__ __noinline__ void producer_loop(const Params& p, Shared& sm, unsigned
     }
 }
 
-// ------------------------------------------------------------------ tile: candidate selection
+// ------------------------------------------------------------------ tile: natural-alternative summary
+//
+// A natural-alternative tile keeps no candidates.  Each compute warp writes the
+// four largest maxima of its 32 threads (each thread's maximum over its 8
+// vectors, from pass 1) with their positions: summary entry
+//   (ord32(thread maximum) << 32) | (tile << 8) | thread,   0 = none
+// (threads whose lanes all lie past V have none).  The record stage turns the
+// row's entries into a threshold theta below which no natural alternative can
+// lie, and re-reads only the threads whose maximum reaches it (natural_record).
 
-// Element k of the calling thread (tile layout), read from the stage; -inf past nv.
-__device__ __forceinline__ int warp_excl_scan_i(int v, int lane, int* total) {
-    int incl = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_up_sync(kFull, incl, o);
-        if (lane >= o) incl += t;
-    }
-    *total = __shfl_sync(kFull, incl, 31);
-    return incl - v;
-}
 
-// Warp-level top-4 extraction on ord32 values: returns the 4th largest
-// (knocking out one lane per round), and the largest through *mx.
-__device__ __forceinline__ uint32_t warp_fourth_largest(uint32_t u, int lane, uint32_t* mx) {
-    uint32_t r = 0;
+// The warp's four largest thread maxima u (ord32, 0 = none), largest first:
+// lane r < 4 receives entry r.  Equal maxima are taken lowest lane first.
+__device__ __forceinline__ unsigned long long warp_summary(uint32_t u, int lane, uint32_t pos_base) {
+    unsigned long long mine = 0ull;
 #pragma unroll
-    for (int round = 0; round < 4; ++round) {
-        r = __reduce_max_sync(kFull, u);
-        if (round == 0) *mx = r;
-        const unsigned b = __ballot_sync(kFull, u == r);
-        if (lane == __ffs(b) - 1) u = 0u;
+    for (int r = 0; r < 4; ++r) {
+        const uint32_t v = __reduce_max_sync(kFull, u);
+        const unsigned b = __ballot_sync(kFull, u == v);
+        const int l = __ffs(b) - 1;
+        if (lane == r && v != 0u) mine = ((unsigned long long)v << 32) | (unsigned long long)(pos_base + (uint32_t)l);
+        if (lane == l) u = 0u;
     }
-    return r;
+    return mine;
 }
 
 // Tile element id (within the tile) of the thread's first element equal to m,
@@ -907,184 +899,6 @@ __device__ __forceinline__ int first_equal(const unsigned char* sp, int tid, int
     return (cf * kConsumerThreads + tid) * L::EPV + ef;
 }
 
-// Exact best 32 keys (value descending, id ascending) of the warp's share of a
-// tile, for the rare warp with more than 32 elements >= theta (long runs of
-// equal or close values).  The warp's 32nd largest value v is found by
-// bisection over the ordered bit patterns in [theta, warp maximum] (BF16: over
-// the 16-bit patterns of BF16 values only); each probe counts, warp-wide, the
-// elements >= it in the thread's vectors whose maximum reaches theta (pass),
-// since no other vector holds one.  Then every element above v (fewer than 32)
-// and the smallest ids equal to v are written to region[0..32), in no
-// particular order.  The -inf lanes of a partial tile are never taken.
-template <int ELT, bool FULL>
-__device__ __noinline__ void warp_top32_select(const unsigned char* sp, int tid, unsigned pass, float theta,
-                                               uint32_t omx, int tbase, unsigned long long* region) {
-    using L = TileLayout<ELT>;
-    const int lane = tid & 31;
-    auto elem = [](const uint32_t (&w)[4], int e) {
-        return (ELT == 2) ? ((e & 1) ? bf16_hi(w[e >> 1]) : bf16_lo(w[e >> 1])) : __uint_as_float(w[e]);
-    };
-    auto count_ge = [&](float x) {
-        int c = 0;
-        for (unsigned q = pass; q; q &= q - 1u) {
-            const uint4 v = ld_vec<ELT, FULL>(sp, __ffs(q) - 1, tid, 0);
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int e = 0; e < L::EPV; ++e) {
-                const float y = elem(w, e);
-                c += (y >= x && (FULL || y > kNegInf)) ? 1 : 0;
-            }
-        }
-        return warp_sum_i(c);
-    };
-    // v: the largest pattern whose value still has >= 32 elements at or above
-    // it (true at theta, whose count is the warp's candidate count)
-    float v;
-    if constexpr (ELT == 2) {
-        auto val = [](uint32_t k) { return unord32((k << 16) | ((k & 0x8000u) ? 0u : 0xFFFFu)); };
-        uint32_t lo = ord32(theta) >> 16, hi = omx >> 16;
-        while (lo < hi) {
-            const uint32_t mid = lo + ((hi - lo + 1u) >> 1);
-            if (count_ge(val(mid)) >= 32) lo = mid;
-            else hi = mid - 1u;
-        }
-        v = val(lo);
-    } else {
-        uint32_t lo = ord32(theta), hi = omx;
-        while (lo < hi) {
-            const uint32_t d = hi - lo;
-            const uint32_t mid = lo + (d >> 1) + (d & 1u);
-            if (count_ge(unord32(mid)) >= 32) lo = mid;
-            else hi = mid - 1u;
-        }
-        v = unord32(lo);
-    }
-    // every element above v
-    int gt = 0;
-    for (unsigned q = pass; q; q &= q - 1u) {
-        const uint4 x = ld_vec<ELT, FULL>(sp, __ffs(q) - 1, tid, 0);
-        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-        for (int e = 0; e < L::EPV; ++e) {
-            const float y = elem(w, e);
-            gt += (y > v && (FULL || y > kNegInf)) ? 1 : 0;
-        }
-    }
-    int got = 0;
-    int pos = warp_excl_scan_i(gt, lane, &got);  // got < 32
-    for (unsigned q = pass; q; q &= q - 1u) {
-        const int c = __ffs(q) - 1;
-        const uint4 x = ld_vec<ELT, FULL>(sp, c, tid, 0);
-        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-        for (int e = 0; e < L::EPV; ++e) {
-            const float y = elem(w, e);
-            if (y > v && (FULL || y > kNegInf))
-                region[pos++] = make_key(y, (uint32_t)(tbase + (c * kConsumerThreads + tid) * L::EPV + e));
-        }
-    }
-    // elements equal to v in ascending id order: vector by vector, lanes in
-    // order within each
-    for (int c = 0; c < L::NCH && got < 32; ++c) {
-        const bool mine_c = (pass >> c) & 1u;
-        if (!__any_sync(kFull, mine_c)) continue;
-        uint32_t w[4] = {0u, 0u, 0u, 0u};
-        int mine = 0;
-        if (mine_c) {
-            const uint4 x = ld_vec<ELT, FULL>(sp, c, tid, 0);
-            w[0] = x.x; w[1] = x.y; w[2] = x.z; w[3] = x.w;
-#pragma unroll
-            for (int e = 0; e < L::EPV; ++e) {
-                const float y = elem(w, e);
-                mine += (y == v && (FULL || y > kNegInf)) ? 1 : 0;
-            }
-        }
-        int total = 0;
-        int before = warp_excl_scan_i(mine, lane, &total);
-        if (mine_c) {
-#pragma unroll
-            for (int e = 0; e < L::EPV; ++e) {
-                const float y = elem(w, e);
-                if (y == v && (FULL || y > kNegInf)) {
-                    if (got + before < 32)
-                        region[got + before] = make_key(y, (uint32_t)(tbase + (c * kConsumerThreads + tid) * L::EPV + e));
-                    ++before;
-                }
-            }
-        }
-        got += total;
-    }
-}
-
-// Writes the keys of the warp's elements >= theta (full tile) into its region
-// of 32 keys and returns the warp's count (above 32 means the region holds only
-// some of them).  Each lane re-reads only its vectors whose maximum reaches
-// theta and keeps its first two candidates in registers; ballots give the
-// slots.  A lane with more than two candidates (rare) writes the rest after a
-// warp scan.  Every lane of the warp calls it.
-template <int ELT, bool FULL>
-__device__ __forceinline__ int capture_candidates(const unsigned char* sp, int tid, int nv, float theta, int tbase,
-                                                  const uint32_t (&cm)[TileLayout<ELT>::NCH],
-                                                  unsigned long long* region) {
-    using L = TileLayout<ELT>;
-    const int lane = tid & 31;
-    unsigned pass = 0u;
-#pragma unroll
-    for (int c = 0; c < L::NCH; ++c) pass |= (vec_max<ELT>(cm[c]) >= theta ? 1u : 0u) << c;
-    int n = 0, k0 = 0, k1 = 0;     // k: the thread's element index c*EPV + e
-    float x0 = 0.0f, x1 = 0.0f;
-    for (unsigned q = pass; q; q &= q - 1u) {
-        const int c = __ffs(q) - 1;
-        const uint4 v = ld_vec<ELT, FULL>(sp, c, tid, nv);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int e = 0; e < L::EPV; ++e) {
-            const float x = (ELT == 2) ? ((e & 1) ? bf16_hi(w[e >> 1]) : bf16_lo(w[e >> 1])) : __uint_as_float(w[e]);
-            const bool take = x >= theta && (FULL || x > kNegInf);
-            x1 = (take && n == 1) ? x : x1;
-            k1 = (take && n == 1) ? c * L::EPV + e : k1;
-            x0 = (take && n == 0) ? x : x0;
-            k0 = (take && n == 0) ? c * L::EPV + e : k0;
-            n += take ? 1 : 0;
-        }
-    }
-    const unsigned lt = (1u << lane) - 1u;
-    const unsigned b0 = __ballot_sync(kFull, n >= 1), b1 = __ballot_sync(kFull, n >= 2);
-    const int p0 = __popc(b0 & lt), p1 = __popc(b0) + __popc(b1 & lt);
-    if (n >= 1 && p0 < 32)
-        region[p0] = make_key(x0, (uint32_t)(tbase + ((k0 / L::EPV) * kConsumerThreads + tid) * L::EPV + k0 % L::EPV));
-    if (n >= 2 && p1 < 32)
-        region[p1] = make_key(x1, (uint32_t)(tbase + ((k1 / L::EPV) * kConsumerThreads + tid) * L::EPV + k1 % L::EPV));
-    const int total = (int)__reduce_add_sync(kFull, (unsigned)n);
-    if (__any_sync(kFull, n > 2)) {
-        // candidates beyond a lane's second: slots after all first and second ones
-        int unused = 0;
-        int pos = __popc(b0) + __popc(b1) + warp_excl_scan_i(n > 2 ? n - 2 : 0, lane, &unused);
-        if (n > 2) {
-            int j = 0;
-            for (unsigned q = pass; q && pos < 32; q &= q - 1u) {
-                const int c = __ffs(q) - 1;
-                const uint4 v = ld_vec<ELT, FULL>(sp, c, tid, nv);
-                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                for (int e = 0; e < L::EPV; ++e) {
-                    const float x =
-                        (ELT == 2) ? ((e & 1) ? bf16_hi(w[e >> 1]) : bf16_lo(w[e >> 1])) : __uint_as_float(w[e]);
-                    if (x >= theta && (FULL || x > kNegInf)) {
-                        if (j >= 2 && pos < 32) {
-                            region[pos] = make_key(x, (uint32_t)(tbase + (c * kConsumerThreads + tid) * L::EPV + e));
-                            ++pos;
-                        }
-                        ++j;
-                    }
-                }
-            }
-        }
-    }
-    return total;
-}
-
-
 // The best 32 of two descending lists (one key per lane), descending.
 template <typename T>
 __device__ __forceinline__ T merge_lists(T a, T b, int lane) {
@@ -1092,99 +906,24 @@ __device__ __forceinline__ T merge_lists(T a, T b, int lane) {
     return warp_bitonic_clean_desc(rev > a ? rev : a, lane);
 }
 
-// Best 32 keys (descending, lane i holds the i-th) of a tile's candidate
-// regions: the keys are taken 64 at a time in region order, each half sorted
-// (bitonic), the halves and the running result merged.  When every value is
-// BF16-representable (a BF16 tile, or an FP32 tile of such values) the sort runs
-// on 32-bit keys, exact for those values and ids: the value's ord32 carries no
-// bits in its low half (all zeros or all ones), and a tile id fits in 16 bits,
-// so  key32 = ord32 >> 16 << 16 | (0xFFFF - (id - tbase))  orders like the
-// 64-bit key, at half the shuffles.
-template <typename K>
-__device__ __forceinline__ K slot_key(unsigned long long k, uint32_t tbase) {
-    if constexpr (sizeof(K) == 8) {
-        return k;
-    } else {
-        if (k == 0ull) return 0u;
-        const uint32_t o = static_cast<uint32_t>(k >> 32), id = ~static_cast<uint32_t>(k);
-        return (o & 0xFFFF0000u) | (0xFFFFu - (id - tbase));
-    }
-}
-
-template <typename K>
-__device__ __forceinline__ unsigned long long slot_unkey(K k, uint32_t tbase) {
-    if constexpr (sizeof(K) == 8) {
-        return k;
-    } else {
-        if (k == 0u) return 0ull;
-        const uint32_t hi = k & 0xFFFF0000u;
-        const uint32_t o = hi | ((hi & 0x80000000u) ? 0u : 0xFFFFu);  // the value's ord32 low half
-        const uint32_t id = tbase + (0xFFFFu - (k & 0xFFFFu));
-        return (static_cast<unsigned long long>(o) << 32) | static_cast<unsigned long long>(~id);
-    }
-}
-
-template <typename K>
-__device__ __forceinline__ unsigned long long slot_top32(const CandSlot& R, int lane, uint32_t tbase) {
-    int cw[kWarps];
-    int n = 0;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-        cw[w] = R.wcnt[w];
-        n += cw[w];
-    }
-    K r = 0;
-    for (int q0 = 0; q0 < n; q0 += 64) {
-        unsigned long long a = 0ull, b = 0ull;
-        int before = 0;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-            const int ia = q0 + lane - before, ib = ia + 32;
-            if (ia >= 0 && ia < cw[w]) a = R.cand[w][ia];
-            if (ib >= 0 && ib < cw[w]) b = R.cand[w][ib];
-            before += cw[w];
-        }
-        const K sa = warp_sort_desc(slot_key<K>(a, tbase), lane);
-        const K sb = warp_sort_desc(slot_key<K>(b, tbase), lane);
-        const K c = merge_lists(sa, sb, lane);
-        r = q0 == 0 ? c : merge_lists(r, c, lane);
-    }
-    return slot_unkey<K>(r, tbase);
-}
-
-// True when every candidate of the slot holds a BF16-representable value (the
-// low half of its ord32 all zeros or all ones): an FP32 tile of such values
-// (logits computed in BF16, then widened) can then use the 32-bit keys.
-__device__ __forceinline__ bool slot_bf16_values(const CandSlot& R, int lane) {
-    bool ok = true;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-        const int cw = R.wcnt[w];
-        if (lane < cw) {
-            const uint32_t lo = static_cast<uint32_t>(R.cand[w][lane] >> 32) & 0xFFFFu;
-            ok = ok && (lo == 0u || lo == 0xFFFFu);
-        }
-    }
-    return __all_sync(kFull, ok);
-}
-
 __device__ __noinline__ bool decide_row(const Params& p, int2* cur);
 
-// The compute warp's share of one tile: passes, candidates (natural tiles,
-// through a candidate slot), its partial results published to global memory
+// The compute warp's share of one tile: passes, the summary of its thread
+// maxima (natural tiles), its partial results published to global memory
 // ((max, exp-sum) and the argmax key, atomicMax on the row's best key), then
-// the tile handed to the helper warp through a done slot.  FULL = false for
-// the last, partial tile of a row (its lanes past V already -inf in the
-// stage).  SCORE: prompt scoring (the count of logits above the target's is
-// kept too; a separate instance, so generation runs carry none of it).  False
-// after a timeout.
+// the tile handed to the helper warp through a done slot.  The warps of a CTA
+// never wait for one another.  FULL = false for the last, partial tile of a
+// row (its lanes past V already -inf in the stage).  SCORE: prompt scoring
+// (the count of logits above the target's is kept too; a separate instance,
+// so generation runs carry none of it).  False after a timeout.
 template <int ELT, bool FULL, bool SCORE>
 __device__ __forceinline__ bool tile_work(const Params& p, Shared& sm, const unsigned char* sp, int nv, int tbase,
-                                          const int4& info, int stage, int& ns, uint32_t& nphase,
-                                          int& ds, uint32_t& dphase, unsigned long long deadline) {
+                                          const int4& info, int stage, int& ds, uint32_t& dphase,
+                                          unsigned long long deadline) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int mode = info.w;
     const bool natural = mode == kModeNatural;
+    const long long tslot = (long long)info.x * p.T + info.y;
     // prompt scoring: the target's logit, loaded now and used after the passes
     float xt = 0.0f;
     if (SCORE && lane == 0) xt = load_logit<ELT>(p, info.x, __ldg(&p.targets[info.x]));
@@ -1192,26 +931,7 @@ __device__ __forceinline__ bool tile_work(const Params& p, Shared& sm, const uns
     uint32_t cm[TileLayout<ELT>::NCH];
     const float m = stage_max<ELT, FULL>(sp, tid, nv, cm);
     const uint32_t om = ord32(__fadd_rn(m, 0.0f));
-    uint32_t omx;
-    CandSlot& C = sm.cs[ns];
-    const uint32_t npar = (nphase >> ns) & 1u;
-    if (natural) {
-        // theta = min over warps of the warp's 4th largest thread maximum: at
-        // least 32 elements of the tile are >= theta, so its best 32 are among
-        // them.  The warp publishes its part now and reads the others' after
-        // its exp pass, so the exchange costs no wait in the common case.
-        const uint32_t o4 = warp_fourth_largest(om, lane, &omx);
-        if (__any_sync(kFull, !mbar_wait(&sm.cfree[ns], npar, deadline))) {  // slot read by its last user
-            if (lane == 0) atomicOr(p.status, kStatusTimeout);
-            return false;
-        }
-        if (lane == 0) {
-            C.wTheta[warp] = unord32(o4);
-            mbar_arrive(&sm.ctheta[ns]);
-        }
-    } else {
-        omx = __reduce_max_sync(kFull, om);
-    }
+    const uint32_t omx = __reduce_max_sync(kFull, om);
     // argmax key: smallest id among the lanes holding the warp maximum
     uint32_t id = 0xFFFFFFFFu;
     if (om == omx && m > kNegInf) id = (uint32_t)(tbase + first_equal<ELT, FULL>(sp, tid, nv, m, cm));
@@ -1221,6 +941,12 @@ __device__ __forceinline__ bool tile_work(const Params& p, Shared& sm, const uns
     // handed over (below), long after it returned
     unsigned long long prev_best = 0ull;
     if (lane == 0) prev_best = atomicMax(&p.row_best[info.x], wkey);
+    if (natural) {
+        // the warp's four largest thread maxima, with their positions
+        const unsigned long long e =
+            warp_summary(m > kNegInf ? om : 0u, lane, ((uint32_t)info.y << 8) | (uint32_t)(warp * 32));
+        if (lane < 4) p.part_keys[tslot * kKeysPerTile + warp * 4 + lane] = e;
+    }
     // pass 2: sum exp(x - m) = 2^(x*log2e - mb - mb_lo): mb_lo, the rounding
     // residual of m*log2e, is applied once, so large |m| costs no accuracy
     float s = 0.0f;
@@ -1229,31 +955,8 @@ __device__ __forceinline__ bool tile_work(const Params& p, Shared& sm, const uns
         const float mb_lo = fmaf(m, kLog2e, -mb);
         s = stage_expsum<ELT, FULL>(sp, tid, nv, mb) * ex2(-mb_lo);
     }
-    if (natural) {
-        if (__any_sync(kFull, !mbar_wait(&sm.ctheta[ns], npar, deadline))) {
-            if (lane == 0) atomicOr(p.status, kStatusTimeout);
-            return false;
-        }
-        float theta = C.wTheta[0];
-#pragma unroll
-        for (int w = 1; w < kWarps; ++w) theta = fminf(theta, C.wTheta[w]);
-        const float th = m > kNegInf ? theta : kPosInf;
-        int cw = capture_candidates<ELT, FULL>(sp, tid, nv, th, tbase, cm, C.cand[warp]);
-        if (cw > 32) {
-            // more than 32 at or above theta in this warp (rare): its exact best 32
-            unsigned pass = 0u;
-#pragma unroll
-            for (int c = 0; c < TileLayout<ELT>::NCH; ++c) pass |= (vec_max<ELT>(cm[c]) >= th ? 1u : 0u) << c;
-            warp_top32_select<ELT, FULL>(sp, tid, pass, theta, omx, tbase, C.cand[warp]);
-            cw = 32;
-        }
-        if (lane == 0) {
-            C.wcnt[warp] = cw;
-            if (warp == 0) C.tslot = (long long)info.x * p.T + info.y;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.ccand[ns]);  // the helper warp takes it from here
-        if constexpr (SCORE) {
+    if constexpr (SCORE) {
+        if (natural) {
             // prompt scoring: this warp's lanes whose logit is above the target's,
             // and the smallest of those logits (the rank is finished in the record
             // kernel, once lse is known); vectors whose maximum is not above it
@@ -1278,10 +981,7 @@ __device__ __forceinline__ bool tile_work(const Params& p, Shared& sm, const uns
             }
             cnt = (int)__reduce_add_sync(kFull, (unsigned)cnt);
             mn = warp_min_f(mn);
-            if (lane == 0) {
-                const long long wslot = ((long long)info.x * p.T + info.y) * kWarps + warp;
-                p.part_rank[wslot] = make_int2(cnt, (int)__float_as_uint(mn));
-            }
+            if (lane == 0) p.part_rank[tslot * kWarps + warp] = make_int2(cnt, (int)__float_as_uint(mn));
         }
     }
     // partial results of the warp, then the tile goes to the helper warp
@@ -1293,27 +993,21 @@ __device__ __forceinline__ bool tile_work(const Params& p, Shared& sm, const uns
     const float Mw = unord32(omx);
     const float sc = (m > kNegInf && mode != kModeArgmax) ? s * ex2((m - Mw) * kLog2e) : 0.0f;
     const float sw = warp_sum_f(sc);
-    if (lane == 0) {
-        const long long wslot = ((long long)info.x * p.T + info.y) * kWarps + warp;
-        p.part_ms[wslot] = make_float2(Mw, sw);
-    }
+    if (lane == 0) p.part_ms[tslot * kWarps + warp] = make_float2(Mw, sw);
     if (__any_sync(kFull, !mbar_wait(&sm.dfree[ds], (dphase >> ds) & 1u, deadline))) {  // slot read
         if (lane == 0) atomicOr(p.status, kStatusTimeout);
         return false;
     }
     if (lane == 0) {
-        if (warp == 0) sm.dslot[ds] = make_int4(info.x, info.z, natural ? 1 : 0, 0);
-        // the best-key update has returned, so it is performed at its point of
-        // coherence before the count that follows the arrival
-        asm volatile("" ::"l"(prev_best));
+        if (warp == 0) sm.dslot[ds] = make_int4(info.x, info.z, 0, 0);
+        // the best-key update must have returned (so it is performed at its
+        // point of coherence) before the count that follows the arrival: the
+        // store of its result cannot issue before the result is back
+        sm.wbest[warp] = prev_best;
         mbar_arrive(&sm.dfull[ds]);
     }
     dphase ^= 1u << ds;
     if (++ds == kDoneRing) ds = 0;
-    if (natural) {
-        nphase ^= 1u << ns;
-        if (++ns == kRing) ns = 0;
-    }
     return true;
 }
 
@@ -1330,8 +1024,8 @@ __device__ void compute_loop(const Params& p, Shared& sm, unsigned char* stages,
     const int tid = threadIdx.x, lane = tid & 31;
     const unsigned long long deadline = t0 + p.timeout_ns;
     const int V = (int)p.V;
-    int stage = 0, ns = 0, ds = 0;
-    uint32_t phase = 0, nphase = 0;   // nphase bit r: uses of candidate slot r, mod 2
+    int stage = 0, ds = 0;
+    uint32_t phase = 0;
     uint32_t dphase = 0;              // dphase bit r: uses of done slot r, mod 2
     for (;;) {
         if (__any_sync(kFull, !mbar_wait(&sm.full[stage], phase, deadline))) {
@@ -1348,10 +1042,10 @@ __device__ void compute_loop(const Params& p, Shared& sm, unsigned char* stages,
         trace(p, kTrTileStart, info.x, tile, tid == 0);
         bool ok;
         if (__builtin_expect(nv == kTE, 1)) {
-            ok = tile_work<ELT, true, SCORE>(p, sm, sp, nv, tbase, info, stage, ns, nphase, ds, dphase, deadline);
+            ok = tile_work<ELT, true, SCORE>(p, sm, sp, nv, tbase, info, stage, ds, dphase, deadline);
         } else {
             fill_partial<ELT>(stages + (size_t)stage * kTileBytes, tid, nv);
-            ok = tile_work<ELT, false, SCORE>(p, sm, sp, nv, tbase, info, stage, ns, nphase, ds, dphase, deadline);
+            ok = tile_work<ELT, false, SCORE>(p, sm, sp, nv, tbase, info, stage, ds, dphase, deadline);
         }
         if (!ok) return;
         trace(p, kTrTileEnd, info.x, tile, tid == 0);
@@ -1427,10 +1121,9 @@ __device__ __noinline__ bool decide_row(const Params& p, int2* cur) {
 // ------------------------------------------------------------------ helper warp
 //
 // Takes the compute warps' tiles through the done slots, in order: counts each
-// tile for its row, decides the row when its increment completes it, and
-// writes a natural tile's best 32 keys (descending) from its candidate slot.
-// The compute warps never wait on a count or a decision.  Stops when every
-// compute warp has finished and the next slot holds nothing.
+// tile for its row and decides the row when its increment completes it.  The
+// compute warps never wait on a count or a decision.  Stops when every compute
+// warp has finished and the next slot holds nothing.
 //
 // Ordering without fences.  A decision needs the row's best key complete:
 // every compute warp waits for the result of its best-key atomicMax before
@@ -1445,11 +1138,9 @@ __device__ __noinline__ bool decide_row(const Params& p, int2* cur) {
 template <int ELT>
 __device__ __noinline__ void helper_loop(const Params& p, Shared& sm, unsigned long long deadline) {
     const int lane = threadIdx.x & 31;
-    int ds = 0, ns = 0;
-    int selections = 0;  // natural tiles counted whose keys are not written yet
-    uint32_t dphase = 0, nphase = 0;
+    int ds = 0;
+    uint32_t dphase = 0;
     for (uint32_t i = 0;; ++i) {
-        // counts (and decisions) first: they are on the verify chains' path
         // polled (this warp has nothing else to wait on); lane 0's view decides for the warp
         if (__shfl_sync(kFull, (int)mbar_test_wait(&sm.dfull[ds], (dphase >> ds) & 1u), 0)) {
             const int4 d = sm.dslot[ds];
@@ -1461,33 +1152,12 @@ __device__ __noinline__ void helper_loop(const Params& p, Shared& sm, unsigned l
             }
             dphase ^= 1u << ds;
             if (++ds == kDoneRing) ds = 0;
-            selections += d.z;
             if (lane == 0 && old == p.done_last) {
                 int2 cur = make_int2(d.x, d.y);
                 while (decide_row(p, &cur)) {
                 }
             }
             __syncwarp();
-            continue;
-        }
-        if (selections > 0) {
-            // the oldest natural tile counted: its candidates were in before its done slot
-            const uint32_t cpar = (nphase >> ns) & 1u;
-            if (__any_sync(kFull, !mbar_wait(&sm.ccand[ns], cpar, deadline))) {
-                if (lane == 0) atomicOr(p.status, kStatusTimeout);
-                return;
-            }
-            const CandSlot& C = sm.cs[ns];
-            const uint32_t tbase = static_cast<uint32_t>((C.tslot % p.T) * tile_elems<ELT>());
-            const bool k32 = ELT == 2 || slot_bf16_values(C, lane);
-            const unsigned long long key =
-                k32 ? slot_top32<uint32_t>(C, lane, tbase) : slot_top32<unsigned long long>(C, lane, tbase);
-            p.part_keys[C.tslot * kKeysPerTile + lane] = key;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.cfree[ns]);
-            nphase ^= 1u << ns;
-            if (++ns == kRing) ns = 0;
-            --selections;
             continue;
         }
         if (vload(&sm.sel_exit) == kWarps) {
@@ -1513,12 +1183,6 @@ __global__ void __launch_bounds__(kThreads, StageCfg<ELT>::kMinBlocks) lp_stream
         for (int s = 0; s < S; ++s) {
             mbar_init(&sm.full[s], 1);
             mbar_init(&sm.empty[s], kWarps);
-        }
-        for (int s = 0; s < kRing; ++s) {
-            mbar_init(&sm.ctheta[s], kWarps);
-            mbar_init(&sm.ccand[s], kWarps);
-            mbar_init(&sm.cfree[s], 1);
-            mbar_arrive(&sm.cfree[s]);  // the slot starts free (its phase 0 is complete)
         }
         g_trace_n[0] = g_trace_n[1] = g_trace_n[2] = 0u;
         for (int s = 0; s < kDoneRing; ++s) {
@@ -1555,81 +1219,231 @@ __global__ void __launch_bounds__(kThreads, StageCfg<ELT>::kMinBlocks) lp_stream
 
 // ------------------------------------------------------------------ records
 
-// Natural alternatives from the row's raw top-32 keys r (one per lane, descending),
-// written into rec by one warp.  Exact for the (logprob desc, id asc) order:
-// see the note at the top of the file.
+// ---- natural alternatives of a record (one CTA of 256 threads, the 8 compute warps)
+//
+// The row's summary entries (each compute warp's 4 largest thread maxima, per
+// natural tile) give the threshold theta = the 32nd largest entry value: at
+// least 32 threads, and so 32 lanes, hold a logit >= theta, and every lane >=
+// theta lies in a thread whose maximum reaches theta.  Such a thread is either
+// named by an entry >= theta, or it is not among its warp's 4 largest, and
+// then that warp's 4th entry reaches theta too: that warp share is re-read
+// whole.  So C = {v : x_v >= theta} is gathered exactly, from a few threads'
+// vectors.  C holds the row's 32 largest logits, and fl32(x - lse) is
+// non-decreasing in x, so every lane outside C has a logprob <= lp(x') for the
+// largest float x' below theta: if that is below the K-th logprob L of C, the
+// K best of C by (logprob desc, id asc) are the row's; otherwise the lanes
+// equal to L are collected over the whole row in id order (subtraction ties
+// across theta, rare).  A row with fewer than 32 entries (a tiny vocabulary)
+// gathers every lane; a row whose candidates overflow the shared-memory lists
+// (long runs of equal values) takes the exact path of natural_exact.
+
+// Element e (0..EPV-1) of a 16-byte vector.
 template <int ELT>
-__device__ __noinline__ void natural_from_top32(const Params& p, int* rec, int row, long long base, int kc,
-                                                float lse, unsigned long long r) {
-    const int lane = threadIdx.x & 31;
-    const int T = p.T;
-    const bool real = r != 0ull;
-    const float lp = real ? logprob(key_value(r), lse) : kNegInf;
-    const int keff = (long long)kc < p.V ? kc : (int)p.V;
-    const float Lk = __shfl_sync(kFull, lp, keff - 1);
-    const float lp31 = __shfl_sync(kFull, lp, 31);
-    bool fallback = (p.V > 32) && (lp31 == Lk);
-    if (fallback) {
-        // Lanes equal to Lk outside the raw top-32 lie below its 32nd key
-        // (x32, id32).  If the float just below x32 already maps under Lk, they
-        // all have x == x32 and ids > id32; then the top-32 suffices whenever
-        // it holds at least keff - c_gt lanes equal to Lk with ids <= id32.
-        const unsigned long long k32 = __shfl_sync(kFull, r, 31);
-        const float x32 = key_value(k32);
-        const uint32_t id32 = key_id(k32);
-        if (logprob(nextafterf(x32, kNegInf), lse) != Lk) {
-            const int c_above = __popc(__ballot_sync(kFull, real && lp > Lk));
-            const int enough = __popc(__ballot_sync(kFull, real && lp == Lk && key_id(r) <= id32));
-            if (enough >= keff - c_above) fallback = false;
+__device__ __forceinline__ float vec_elem(const uint4& v, int e) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    if constexpr (ELT == 2) return (e & 1) ? bf16_hi(w[e >> 1]) : bf16_lo(w[e >> 1]);
+    else return __uint_as_float(w[e]);
+}
+
+// Logprob key: descending order = (lp desc, id asc).
+__device__ __forceinline__ unsigned long long lp_key(float x, float lse, uint32_t id) {
+    return (static_cast<unsigned long long>(ord32(logprob(x, lse))) << 32) | static_cast<unsigned long long>(~id);
+}
+
+// The natural pairs of the record (into sm.rec), exact but slow: for rows
+// whose candidates overflow the lists.  L = the K-th largest logprob, found as
+// lp of the K-th largest logit (bisection over the ordered bit patterns of the
+// logits, each step a count over the row); then the lanes above L (fewer than
+// K, sorted by one warp) and the smallest ids equal to L.
+template <int ELT>
+__device__ __noinline__ void natural_exact(const Params& p, RecShared& sm, int row, int keff, float lse) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const long long V = p.V;
+    // the largest o with count(ord32(x) >= o) >= keff
+    uint32_t lo = ord32(kNegInf), hi = ord32(kPosInf);
+    while (lo < hi) {
+        const uint32_t mid = lo + ((hi - lo + 1u) >> 1);
+        int c = 0;
+        for (long long v = tid; v < V; v += kConsumerThreads) c += ord32(__fadd_rn(load_logit<ELT>(p, row, v), 0.0f)) >= mid;
+        c = (int)__reduce_add_sync(kFull, (unsigned)c);
+        if (lane == 0) sm.red_x[warp] = c;
+        cbar();
+        int tot = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) tot += sm.red_x[w];
+        cbar();
+        if (tot >= keff) lo = mid;
+        else hi = mid - 1u;
+    }
+    const float L = logprob(unord32(lo), lse);
+    // lanes reported above L: fewer than keff
+    if (tid == 0) sm.n_keys = 0;
+    cbar();
+    for (long long v = tid; v < V; v += kConsumerThreads) {
+        const float x = load_logit<ELT>(p, row, v);
+        if (logprob(x, lse) > L) {
+            const int i = atomicAdd(&sm.n_keys, 1);
+            if (i < 32) sm.ckeys[i] = lp_key(x, lse, (uint32_t)v);
         }
     }
-    const unsigned long long key2 =
-        real ? ((static_cast<unsigned long long>(ord32(lp)) << 32) | (r & 0xFFFFFFFFull)) : 0ull;
-    const unsigned long long sorted = warp_sort_desc(key2, lane);
-    const int c_gt = fallback ? __popc(__ballot_sync(kFull, real && lp > Lk)) : keff;
-    if (lane < c_gt) {
-        rec[2 + 2 * lane] = (int)key_id(sorted);
-        rec[3 + 2 * lane] = (int)__float_as_uint(key_value(sorted));
+    cbar();
+    const int c_gt = sm.n_keys < 32 ? sm.n_keys : 32;
+    if (warp == 0) {
+        const unsigned long long k = warp_sort_desc(lane < c_gt ? sm.ckeys[lane] : 0ull, lane);
+        if (lane < c_gt) {
+            sm.rec[2 + 2 * lane] = (int)key_id(k);
+            sm.rec[3 + 2 * lane] = (int)__float_as_uint(key_value(k));
+        }
     }
-    if (fallback) {
-        // lanes with logprob == Lk, smallest ids first, tile by tile; a tile can
-        // hide such lanes only if its own 32nd key has logprob == Lk
-        const int need = keff - c_gt;
-        const unsigned lbits = __float_as_uint(Lk);
-        int got = 0;
-        for (int t = 0; t < T && got < need; ++t) {
-            const long long t0e = (long long)t * tile_elems<ELT>();
-            const long long remv = p.V - t0e;
-            const int nvt = remv < tile_elems<ELT>() ? (int)remv : tile_elems<ELT>();
-            const unsigned long long kmin = __ldcg(&p.part_keys[(base + t) * kKeysPerTile + 31]);
-            const bool hid = nvt > 32 && kmin != 0ull && logprob(key_value(kmin), lse) == Lk;
-            if (hid) {
-                for (int e0 = 0; e0 < nvt && got < need; e0 += 32) {
-                    const int e = e0 + lane;
-                    const bool m = e < nvt && logprob(load_logit<ELT>(p, row, t0e + e), lse) == Lk;
-                    const unsigned b = __ballot_sync(kFull, m);
-                    const int before = __popc(b & ((1u << lane) - 1u));
-                    if (m && got + before < need) {
-                        rec[2 + 2 * (c_gt + got + before)] = (int)(t0e + e);
-                        rec[3 + 2 * (c_gt + got + before)] = (int)lbits;
-                    }
-                    got += __popc(b);
-                }
+    // then the lanes equal to L, smallest ids first (warp 0 walks the row in order)
+    if (warp == 0) {
+        const unsigned lbits = __float_as_uint(L);
+        int got = c_gt;
+        for (long long v0 = 0; v0 < V && got < keff; v0 += 32) {
+            const long long v = v0 + lane;
+            const bool m = v < V && logprob(load_logit<ELT>(p, row, v), lse) == L;
+            const unsigned b = __ballot_sync(kFull, m);
+            const int before = __popc(b & ((1u << lane) - 1u));
+            if (m && got + before < keff) {
+                sm.rec[2 + 2 * (got + before)] = (int)v;
+                sm.rec[3 + 2 * (got + before)] = (int)lbits;
+            }
+            got += __popc(b);
+        }
+    }
+    cbar();
+}
+
+// Step 1, every warp: the best 32 summary entries of tiles warp, warp + 8, ...
+// (each tile's 32 entries sorted, then merged into the running list).
+__device__ __forceinline__ unsigned long long summary_top32(const Params& p, long long base, int warp, int lane) {
+    unsigned long long r = 0ull;
+    for (int t = warp; t < p.T; t += kWarps) {
+        const unsigned long long e = __ldcg(&p.part_keys[(base + t) * kKeysPerTile + lane]);
+        r = merge_lists(r, warp_sort_desc(e, lane), lane);
+    }
+    return r;
+}
+
+// Steps 2-5, all 256 threads, after warp 0 has set sm.theta_o (0: gather every
+// lane) and sm.lse: candidates, their logprob keys, the top keff, the
+// subtraction-tie check.  Writes the natural pairs into sm.rec.
+template <int ELT>
+__device__ __noinline__ void natural_record(const Params& p, RecShared& sm, int row, long long base, int keff) {
+    constexpr int TE = tile_elems<ELT>(), EPV = 16 / ELT;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const float lse = sm.lse;
+    const uint32_t th = sm.theta_o;
+    const float theta = th ? unord32(th) : kNegInf;
+    const long long V = p.V;
+    const unsigned char* rowp = reinterpret_cast<const unsigned char*>(p.logits) + (long long)row * p.Vp * ELT;
+    bool overflow = false;
+    if (th == 0u) {
+        // fewer than 32 entries: every lane is a candidate (V is small)
+        if (V > kCandKeys) {
+            overflow = true;
+        } else {
+            for (int v = tid; v < V; v += kConsumerThreads) sm.ckeys[v] = lp_key(load_logit<ELT>(p, row, v), lse, (uint32_t)v);
+            if (tid == 0) sm.n_keys = (int)V;
+        }
+        cbar();
+    } else {
+        // 2. candidate threads: entries >= theta, and whole warp shares whose 4th entry reaches it
+        const int shares = p.T * kWarps;
+        for (int sh = tid; sh < shares; sh += kConsumerThreads) {
+            const ulonglong2* q = reinterpret_cast<const ulonglong2*>(p.part_keys + base * kKeysPerTile + (long long)sh * 4);
+            const ulonglong2 a = __ldcg(q), b = __ldcg(q + 1);
+            const unsigned long long e[4] = {a.x, a.y, b.x, b.y};
+            if (e[3] != 0ull && (uint32_t)(e[3] >> 32) >= th) {
+                const int i = atomicAdd(&sm.n_sh, 1);
+                if (i < kCandShares) sm.csh[i] = (uint32_t)sh;
             } else {
-                const unsigned long long key = __ldcg(&p.part_keys[(base + t) * kKeysPerTile + lane]);
-                const bool m = key != 0ull && logprob(key_value(key), lse) == Lk;
-                // ascending ids: sort the complements descending
-                const uint32_t inv = m ? ~key_id(key) : 0u;
-                const uint32_t sorted_inv = warp_sort_desc(inv, lane);
-                const int cnt = __popc(__ballot_sync(kFull, m));
-                if (lane < cnt && got + lane < need) {
-                    rec[2 + 2 * (c_gt + got + lane)] = (int)(~sorted_inv);
-                    rec[3 + 2 * (c_gt + got + lane)] = (int)lbits;
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    if (e[r] != 0ull && (uint32_t)(e[r] >> 32) >= th) {
+                        const int i = atomicAdd(&sm.n_thr, 1);
+                        if (i < kCandThreads) sm.cthr[i] = (uint32_t)e[r];
+                    }
                 }
-                got += cnt;
+            }
+        }
+        cbar();
+        const int nthr = sm.n_thr, nsh = sm.n_sh;
+        overflow = nthr > kCandThreads || nsh > kCandShares;
+        if (!overflow) {
+            // 3. their vectors, re-read from global memory: keys of the lanes >= theta
+            const int items = (nthr + nsh * 32) * TileLayout<ELT>::NCH;
+            for (int it = tid; it < items; it += kConsumerThreads) {
+                const int c = it % TileLayout<ELT>::NCH, j = it / TileLayout<ELT>::NCH;
+                uint32_t pos;  // tile << 8 | thread
+                if (j < nthr) {
+                    pos = sm.cthr[j];
+                } else {
+                    const uint32_t sh = sm.csh[(j - nthr) >> 5];
+                    pos = ((sh >> 3) << 8) | ((sh & 7u) * 32u + (uint32_t)((j - nthr) & 31));
+                }
+                const long long v0 = (long long)(pos >> 8) * TE + (long long)(c * kConsumerThreads + (int)(pos & 0xFFu)) * EPV;
+                if (v0 >= V) continue;
+                const uint4 x = __ldcs(reinterpret_cast<const uint4*>(rowp + v0 * ELT));
+#pragma unroll
+                for (int e = 0; e < EPV; ++e) {
+                    const float y = vec_elem<ELT>(x, e);
+                    if (v0 + e < V && y >= theta) {
+                        const int i = atomicAdd(&sm.n_keys, 1);
+                        if (i < kCandKeys) sm.ckeys[i] = lp_key(y, lse, (uint32_t)(v0 + e));
+                    }
+                }
+            }
+            cbar();
+            overflow = sm.n_keys > kCandKeys;
+        }
+    }
+    if (overflow) {
+        natural_exact<ELT>(p, sm, row, keff, lse);
+        return;
+    }
+    // 4. the best 32 keys: each warp runs over chunks of 64, warp 0 merges the 8 lists
+    const int nk = sm.n_keys;
+    unsigned long long r = 0ull;
+    for (int q0 = warp * 64; q0 < nk; q0 += kWarps * 64) {
+        const unsigned long long a = q0 + lane < nk ? sm.ckeys[q0 + lane] : 0ull;
+        const unsigned long long b = q0 + 32 + lane < nk ? sm.ckeys[q0 + 32 + lane] : 0ull;
+        r = merge_lists(r, merge_lists(warp_sort_desc(a, lane), warp_sort_desc(b, lane), lane), lane);
+    }
+    sm.lists[warp][lane] = r;
+    cbar();
+    if (warp == 0) {
+        const unsigned long long b0 = merge_lists(sm.lists[0][lane], sm.lists[1][lane], lane);
+        const unsigned long long b1 = merge_lists(sm.lists[2][lane], sm.lists[3][lane], lane);
+        const unsigned long long b2 = merge_lists(sm.lists[4][lane], sm.lists[5][lane], lane);
+        const unsigned long long b3 = merge_lists(sm.lists[6][lane], sm.lists[7][lane], lane);
+        const unsigned long long k = merge_lists(merge_lists(b0, b1, lane), merge_lists(b2, b3, lane), lane);
+        // 5. lanes below theta can tie with the K-th logprob only if the float
+        // just below theta already reports it
+        const float L = key_value(__shfl_sync(kFull, k, keff - 1));
+        const bool ties = th != 0u && logprob(nextafterf(theta, kNegInf), lse) == L;
+        const int c_gt = ties ? __popc(__ballot_sync(kFull, k != 0ull && key_value(k) > L)) : keff;
+        if (lane < c_gt) {
+            sm.rec[2 + 2 * lane] = (int)key_id(k);
+            sm.rec[3 + 2 * lane] = (int)__float_as_uint(key_value(k));
+        }
+        if (ties) {
+            const unsigned lbits = __float_as_uint(L);
+            int got = c_gt;
+            for (long long v0 = 0; v0 < V && got < keff; v0 += 32) {
+                const long long v = v0 + lane;
+                const bool m = v < V && logprob(load_logit<ELT>(p, row, v), lse) == L;
+                const unsigned bb = __ballot_sync(kFull, m);
+                const int before = __popc(bb & ((1u << lane) - 1u));
+                if (m && got + before < keff) {
+                    sm.rec[2 + 2 * (got + before)] = (int)v;
+                    sm.rec[3 + 2 * (got + before)] = (int)lbits;
+                }
+                got += __popc(bb);
             }
         }
     }
+    cbar();
 }
 
 // Prompt scoring: the largest float X with fl32(X - lse) <= lp, where lp =
@@ -1679,8 +1493,11 @@ __device__ __noinline__ void record_block(const Params& p, RecShared& sm, int ro
     constexpr bool score = SCORE;
     for (int w = tid; w < kRecordWords; w += kConsumerThreads)
         sm.rec[w] = (w >= 2 && (w & 1) == 0) ? -1 : (int)kUnusedBits;
-    if (tid == 0) sm.corr = 0;
-    // loads: tile partials, the chosen logit, explicit-id logits, tile key lists
+    if (tid == 0) {
+        sm.corr = 0;
+        sm.n_thr = sm.n_sh = sm.n_keys = 0;
+    }
+    // loads: tile partials, the chosen logit, explicit-id logits, summary entries
     float m = kNegInf, s = 0.0f;
     int above = 0;  // prompt scoring: logits above the target's
     for (int t = tid; t < T * kWarps; t += kConsumerThreads) {  // one (max, exp-sum) per warp of each tile
@@ -1697,16 +1514,7 @@ __device__ __noinline__ void record_block(const Params& p, RecShared& sm, int ro
         id = __ldg(&p.token_ids[(long long)g * kMaxIds + tid]);
         if (id >= 0 && id < p.V) xi = load_logit<ELT>(p, row, id);
     }
-    if (natural) {
-        const unsigned long long* kp = p.part_keys + base * kKeysPerTile + lane;
-        unsigned long long r = 0;
-        for (int t = warp; t < T; t += 16) {
-            const unsigned long long a0 = __ldcg(kp + (long long)t * kKeysPerTile);
-            const unsigned long long a1 = (t + 8 < T) ? __ldcg(kp + (long long)(t + 8) * kKeysPerTile) : 0ull;
-            r = merge_lists(r, merge_lists(a0, a1, lane), lane);
-        }
-        sm.lists[warp][lane] = r;
-    }
+    if (natural) sm.lists[warp][lane] = summary_top32(p, base, warp, lane);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         const float m2 = __shfl_xor_sync(kFull, m, o), s2 = __shfl_xor_sync(kFull, s, o);
@@ -1741,15 +1549,17 @@ __device__ __noinline__ void record_block(const Params& p, RecShared& sm, int ro
             sm.xlim = lp == lp ? score_limit(sm.xchosen, lse, lp, lane) : sm.xchosen;  // NaN: nothing is above
         }
         if (natural) {
+            // theta: the row's 32nd largest summary entry (0: fewer than 32 entries)
             const unsigned long long b0 = merge_lists(sm.lists[0][lane], sm.lists[1][lane], lane);
             const unsigned long long b1 = merge_lists(sm.lists[2][lane], sm.lists[3][lane], lane);
             const unsigned long long b2 = merge_lists(sm.lists[4][lane], sm.lists[5][lane], lane);
             const unsigned long long b3 = merge_lists(sm.lists[6][lane], sm.lists[7][lane], lane);
             const unsigned long long r = merge_lists(merge_lists(b0, b1, lane), merge_lists(b2, b3, lane), lane);
-            natural_from_top32<ELT>(p, sm.rec, row, base, kc, lse, r);
+            if (lane == 31) sm.theta_o = (uint32_t)(r >> 32);
         }
     }
     cbar();
+    if (natural) natural_record<ELT>(p, sm, row, base, (long long)kc < p.V ? kc : (int)p.V);
     if (ids && tid < kc) {
         int bits = (int)kUnusedBits;
         if (id >= 0 && id < p.V) {
@@ -1803,10 +1613,13 @@ __global__ void __launch_bounds__(kConsumerThreads) lp_record_kernel(Params p) {
     __shared__ RecShared rs;
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (vload(&p.ctrl->abort) != 0u) return;
+    unsigned long long* tr = p.trace != nullptr ? p.trace + ((size_t)p.trace_ctas * 3) * p.trace_cap * 2 : nullptr;
+    if (tr != nullptr && threadIdx.x == 0) atomicMin(&tr[4], globaltimer());
     for (int row = blockIdx.x; row < p.rows; row += gridDim.x) {
         const int4 t = __ldcg(&p.rec_tasks[row]);  // (chosen, queue entry, descriptor word, count); 0 word: none
         if (t.z != 0) record_block<ELT, SCORE>(p, rs, row, t.y, t.x, t.z, t.w);
     }
+    if (tr != nullptr && threadIdx.x == 0) atomicMax(&tr[6], globaltimer());
 }
 
 template <int ELT>

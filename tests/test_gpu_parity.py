@@ -228,6 +228,44 @@ def test_poisoned_scratch_and_repeated_runs():
     plan.close()
 
 
+@pytest.mark.parametrize("name", ["large", "spec"])
+def test_decisions_stable_over_back_to_back_runs(name):
+    # Each acceptance decision reads the row's best key, which the compute warps
+    # of other CTAs update; a decision taken before the last update has landed
+    # picks a wrong argmax.  1,000 back-to-back runs on the full-size block (no
+    # L2 flush, scratch poisoned before every third) must each give the
+    # oracle's accepted counts and emitted tokens.
+    import torch
+    w = W.make(name)
+    orc = PT.run_oracle(w, THREADS)
+    d = PT.to_device(w)
+    dev = torch.device("cuda", 0)
+    rows, G, reps = w.rows, w.groups, 1000
+    out = dict(records=torch.zeros((rows, 258), dtype=torch.int32, device=dev),
+               accepted=torch.zeros(G, dtype=torch.int32, device=dev),
+               emitted_tokens=torch.zeros(rows, dtype=torch.int32, device=dev),
+               lse_out=torch.zeros(rows, dtype=torch.float32, device=dev),
+               status=torch.zeros(1, dtype=torch.int32, device=dev))
+    plan = PT.make_plan(w)
+    plan.bind(**d, **out)
+    accs = torch.zeros((reps, G), dtype=torch.int32, device=dev)
+    ems = torch.zeros((reps, rows), dtype=torch.int32, device=dev)
+    sts = torch.zeros(reps, dtype=torch.int32, device=dev)
+    for r in range(reps):
+        if r % 3 == 0:
+            plan.poison_scratch()
+        plan.run()
+        accs[r].copy_(out["accepted"])
+        ems[r].copy_(out["emitted_tokens"])
+        sts[r].copy_(out["status"][0])
+    torch.cuda.synchronize()
+    A, E, S = accs.cpu().numpy(), ems.cpu().numpy(), sts.cpu().numpy()
+    plan.close()
+    assert (S == 0).all()
+    bad = np.flatnonzero((A != orc["accepted"][None, :]).any(1) | (E != orc["emitted_tokens"][None, :]).any(1))
+    assert bad.size == 0, f"{bad.size} of {reps} runs differ from the oracle (first: run {bad[:5].tolist()})"
+
+
 def test_malformed_groups_write_nothing():
     x = np.zeros((3, 100), np.float32)
     w = W.custom(x, 100, [2, 1], k_max=0)   # a group of 2 rows with k_max 0
