@@ -78,6 +78,8 @@ struct Ctrl {
     unsigned int abort;       // 1: malformed groups, the stream kernel does nothing
     unsigned int never;       // never written: the forced-timeout test hook waits on it
     unsigned int pad4[29];
+    unsigned int rec_count;   // record tasks appended (rec_tasks[0, rec_count))
+    unsigned int pad5[31];
 };
 
 struct Params {
@@ -111,8 +113,8 @@ struct Params {
     unsigned long long* row_best;   // [max_rows] best (argmax) key over the finished tiles
     int4* gdesc;          // [max_groups] x = first row, y = k | mode << 8 | explicit << 12 |
                           // requested << 13, z = top_k or id count, w = sampled token
-    int4* rec_tasks;      // [max_rows] per row: (chosen token, queue entry, group descriptor word, count);
-                          // descriptor word 0: no record to build
+    int4* rec_tasks;      // [max_rows] compact list of the records to build: (chosen token, row,
+                          // group descriptor word | count << 16, group), appended by the deciders
     float2* part_ms;      // [max_rows * T * 8] (max, exp-sum) of each compute warp's share of a tile
     int2* part_rank;      // [max_rows * T * 8] prompt scoring: (lanes above the target's logit, the
                           // smallest such logit's bits) of each compute warp's share of a tile

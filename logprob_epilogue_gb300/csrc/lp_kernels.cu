@@ -116,7 +116,7 @@ __device__ __forceinline__ void vstore(T* p, T v) { *reinterpret_cast<volatile T
 // p.trace_cap events; an event is (globaltimer ns, type << 56 | row << 24 | tile).
 enum : unsigned { kTrKernel = 1, kTrClaim, kTrIssue, kTrTileStart, kTrTileEnd, kTrPublish, kTrMergeStart,
                   kTrDecision, kTrMergeEnd, kTrPrepStart, kTrPrepEnd, kTrExit, kTrTileB1, kTrTileB2,
-                  kTrWarpAppend, kTrWarpDone, kTrRecStart, kTrRecEnd };
+                  kTrWarpAppend, kTrWarpDone, kTrRecStart, kTrRecEnd, kTrRecA, kTrRecB, kTrRecC, kTrRecD };
 
 __shared__ unsigned g_trace_n[3];  // per-CTA event counts (producer, compute, merge)
 
@@ -133,6 +133,17 @@ __device__ __forceinline__ void trace(const Params& p, unsigned type, int row, i
     e[0] = globaltimer();
     e[1] = ((unsigned long long)type << 56) | ((unsigned long long)(row & 0xFFFFFFFF) << 24) |
            (unsigned long long)(tile & 0xFFFFFF);
+}
+
+// Record-kernel events go to the merge-role ring of CTA blockIdx.x (after the
+// stream kernel's events of that CTA).
+__device__ __forceinline__ void rtrace(const Params& p, unsigned type, int row) {
+    if (p.trace == nullptr || threadIdx.x != 0 || (int)blockIdx.x >= p.trace_ctas) return;
+    const unsigned i = atomicAdd(&p.trace_count[blockIdx.x * 3 + 2], 1u);
+    if (i >= (unsigned)p.trace_cap) return;
+    unsigned long long* e = p.trace + (((size_t)blockIdx.x * 3 + 2) * p.trace_cap + i) * 2;
+    e[0] = globaltimer();
+    e[1] = ((unsigned long long)type << 56) | ((unsigned long long)(row & 0xFFFFFFFF) << 24);
 }
 
 // ---- mbarrier / bulk copy (PTX ISA: mbarrier, cp.async.bulk)
@@ -181,6 +192,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsign
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 63u) == 63u && globaltimer() > deadline) return false;
     }
+}
+
+#ifndef LP_NATURAL_KEEP
+#define LP_NATURAL_KEEP 0
+#endif
+__device__ __forceinline__ uint64_t evict_normal_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
 }
 
 __device__ __forceinline__ uint64_t evict_first_policy() {
@@ -265,7 +285,6 @@ constexpr int kCandKeys = 1024;      // candidate logprob keys
 
 // Shared memory of the record kernel.
 struct RecShared {
-    unsigned long long lists[kWarps][32];   // per-warp partial top-32 lists
     float red_f[kWarps];
     float red_f2[kWarps];
     int red_i[kWarps];
@@ -275,11 +294,13 @@ struct RecShared {
     float xlim;                             // prompt scoring: largest logit whose lp is the target's
     int corr;                               // prompt scoring: logits in (target's, xlim]
     uint32_t theta_o;                       // natural: ord32 of the candidate threshold (0: none)
+    uint32_t wtop[kWarps][8];               // natural: each warp's 8 largest summary entry values
+    unsigned long long lkey;                // natural: the keff-th best logprob key
     int n_thr, n_sh, n_keys;                // natural: candidate threads, shares and keys
     int rec[kRecordWords + 2];              // record being assembled
     uint32_t cthr[kCandThreads];
     uint32_t csh[kCandShares];
-    unsigned long long ckeys[kCandKeys];
+    alignas(16) unsigned long long ckeys[kCandKeys + 8];
 };
 
 // ---- tile element access
@@ -536,7 +557,6 @@ __global__ void __launch_bounds__(1024) lp_prepare_kernel(Params p) {
         p.queue[r] = ~0ull;
         p.tclaim[r] = 0u;
         p.row_best[r] = 0ull;
-        p.rec_tasks[r] = make_int4(0, 0, 0, 0);
     }
     if (tid == 0) *p.status = 0u;
     // validation: indptr starts at >= 0, ends at <= rows, group sizes 1..k_max+1
@@ -557,6 +577,7 @@ __global__ void __launch_bounds__(1024) lp_prepare_kernel(Params p) {
             p.ctrl->chain_tail = 0u;
             p.ctrl->fresh_rows = 0u;
             p.ctrl->outstanding = 0;
+            p.ctrl->rec_count = 0u;
         }
         return;
     }
@@ -677,6 +698,7 @@ __global__ void __launch_bounds__(1024) lp_prepare_kernel(Params p) {
         p.ctrl->chain_tail = 0u;
         p.ctrl->fresh_rows = static_cast<unsigned>(s_base);
         p.ctrl->outstanding = s_base;
+        p.ctrl->rec_count = 0u;
         p.ctrl->abort = 0u;
     }
 }
@@ -705,6 +727,7 @@ __device__ __noinline__ void producer_loop(const Params& p, Shared& sm, unsigned
     constexpr int kTE = tile_elems<ELT>();
     const unsigned long long deadline = t0 + p.timeout_ns;
     const uint64_t policy = evict_first_policy();
+    const uint64_t npolicy = LP_NATURAL_KEEP ? evict_normal_policy() : policy;
     Ctrl* ctrl = p.ctrl;
     const unsigned T = (unsigned)p.T;
     // fresh item b is this CTA's first (the counter starts past the grid); its
@@ -835,7 +858,7 @@ __device__ __noinline__ void producer_loop(const Params& p, Shared& sm, unsigned
         const unsigned char* src =
             reinterpret_cast<const unsigned char*>(p.logits) + ((long long)item.x * p.Vp + tbase) * ELT;
         mbar_arrive_expect_tx(&sm.full[stage], bytes);
-        bulk_load(stages + (size_t)stage * kTileBytes, src, bytes, &sm.full[stage], policy);
+        bulk_load(stages + (size_t)stage * kTileBytes, src, bytes, &sm.full[stage], item.w == kModeNatural ? npolicy : policy);
         trace(p, kTrIssue, item.x, item.y, true);
         if (++stage == S) {
             stage = 0;
@@ -1104,9 +1127,10 @@ __device__ __noinline__ bool decide_row(const Params& p, int2* cur) {
             for (int jj = j + 1; jj <= k; ++jj) p.emitted[r0 + jj] = -1;
         }
     }
-    if (req) {
+    if (req) {  // the record kernel builds it
         if (chosen >= p.V) atomicOr(p.status, kStatusBadToken);
-        p.rec_tasks[row] = make_int4(chosen, entry, d.y, d.z);  // built by the record kernel
+        const unsigned i = atomicAdd(&p.ctrl->rec_count, 1u);
+        p.rec_tasks[i] = make_int4(chosen, row, (d.y & 0xFFFF) | (d.z << 16), g);
     }
     trace(p, kTrDecision, row, accept ? 1 : 0, true);
     if (!accept) {
@@ -1222,20 +1246,22 @@ __global__ void __launch_bounds__(kThreads, StageCfg<ELT>::kMinBlocks) lp_stream
 // ---- natural alternatives of a record (one CTA of 256 threads, the 8 compute warps)
 //
 // The row's summary entries (each compute warp's 4 largest thread maxima, per
-// natural tile) give the threshold theta = the 32nd largest entry value: at
-// least 32 threads, and so 32 lanes, hold a logit >= theta, and every lane >=
-// theta lies in a thread whose maximum reaches theta.  Such a thread is either
-// named by an entry >= theta, or it is not among its warp's 4 largest, and
-// then that warp's 4th entry reaches theta too: that warp share is re-read
-// whole.  So C = {v : x_v >= theta} is gathered exactly, from a few threads'
-// vectors.  C holds the row's 32 largest logits, and fl32(x - lse) is
-// non-decreasing in x, so every lane outside C has a logprob <= lp(x') for the
-// largest float x' below theta: if that is below the K-th logprob L of C, the
-// K best of C by (logprob desc, id asc) are the row's; otherwise the lanes
-// equal to L are collected over the whole row in id order (subtraction ties
-// across theta, rare).  A row with fewer than 32 entries (a tiny vocabulary)
-// gathers every lane; a row whose candidates overflow the shared-memory lists
-// (long runs of equal values) takes the exact path of natural_exact.
+// natural tile) give a threshold theta such that at least 32 entries, so 32
+// distinct lanes, are >= theta: warp w of the record CTA takes the entries of
+// warp column w of every tile and finds their 4th largest; theta is the
+// smallest of the 8.  Every lane >= theta lies in a thread whose maximum
+// reaches theta.  Such a thread is either named by an entry >= theta, or it is
+// not among its warp share's 4 largest, and then the share's 4th entry reaches
+// theta too: that share is re-read whole.  So C = {v : x_v >= theta} is
+// gathered exactly, from a few threads' vectors.  C holds the row's 32 largest
+// logits, and fl32(x - lse) is non-decreasing in x, so every lane outside C has
+// a logprob <= lp(x') for the largest float x' below theta: if that is below
+// the K-th logprob L of C, the K best of C by (logprob desc, id asc) are the
+// row's; otherwise the lanes equal to L are collected over the whole row in id
+// order (subtraction ties across theta, rare).  A row whose entries cannot
+// give a theta (a tiny vocabulary) takes every lane; a row whose candidates
+// overflow the shared-memory lists (long runs of equal values) takes the exact
+// path of natural_exact.
 
 // Element e (0..EPV-1) of a 16-byte vector.
 template <int ELT>
@@ -1248,6 +1274,26 @@ __device__ __forceinline__ float vec_elem(const uint4& v, int e) {
 // Logprob key: descending order = (lp desc, id asc).
 __device__ __forceinline__ unsigned long long lp_key(float x, float lse, uint32_t id) {
     return (static_cast<unsigned long long>(ord32(logprob(x, lse))) << 32) | static_cast<unsigned long long>(~id);
+}
+
+// Warp 0 writes, from pair slot `from` on, the lanes whose logprob equals L,
+// smallest ids first, until keff pairs are written (a walk over the row).
+template <int ELT>
+__device__ __forceinline__ void fill_equal_lanes(const Params& p, int* rec, int row, float lse, float L, int from,
+                                                 int keff, int lane) {
+    const unsigned lbits = __float_as_uint(L);
+    int got = from;
+    for (long long v0 = 0; v0 < p.V && got < keff; v0 += 32) {
+        const long long v = v0 + lane;
+        const bool m = v < p.V && logprob(load_logit<ELT>(p, row, v), lse) == L;
+        const unsigned bb = __ballot_sync(kFull, m);
+        const int before = __popc(bb & ((1u << lane) - 1u));
+        if (m && got + before < keff) {
+            rec[2 + 2 * (got + before)] = (int)v;
+            rec[3 + 2 * (got + before)] = (int)lbits;
+        }
+        got += __popc(bb);
+    }
 }
 
 // The natural pairs of the record (into sm.rec), exact but slow: for rows
@@ -1287,50 +1333,79 @@ __device__ __noinline__ void natural_exact(const Params& p, RecShared& sm, int r
         }
     }
     cbar();
-    const int c_gt = sm.n_keys < 32 ? sm.n_keys : 32;
     if (warp == 0) {
+        const int c_gt = sm.n_keys < 32 ? sm.n_keys : 32;
         const unsigned long long k = warp_sort_desc(lane < c_gt ? sm.ckeys[lane] : 0ull, lane);
         if (lane < c_gt) {
             sm.rec[2 + 2 * lane] = (int)key_id(k);
             sm.rec[3 + 2 * lane] = (int)__float_as_uint(key_value(k));
         }
-    }
-    // then the lanes equal to L, smallest ids first (warp 0 walks the row in order)
-    if (warp == 0) {
-        const unsigned lbits = __float_as_uint(L);
-        int got = c_gt;
-        for (long long v0 = 0; v0 < V && got < keff; v0 += 32) {
-            const long long v = v0 + lane;
-            const bool m = v < V && logprob(load_logit<ELT>(p, row, v), lse) == L;
-            const unsigned b = __ballot_sync(kFull, m);
-            const int before = __popc(b & ((1u << lane) - 1u));
-            if (m && got + before < keff) {
-                sm.rec[2 + 2 * (got + before)] = (int)v;
-                sm.rec[3 + 2 * (got + before)] = (int)lbits;
-            }
-            got += __popc(b);
-        }
+        fill_equal_lanes<ELT>(p, sm.rec, row, lse, L, c_gt, keff, lane);
     }
     cbar();
 }
 
-// Step 1, every warp: the best 32 summary entries of tiles warp, warp + 8, ...
-// (each tile's 32 entries sorted, then merged into the running list).
-__device__ __forceinline__ unsigned long long summary_top32(const Params& p, long long base, int warp, int lane) {
-    unsigned long long r = 0ull;
-    for (int t = warp; t < p.T; t += kWarps) {
-        const unsigned long long e = __ldcg(&p.part_keys[(base + t) * kKeysPerTile + lane]);
-        r = merge_lists(r, warp_sort_desc(e, lane), lane);
+// Up to kCachedShares warp shares per thread stay in registers between the
+// threshold and the candidate steps; further ones are loaded again.
+constexpr int kCachedShares = 2;
+
+// Step 1 (before the record's first barrier): thread (w, lane) takes the
+// shares of warp column w in tiles lane, lane + 32, ...; the warp's 8 largest
+// entry values go to sm.wtop[w] (0: none).  The 32nd largest of those 64
+// values is a threshold with at least 32 entries at or above it.
+constexpr int kWarpTop = 8;
+__device__ __forceinline__ void summary_top(const Params& p, RecShared& sm, long long base, int warp, int lane,
+                                            unsigned long long (&cache)[kCachedShares][4]) {
+    uint32_t top[4] = {0u, 0u, 0u, 0u};  // this thread's 4 largest entry values, descending
+    int i = 0;
+    for (int t = lane; t < p.T; t += 32, ++i) {
+        const ulonglong2* q = reinterpret_cast<const ulonglong2*>(p.part_keys + (base + t) * kKeysPerTile + warp * 4);
+        const ulonglong2 a = __ldcg(q), b = __ldcg(q + 1);
+        const unsigned long long e[4] = {a.x, a.y, b.x, b.y};
+        if (i < kCachedShares) {
+#pragma unroll
+            for (int r = 0; r < 4; ++r) cache[i][r] = e[r];
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {  // insert
+            uint32_t v = (uint32_t)(e[r] >> 32);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint32_t hi = v > top[k] ? v : top[k], lo = v > top[k] ? top[k] : v;
+                top[k] = hi;
+                v = lo;
+            }
+        }
     }
-    return r;
+    for (; i < kCachedShares; ++i) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) cache[i][r] = 0ull;
+    }
+    // the warp's 8 largest: knock out the largest head eight times.  A thread
+    // keeps only its own 4 largest; if it held more of the warp's 8, smaller
+    // values are taken instead, still each the value of a distinct entry, so
+    // the count behind the threshold holds.
+#pragma unroll
+    for (int r = 0; r < kWarpTop; ++r) {
+        const uint32_t v = __reduce_max_sync(kFull, top[0]);
+        const unsigned b = __ballot_sync(kFull, top[0] == v);
+        if (lane == __ffs(b) - 1) {
+            top[0] = top[1];
+            top[1] = top[2];
+            top[2] = top[3];
+            top[3] = 0u;
+        }
+        if (lane == r) sm.wtop[warp][r] = v;
+    }
 }
 
-// Steps 2-5, all 256 threads, after warp 0 has set sm.theta_o (0: gather every
-// lane) and sm.lse: candidates, their logprob keys, the top keff, the
-// subtraction-tie check.  Writes the natural pairs into sm.rec.
+// Steps 2-5, all 256 threads, after warp 0 has set sm.theta_o (0: every lane
+// is a candidate) and sm.lse: candidates, their logprob keys, the best keff by
+// rank, the subtraction-tie check.  Writes the natural pairs into sm.rec.
 template <int ELT>
-__device__ __noinline__ void natural_record(const Params& p, RecShared& sm, int row, long long base, int keff) {
-    constexpr int TE = tile_elems<ELT>(), EPV = 16 / ELT;
+__device__ __noinline__ void natural_record(const Params& p, RecShared& sm, int row, long long base, int keff,
+                                            const unsigned long long (&cache)[kCachedShares][4]) {
+    constexpr int TE = tile_elems<ELT>(), EPV = 16 / ELT, NCH = TileLayout<ELT>::NCH;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const float lse = sm.lse;
     const uint32_t th = sm.theta_o;
@@ -1339,7 +1414,7 @@ __device__ __noinline__ void natural_record(const Params& p, RecShared& sm, int 
     const unsigned char* rowp = reinterpret_cast<const unsigned char*>(p.logits) + (long long)row * p.Vp * ELT;
     bool overflow = false;
     if (th == 0u) {
-        // fewer than 32 entries: every lane is a candidate (V is small)
+        // no threshold (a tiny vocabulary): every lane is a candidate
         if (V > kCandKeys) {
             overflow = true;
         } else {
@@ -1348,21 +1423,27 @@ __device__ __noinline__ void natural_record(const Params& p, RecShared& sm, int 
         }
         cbar();
     } else {
-        // 2. candidate threads: entries >= theta, and whole warp shares whose 4th entry reaches it
-        const int shares = p.T * kWarps;
-        for (int sh = tid; sh < shares; sh += kConsumerThreads) {
-            const ulonglong2* q = reinterpret_cast<const ulonglong2*>(p.part_keys + base * kKeysPerTile + (long long)sh * 4);
-            const ulonglong2 a = __ldcg(q), b = __ldcg(q + 1);
-            const unsigned long long e[4] = {a.x, a.y, b.x, b.y};
+        // 2. candidate threads: entries >= theta, and whole shares whose 4th entry reaches it
+        int i = 0;
+        for (int t = lane; t < p.T; t += 32, ++i) {
+            unsigned long long e[4];
+            if (i < kCachedShares) {
+#pragma unroll
+                for (int r = 0; r < 4; ++r) e[r] = cache[i][r];
+            } else {
+                const ulonglong2* q = reinterpret_cast<const ulonglong2*>(p.part_keys + (base + t) * kKeysPerTile + warp * 4);
+                const ulonglong2 a = __ldcg(q), b = __ldcg(q + 1);
+                e[0] = a.x; e[1] = a.y; e[2] = b.x; e[3] = b.y;
+            }
             if (e[3] != 0ull && (uint32_t)(e[3] >> 32) >= th) {
-                const int i = atomicAdd(&sm.n_sh, 1);
-                if (i < kCandShares) sm.csh[i] = (uint32_t)sh;
+                const int k = atomicAdd(&sm.n_sh, 1);
+                if (k < kCandShares) sm.csh[k] = (uint32_t)(t * kWarps + warp);
             } else {
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
                     if (e[r] != 0ull && (uint32_t)(e[r] >> 32) >= th) {
-                        const int i = atomicAdd(&sm.n_thr, 1);
-                        if (i < kCandThreads) sm.cthr[i] = (uint32_t)e[r];
+                        const int k = atomicAdd(&sm.n_thr, 1);
+                        if (k < kCandThreads) sm.cthr[k] = (uint32_t)e[r];
                     }
                 }
             }
@@ -1371,26 +1452,56 @@ __device__ __noinline__ void natural_record(const Params& p, RecShared& sm, int 
         const int nthr = sm.n_thr, nsh = sm.n_sh;
         overflow = nthr > kCandThreads || nsh > kCandShares;
         if (!overflow) {
-            // 3. their vectors, re-read from global memory: keys of the lanes >= theta
-            const int items = (nthr + nsh * 32) * TileLayout<ELT>::NCH;
-            for (int it = tid; it < items; it += kConsumerThreads) {
-                const int c = it % TileLayout<ELT>::NCH, j = it / TileLayout<ELT>::NCH;
-                uint32_t pos;  // tile << 8 | thread
-                if (j < nthr) {
-                    pos = sm.cthr[j];
-                } else {
-                    const uint32_t sh = sm.csh[(j - nthr) >> 5];
-                    pos = ((sh >> 3) << 8) | ((sh & 7u) * 32u + (uint32_t)((j - nthr) & 31));
-                }
-                const long long v0 = (long long)(pos >> 8) * TE + (long long)(c * kConsumerThreads + (int)(pos & 0xFFu)) * EPV;
-                if (v0 >= V) continue;
-                const uint4 x = __ldcs(reinterpret_cast<const uint4*>(rowp + v0 * ELT));
+            // 3. their vectors, re-read from global memory (4 loads in flight per
+            // thread): keys of the lanes >= theta
+            const int items = (nthr + nsh * 32) * NCH;
+            for (int it0 = 0; it0 < items; it0 += 4 * kConsumerThreads) {
+                uint4 x[4];
+                long long v0[4];
 #pragma unroll
-                for (int e = 0; e < EPV; ++e) {
-                    const float y = vec_elem<ELT>(x, e);
-                    if (v0 + e < V && y >= theta) {
-                        const int i = atomicAdd(&sm.n_keys, 1);
-                        if (i < kCandKeys) sm.ckeys[i] = lp_key(y, lse, (uint32_t)(v0 + e));
+                for (int u = 0; u < 4; ++u) {
+                    const int it = it0 + u * kConsumerThreads + tid;
+                    v0[u] = V;
+                    if (it < items) {
+                        const int c = it % NCH, j = it / NCH;
+                        uint32_t pos;  // tile << 8 | thread
+                        if (j < nthr) {
+                            pos = sm.cthr[j];
+                        } else {
+                            const uint32_t sh = sm.csh[(j - nthr) >> 5];
+                            pos = ((sh / kWarps) << 8) | ((sh % kWarps) * 32u + (uint32_t)((j - nthr) & 31));
+                        }
+                        v0[u] = (long long)(pos >> 8) * TE + (long long)(c * kConsumerThreads + (int)(pos & 0xFFu)) * EPV;
+                    }
+                    if (v0[u] < V) x[u] = __ldcs(reinterpret_cast<const uint4*>(rowp + v0[u] * ELT));
+                }
+                // warp-aggregated appends: one shared atomic per warp and round
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    int n = 0;
+                    if (v0[u] < V) {
+#pragma unroll
+                        for (int e = 0; e < EPV; ++e) n += (v0[u] + e < V && vec_elem<ELT>(x[u], e) >= theta) ? 1 : 0;
+                    }
+                    if (!__any_sync(kFull, n > 0)) continue;
+                    int tot = n;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const int q = __shfl_up_sync(kFull, tot, o);
+                        if (lane >= o) tot += q;
+                    }
+                    int k0 = 0;
+                    if (lane == 31) k0 = atomicAdd(&sm.n_keys, tot);
+                    int k = __shfl_sync(kFull, k0, 31) + tot - n;
+                    if (n > 0) {
+#pragma unroll
+                        for (int e = 0; e < EPV; ++e) {
+                            const float y = vec_elem<ELT>(x[u], e);
+                            if (v0[u] + e < V && y >= theta) {
+                                if (k < kCandKeys) sm.ckeys[k] = lp_key(y, lse, (uint32_t)(v0[u] + e));
+                                ++k;
+                            }
+                        }
                     }
                 }
             }
@@ -1402,48 +1513,45 @@ __device__ __noinline__ void natural_record(const Params& p, RecShared& sm, int 
         natural_exact<ELT>(p, sm, row, keff, lse);
         return;
     }
-    // 4. the best 32 keys: each warp runs over chunks of 64, warp 0 merges the 8 lists
+    // 4. the best keff keys by rank (keys are distinct: they carry the id)
     const int nk = sm.n_keys;
-    unsigned long long r = 0ull;
-    for (int q0 = warp * 64; q0 < nk; q0 += kWarps * 64) {
-        const unsigned long long a = q0 + lane < nk ? sm.ckeys[q0 + lane] : 0ull;
-        const unsigned long long b = q0 + 32 + lane < nk ? sm.ckeys[q0 + 32 + lane] : 0ull;
-        r = merge_lists(r, merge_lists(warp_sort_desc(a, lane), warp_sort_desc(b, lane), lane), lane);
-    }
-    sm.lists[warp][lane] = r;
+    for (int j = nk + tid; j < ((nk + 7) & ~7); j += kConsumerThreads) sm.ckeys[j] = 0ull;  // pad to 8
     cbar();
-    if (warp == 0) {
-        const unsigned long long b0 = merge_lists(sm.lists[0][lane], sm.lists[1][lane], lane);
-        const unsigned long long b1 = merge_lists(sm.lists[2][lane], sm.lists[3][lane], lane);
-        const unsigned long long b2 = merge_lists(sm.lists[4][lane], sm.lists[5][lane], lane);
-        const unsigned long long b3 = merge_lists(sm.lists[6][lane], sm.lists[7][lane], lane);
-        const unsigned long long k = merge_lists(merge_lists(b0, b1, lane), merge_lists(b2, b3, lane), lane);
-        // 5. lanes below theta can tie with the K-th logprob only if the float
-        // just below theta already reports it
-        const float L = key_value(__shfl_sync(kFull, k, keff - 1));
-        const bool ties = th != 0u && logprob(nextafterf(theta, kNegInf), lse) == L;
-        const int c_gt = ties ? __popc(__ballot_sync(kFull, k != 0ull && key_value(k) > L)) : keff;
-        if (lane < c_gt) {
-            sm.rec[2 + 2 * lane] = (int)key_id(k);
-            sm.rec[3 + 2 * lane] = (int)__float_as_uint(key_value(k));
+    for (int i = tid; i < nk; i += kConsumerThreads) {
+        const unsigned long long k = sm.ckeys[i];
+        int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+        for (int j = 0; j < nk; j += 8) {
+            const ulonglong2 a = *reinterpret_cast<const ulonglong2*>(&sm.ckeys[j]);
+            const ulonglong2 b = *reinterpret_cast<const ulonglong2*>(&sm.ckeys[j + 2]);
+            const ulonglong2 c = *reinterpret_cast<const ulonglong2*>(&sm.ckeys[j + 4]);
+            const ulonglong2 d = *reinterpret_cast<const ulonglong2*>(&sm.ckeys[j + 6]);
+            r0 += (a.x > k) + (a.y > k);
+            r1 += (b.x > k) + (b.y > k);
+            r2 += (c.x > k) + (c.y > k);
+            r3 += (d.x > k) + (d.y > k);
         }
-        if (ties) {
-            const unsigned lbits = __float_as_uint(L);
-            int got = c_gt;
-            for (long long v0 = 0; v0 < V && got < keff; v0 += 32) {
-                const long long v = v0 + lane;
-                const bool m = v < V && logprob(load_logit<ELT>(p, row, v), lse) == L;
-                const unsigned bb = __ballot_sync(kFull, m);
-                const int before = __popc(bb & ((1u << lane) - 1u));
-                if (m && got + before < keff) {
-                    sm.rec[2 + 2 * (got + before)] = (int)v;
-                    sm.rec[3 + 2 * (got + before)] = (int)lbits;
-                }
-                got += __popc(bb);
-            }
+        const int rank = r0 + r1 + r2 + r3;
+        if (rank < keff) {
+            sm.rec[2 + 2 * rank] = (int)key_id(k);
+            sm.rec[3 + 2 * rank] = (int)__float_as_uint(key_value(k));
+            if (rank == keff - 1) sm.lkey = k;
         }
     }
     cbar();
+    // 5. lanes below theta can tie with the K-th logprob only if the float just
+    // below theta already reports it
+    const float L = key_value(sm.lkey);
+    if (th != 0u && logprob(nextafterf(theta, kNegInf), lse) == L) {
+        if (tid == 0) sm.n_thr = 0;
+        cbar();
+        int gt = 0;
+        for (int i = tid; i < nk; i += kConsumerThreads) gt += key_value(sm.ckeys[i]) > L;
+        gt = (int)__reduce_add_sync(kFull, (unsigned)gt);
+        if (lane == 0 && gt) atomicAdd(&sm.n_thr, gt);
+        cbar();
+        if (warp == 0) fill_equal_lanes<ELT>(p, sm.rec, row, lse, L, sm.n_thr, keff, lane);
+        cbar();
+    }
 }
 
 // Prompt scoring: the largest float X with fl32(X - lse) <= lp, where lp =
@@ -1478,14 +1586,12 @@ __device__ __forceinline__ void ms_merge(float& m, float& s, float m2, float s2)
 
 // Record of a requested, emitted row, built by one CTA of 256 threads: lse from
 // the tile partials, the chosen pair, then the explicit-id gather or the
-// natural alternatives (each warp merges every 8th tile list, warp 0 merges
-// the 8).  Every global load is issued before the first barrier.  SCORE: the
-// prompt-scoring record (rank, 43 words) instead of the 258-word one.
+// natural alternatives.  Every global load is issued before the first barrier.
+// SCORE: the prompt-scoring record (rank, 43 words) instead of the 258-word one.
 template <int ELT, bool SCORE>
-__device__ __noinline__ void record_block(const Params& p, RecShared& sm, int row, int entry, int chosen, int dy,
+__device__ __noinline__ void record_block(const Params& p, RecShared& sm, int row, int g, int chosen, int dy,
                                           int kc) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int g = entry >> 4;
     const int mode = (dy >> 8) & 3, ids = (dy >> 12) & 1;
     const int T = p.T;
     const long long base = (long long)row * T;
@@ -1514,7 +1620,8 @@ __device__ __noinline__ void record_block(const Params& p, RecShared& sm, int ro
         id = __ldg(&p.token_ids[(long long)g * kMaxIds + tid]);
         if (id >= 0 && id < p.V) xi = load_logit<ELT>(p, row, id);
     }
-    if (natural) sm.lists[warp][lane] = summary_top32(p, base, warp, lane);
+    unsigned long long cache[kCachedShares][4];
+    if (natural) summary_top(p, sm, base, warp, lane, cache);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         const float m2 = __shfl_xor_sync(kFull, m, o), s2 = __shfl_xor_sync(kFull, s, o);
@@ -1527,6 +1634,7 @@ __device__ __noinline__ void record_block(const Params& p, RecShared& sm, int ro
     }
     if (tid == 32) sm.xchosen = xc;
     cbar();
+    rtrace(p, kTrRecA, row);
     if (warp == 0) {
         // lse = M + log(sum_t s_t exp(m_t - M)); S >= 1 holds the maximum's own
         // term, so logf(S) is accurate to an ulp of a small number and the sum
@@ -1544,22 +1652,30 @@ __device__ __noinline__ void record_block(const Params& p, RecShared& sm, int ro
                                                       : (int)kUnusedBits;
             if (p.lse_out) p.lse_out[row] = lse;
         }
+        if (natural) {
+            // theta: the 32nd largest of the 8 warps' 8 largest entry values (0:
+            // fewer than 32 entries)
+            const uint32_t* wt = &sm.wtop[0][0];
+            const uint32_t a = wt[lane], b = wt[lane + 32];
+            int ra = 0, rb = 0;  // ranks by (value desc, index asc)
+#pragma unroll 8
+            for (int j = 0; j < 64; ++j) {
+                const uint32_t v = wt[j];
+                ra += v > a || (v == a && j < lane);
+                rb += v > b || (v == b && j < lane + 32);
+            }
+            if (ra == 31) sm.theta_o = a;
+            if (rb == 31) sm.theta_o = b;
+        }
         if constexpr (SCORE) {
             const float lp = logprob(sm.xchosen, lse);
             sm.xlim = lp == lp ? score_limit(sm.xchosen, lse, lp, lane) : sm.xchosen;  // NaN: nothing is above
         }
-        if (natural) {
-            // theta: the row's 32nd largest summary entry (0: fewer than 32 entries)
-            const unsigned long long b0 = merge_lists(sm.lists[0][lane], sm.lists[1][lane], lane);
-            const unsigned long long b1 = merge_lists(sm.lists[2][lane], sm.lists[3][lane], lane);
-            const unsigned long long b2 = merge_lists(sm.lists[4][lane], sm.lists[5][lane], lane);
-            const unsigned long long b3 = merge_lists(sm.lists[6][lane], sm.lists[7][lane], lane);
-            const unsigned long long r = merge_lists(merge_lists(b0, b1, lane), merge_lists(b2, b3, lane), lane);
-            if (lane == 31) sm.theta_o = (uint32_t)(r >> 32);
-        }
     }
     cbar();
-    if (natural) natural_record<ELT>(p, sm, row, base, (long long)kc < p.V ? kc : (int)p.V);
+    rtrace(p, kTrRecB, row);
+    if (natural) natural_record<ELT>(p, sm, row, base, (long long)kc < p.V ? kc : (int)p.V, cache);
+    rtrace(p, kTrRecC, row);
     if (ids && tid < kc) {
         int bits = (int)kUnusedBits;
         if (id >= 0 && id < p.V) {
@@ -1606,18 +1722,23 @@ __device__ __noinline__ void record_block(const Params& p, RecShared& sm, int ro
     cbar();
 }
 
-// Builds the records of the rows the stream kernel flagged (launched after it
+// Builds the records of the rows the stream kernel decided (launched after it
 // with programmatic dependent launch: it waits for the stream grid to finish).
+// The deciders append each record task to a compact list; CTA b takes tasks
+// b, b + grid, ...
 template <int ELT, bool SCORE>
-__global__ void __launch_bounds__(kConsumerThreads) lp_record_kernel(Params p) {
+__global__ void __launch_bounds__(kConsumerThreads, 3) lp_record_kernel(Params p) {
     __shared__ RecShared rs;
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (vload(&p.ctrl->abort) != 0u) return;
     unsigned long long* tr = p.trace != nullptr ? p.trace + ((size_t)p.trace_ctas * 3) * p.trace_cap * 2 : nullptr;
     if (tr != nullptr && threadIdx.x == 0) atomicMin(&tr[4], globaltimer());
-    for (int row = blockIdx.x; row < p.rows; row += gridDim.x) {
-        const int4 t = __ldcg(&p.rec_tasks[row]);  // (chosen, queue entry, descriptor word, count); 0 word: none
-        if (t.z != 0) record_block<ELT, SCORE>(p, rs, row, t.y, t.x, t.z, t.w);
+    const unsigned n = __ldcg(&p.ctrl->rec_count);
+    for (unsigned i = blockIdx.x; i < n; i += gridDim.x) {
+        const int4 t = __ldcg(&p.rec_tasks[i]);  // (chosen, row, descriptor word | count << 16, group)
+        rtrace(p, kTrRecStart, t.y);
+        record_block<ELT, SCORE>(p, rs, t.y, t.w, t.x, t.z & 0xFFFF, t.z >> 16);
+        rtrace(p, kTrRecEnd, t.y);
     }
     if (tr != nullptr && threadIdx.x == 0) atomicMax(&tr[6], globaltimer());
 }
@@ -1685,8 +1806,10 @@ cudaError_t launch_epilogue(const Params& p_in, int dtype, const LaunchCfg& cfg,
         e = score ? cudaLaunchKernelEx(&lc, lp_stream_kernel<4, true>, p) : cudaLaunchKernelEx(&lc, lp_stream_kernel<4, false>, p);
     }
     if (e != cudaSuccess) return e;
-    // records: one CTA per row (rows without a record return at once)
-    int rgrid = p.rows;
+    // records: CTA b builds tasks b, b + grid, ... of the compact task list
+    // (at most one per row); three 256-thread CTAs per SM are resident
+    int rgrid = cfg.sms * 3;
+    if (rgrid > p.rows) rgrid = p.rows;
     if (rgrid < 1) rgrid = 1;
     cudaLaunchConfig_t rc = {};
     rc.gridDim = dim3(rgrid);

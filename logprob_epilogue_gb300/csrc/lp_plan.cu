@@ -504,6 +504,8 @@ int lp_debug_poison_scratch(lp_plan_t plan, void* stream) {
     if (e == cudaSuccess) e = cudaMemsetAsync(plan->part_keys, 0xFF, plan->part_keys_bytes, s);
     // the scoring partials: one int2 per warp of a tile, the size of part_ms
     if (e == cudaSuccess) e = cudaMemsetAsync(plan->part_rank, 0xFF, plan->part_ms_bytes, s);
+    // record tasks past the run's count are never read
+    if (e == cudaSuccess) e = cudaMemsetAsync(plan->rec_tasks, 0xFF, (size_t)plan->d.max_rows * sizeof(int4), s);
     if (e != cudaSuccess) return cuda_fail(e);
     return LP_OK;
 }
