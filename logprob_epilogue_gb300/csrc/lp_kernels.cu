@@ -618,6 +618,9 @@ __global__ void __launch_bounds__(1024) lp_prepare_kernel(Params p) {
                     ids = 1;
                     kc = cnt;
                     mode = kModeLse;
+                    // the record gathers these ids at the end of the run: bring them into L2 now
+                    const int* tp = p.token_ids + (long long)g * kMaxIds;
+                    for (int b = 0; b < cnt; b += 32) asm volatile("prefetch.global.L2 [%0];" ::"l"(tp + b));
                 } else {
                     if ((K < 0 || K > p.k_alt_max) && p.targets == nullptr) {
                         st |= kStatusBadCount;
@@ -1130,7 +1133,8 @@ __device__ __noinline__ bool decide_row(const Params& p, int2* cur) {
     if (req) {  // the record kernel builds it
         if (chosen >= p.V) atomicOr(p.status, kStatusBadToken);
         const unsigned i = atomicAdd(&p.ctrl->rec_count, 1u);
-        p.rec_tasks[i] = make_int4(chosen, row, (d.y & 0xFFFF) | (d.z << 16), g);
+        const int is_amax = (k == 0 && samp >= 0) ? 0 : 1;  // the chosen logit is then the row maximum
+        p.rec_tasks[i] = make_int4(chosen, row, (d.y & 0x3FFF) | (is_amax << 14) | (d.z << 16), g);
     }
     trace(p, kTrDecision, row, accept ? 1 : 0, true);
     if (!accept) {
@@ -1593,6 +1597,7 @@ __device__ __noinline__ void record_block(const Params& p, RecShared& sm, int ro
                                           int kc) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int mode = (dy >> 8) & 3, ids = (dy >> 12) & 1;
+    const bool chosen_is_max = ((dy >> 14) & 1) != 0;  // its logit is the row maximum
     const int T = p.T;
     const long long base = (long long)row * T;
     const bool natural = !ids && mode == kModeNatural && kc > 0;
@@ -1613,7 +1618,7 @@ __device__ __noinline__ void record_block(const Params& p, RecShared& sm, int ro
     }
     if (score) above = (int)__reduce_add_sync(kFull, (unsigned)above);
     float xc = 0.0f;
-    if (tid == 32 && chosen >= 0 && chosen < p.V) xc = load_logit<ELT>(p, row, chosen);
+    if (tid == 32 && !chosen_is_max && chosen >= 0 && chosen < p.V) xc = load_logit<ELT>(p, row, chosen);
     int id = -1;
     float xi = 0.0f;
     if (ids && tid < kc) {
@@ -1645,6 +1650,8 @@ __device__ __noinline__ void record_block(const Params& p, RecShared& sm, int ro
         float lse = 0.0f;
         if (lane == 0) lse = M + logf(S);
         lse = __shfl_sync(kFull, lse, 0);
+        if (chosen_is_max && lane == 0) sm.xchosen = M;
+        __syncwarp();
         if (lane == 0) {
             sm.lse = lse;
             sm.rec[0] = chosen;
@@ -1735,9 +1742,10 @@ __global__ void __launch_bounds__(kConsumerThreads, 3) lp_record_kernel(Params p
     if (tr != nullptr && threadIdx.x == 0) atomicMin(&tr[4], globaltimer());
     const unsigned n = __ldcg(&p.ctrl->rec_count);
     for (unsigned i = blockIdx.x; i < n; i += gridDim.x) {
-        const int4 t = __ldcg(&p.rec_tasks[i]);  // (chosen, row, descriptor word | count << 16, group)
+        // (chosen, row, descriptor word | chosen-is-argmax << 14 | count << 16, group)
+        const int4 t = __ldcg(&p.rec_tasks[i]);
         rtrace(p, kTrRecStart, t.y);
-        record_block<ELT, SCORE>(p, rs, t.y, t.w, t.x, t.z & 0xFFFF, t.z >> 16);
+        record_block<ELT, SCORE>(p, rs, t.y, t.w, t.x, t.z & 0x7FFF, t.z >> 16);
         rtrace(p, kTrRecEnd, t.y);
     }
     if (tr != nullptr && threadIdx.x == 0) atomicMax(&tr[6], globaltimer());
