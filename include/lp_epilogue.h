@@ -55,6 +55,13 @@
  * One plan serves one stream at a time; the plan must outlive queued work.
  * Binds and runs of one plan are not thread-safe.
  *
+ * Residency: the stream kernel is persistent (a few CTAs per multiprocessor)
+ * and its CTAs hand work to one another, but every work item is claimed
+ * through a counter by a CTA that is already running, so a run does not need
+ * the whole GPU: beside another kernel on another stream (or in a parallel
+ * graph branch), the CTAs that are resident do all the work and the others,
+ * when they start, find none.  The run then takes longer; it does not stall.
+ *
  * Errors: every function returns LP_OK (0) or a negative LP_E* code and never
  * aborts.  Conditions only visible on the device are reported in the bound
  * status word (LP_STATUS_* bits), which each lp_run resets to 0 first.
@@ -263,6 +270,12 @@ int lp_debug_poison_scratch(lp_plan_t plan, void* stream);
  * prepare kernel's start and end.  With events == NULL only the geometry is
  * returned.  Synchronises the plan's last stream.  LP_ESTATE without tracing. */
 int lp_debug_trace(lp_plan_t plan, uint64_t* events, uint32_t* counts, int32_t* ctas, int32_t* cap);
+
+/* Debug (tests): launches `ctas` CTAs on `stream` of device `device` that each
+ * hold a whole multiprocessor's shared memory and spin for `ns` nanoseconds
+ * (at most 10 s), then exit: a kernel that keeps part of the GPU busy beside
+ * a run on another stream.  LP_EINVAL for a bad count or duration. */
+int lp_debug_occupy(int32_t device, int32_t ctas, int64_t ns, void* stream);
 
 /* Tiles per row for this plan (ceil(V / tile elements)). */
 int lp_plan_tiles_per_row(lp_plan_t plan);

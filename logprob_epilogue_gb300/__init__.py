@@ -41,7 +41,7 @@ STATIC_SCRATCH_BYTES = 4 << 20  # fixed device scratch of run_static
 # Every symbol include/lp_epilogue.h declares.
 EXPORTS = ("lp_plan_create", "lp_plan_destroy", "lp_plan_scratch_bytes", "lp_bind", "lp_run", "lp_run_host",
            "lp_run_host_bytes", "lp_debug_tiles_read", "lp_debug_poison_scratch", "lp_debug_trace",
-           "lp_plan_tiles_per_row", "lp_run_static", "lp_score", "lp_bind_clip",
+           "lp_plan_tiles_per_row", "lp_run_static", "lp_score", "lp_bind_clip", "lp_debug_occupy",
            "lp_strerror", "lp_last_cuda_error")
 
 
@@ -124,6 +124,7 @@ def lib() -> ctypes.CDLL:
         L.lp_debug_poison_scratch.argtypes = [P, P]
         L.lp_plan_tiles_per_row.argtypes = [P]
         L.lp_debug_trace.argtypes = [P, P, P, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]
+        L.lp_debug_occupy.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, P]
         L.lp_run_static.argtypes = [ctypes.POINTER(PlanDesc), ctypes.POINTER(IO), P]
         L.lp_score.argtypes = [P, ctypes.POINTER(ScoreIO), P]
         L.lp_bind_clip.argtypes = [P, P, P]
@@ -353,6 +354,13 @@ class Plan:
         if stream is None:
             stream = torch.cuda.current_stream(self.device)
         _check(lib().lp_debug_poison_scratch(self._h, ctypes.c_void_p(stream.cuda_stream)), "lp_debug_poison_scratch")
+
+
+def debug_occupy(device: int, ctas: int, ns: int, stream) -> None:
+    """Test hook: ``ctas`` CTAs on ``stream`` that each hold a multiprocessor's
+    shared memory and spin for ``ns`` nanoseconds."""
+    _check(lib().lp_debug_occupy(int(device), int(ctas), int(ns), ctypes.c_void_p(stream.cuda_stream)),
+           "lp_debug_occupy")
 
 
 def run_static(desc: PlanDesc, *, logits, group_indptr, draft_tokens, sampled_tokens, requested, top_k,

@@ -87,7 +87,7 @@ struct Params {
     const void* logits;
     long long V, Vp;      // elements
     int rows, G, T;       // T = tiles per row
-    int stream_grid;      // CTAs of the stream kernel (CTA b takes fresh item b first)
+    int stream_grid;      // CTAs of the stream kernel
     int k_max, k_alt_max, max_ids;
     // inputs
     const int* indptr;
@@ -146,6 +146,8 @@ struct LaunchCfg {
 
 // Enqueue the prepare, stream and record kernels (lp_kernels.cu).
 cudaError_t launch_epilogue(const Params& p, int dtype, const LaunchCfg& cfg, cudaStream_t stream);
+// Test hook: `ctas` CTAs that each hold a multiprocessor's shared memory for `ns`.
+cudaError_t launch_occupy(int ctas, unsigned long long ns, cudaStream_t stream);
 // Occupancy-derived configuration for a dtype on the current device.
 cudaError_t query_launch_cfg(int dtype, LaunchCfg* cfg);
 

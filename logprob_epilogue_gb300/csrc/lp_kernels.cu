@@ -695,8 +695,7 @@ __global__ void __launch_bounds__(1024) lp_prepare_kernel(Params p) {
             e[2] = globaltimer();
             e[3] = (unsigned long long)kTrPrepEnd << 56;
         }
-        // the stream kernel's CTA b takes fresh item b first, without a claim
-        p.ctrl->fresh_next = static_cast<unsigned>(p.stream_grid);
+        p.ctrl->fresh_next = 0u;
         p.ctrl->chain_next = 0u;
         p.ctrl->chain_tail = 0u;
         p.ctrl->fresh_rows = static_cast<unsigned>(s_base);
@@ -733,18 +732,18 @@ __device__ __noinline__ void producer_loop(const Params& p, Shared& sm, unsigned
     const uint64_t npolicy = LP_NATURAL_KEEP ? evict_normal_policy() : policy;
     Ctrl* ctrl = p.ctrl;
     const unsigned T = (unsigned)p.T;
-    // fresh item b is this CTA's first (the counter starts past the grid); its
-    // entry is loaded with the depth-0 row count, and the first chained claim
-    // waits until the first copy is issued
+    // Every item, the first included, is claimed through a counter: a CTA
+    // that is not resident holds no work, so the run never waits for one (the
+    // grid need not be co-resident, e.g. beside another kernel).  The first
+    // chained claim waits until the first copy is issued.
     unsigned chain_claim = kNone;
     unsigned long long ra_e = ~0ull;  // read-ahead candidate: entry of the successor of the last row streamed
     unsigned long long idle_t0 = 0;   // start of the current wait for a chained item (0: not waiting)
-    unsigned fresh_ahead = blockIdx.x;
-    const unsigned first_pos = blockIdx.x / T;
-    unsigned long long fresh_entry = first_pos < (unsigned)p.rows ? vload(&p.queue[first_pos]) : ~0ull;
+    unsigned fresh_ahead = atomicAdd(&ctrl->fresh_next, 1u);
     const unsigned F = vload(&ctrl->fresh_rows);
     const unsigned fresh_items = F * T;
     bool fresh_done = fresh_ahead >= fresh_items;
+    unsigned long long fresh_entry = fresh_done ? ~0ull : vload(&p.queue[fresh_ahead / T]);
     int stage = 0;
     uint32_t phase = 0;
     bool timed_out = false;
@@ -1751,6 +1750,15 @@ __global__ void __launch_bounds__(kConsumerThreads, 3) lp_record_kernel(Params p
     if (tr != nullptr && threadIdx.x == 0) atomicMax(&tr[6], globaltimer());
 }
 
+// Test hook: each CTA holds `smem` bytes of shared memory (so no stream CTA
+// fits beside it) and spins on the global timer for `ns`, then exits.
+__global__ void lp_occupy_kernel(unsigned long long ns) {
+    extern __shared__ unsigned char occ[];
+    const unsigned long long t0 = globaltimer();
+    if (threadIdx.x == 0) occ[0] = 0;
+    while (globaltimer() - t0 < ns) __nanosleep(1000);
+}
+
 template <int ELT>
 constexpr int stream_smem_bytes() {
     return StageCfg<ELT>::kStages * kTileBytes + (int)sizeof(Shared);
@@ -1786,6 +1794,16 @@ cudaError_t query_launch_cfg(int dtype, LaunchCfg* cfg) {
     cfg->grid = sms * (occ > 0 ? occ : 1);
     cfg->sms = sms;
     return cudaSuccess;
+}
+
+cudaError_t launch_occupy(int ctas, unsigned long long ns, cudaStream_t stream) {
+    int dev = 0, smem = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(lp_occupy_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    lp_occupy_kernel<<<ctas, 32, smem, stream>>>(ns);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_epilogue(const Params& p_in, int dtype, const LaunchCfg& cfg, cudaStream_t stream) {

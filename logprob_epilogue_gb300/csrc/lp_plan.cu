@@ -510,6 +510,14 @@ int lp_debug_poison_scratch(lp_plan_t plan, void* stream) {
     return LP_OK;
 }
 
+int lp_debug_occupy(int32_t device, int32_t ctas, int64_t ns, void* stream) {
+    if (ctas < 1 || ns < 0 || ns > 10000000000LL) return LP_EINVAL;
+    DeviceGuard guard(device);
+    if (!guard.ok) return cuda_fail(cudaGetLastError());
+    const cudaError_t e = lp::launch_occupy(ctas, (unsigned long long)ns, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? LP_OK : cuda_fail(e);
+}
+
 int lp_debug_trace(lp_plan_t plan, uint64_t* events, uint32_t* counts, int32_t* ctas, int32_t* cap) {
     if (!plan || !ctas || !cap) return LP_EINVAL;
     if (!plan->trace) return LP_ESTATE;

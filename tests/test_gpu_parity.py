@@ -266,6 +266,29 @@ def test_decisions_stable_over_back_to_back_runs(name):
     assert bad.size == 0, f"{bad.size} of {reps} runs differ from the oracle (first: run {bad[:5].tolist()})"
 
 
+@pytest.mark.parametrize("name", ["spec", "large"])
+def test_run_beside_a_kernel_holding_half_the_gpu(name):
+    # Another kernel, on another stream, holds half the multiprocessors for
+    # 150 ms, longer than the plan's 30 ms limit on every device wait, so the
+    # stream kernel starts with only part of its grid resident.  The resident
+    # CTAs must do all the work: same outputs as the oracle, status 0.
+    import torch
+    import logprob_epilogue_gb300 as lpe
+    w = {"spec": lambda: W.spec(groups=24), "large": lambda: W.large(groups=16)}[name]()
+    dev = torch.device("cuda", 0)
+    d = PT.to_device(w)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    side = torch.cuda.Stream(dev)
+    lpe.debug_occupy(0, sms // 2, 150_000_000, side)
+    gpu, plan = PT.run_gpu(w, plan=PT.make_plan(w, timeout_ns=30_000_000), dev_inputs=d)
+    side.synchronize()
+    orc = PT.run_oracle(w, THREADS)
+    assert gpu["status"] == 0
+    PT.compare(w, gpu, orc)
+    PT.check_tiles(w, orc, gpu["tiles_read"], strict=True)
+    plan.close()
+
+
 def test_malformed_groups_write_nothing():
     x = np.zeros((3, 100), np.float32)
     w = W.custom(x, 100, [2, 1], k_max=0)   # a group of 2 rows with k_max 0
