@@ -552,6 +552,12 @@ __global__ void __launch_bounds__(1024) lp_prepare_kernel(Params p) {
     // this thread's first group: its inputs are in flight while the rows are reset
     GroupIn in0 = {0, 1, 0, 0, 0, 0};
     if (tid < G) in0 = load_group(p, tid);
+    // the deciders read drafts (and EOS tokens) on the verify chains' path:
+    // bring them into L2 now
+    if (p.drafts != nullptr)
+        for (int r = tid * 32; r < p.rows; r += nthr * 32) asm volatile("prefetch.global.L2 [%0];" ::"l"(p.drafts + r));
+    if (p.eos != nullptr)
+        for (int g = tid * 32; g < G; g += nthr * 32) asm volatile("prefetch.global.L2 [%0];" ::"l"(p.eos + g));
     for (int r = tid; r < p.rows; r += nthr) {
         p.done[r] = 0;
         p.queue[r] = ~0ull;
