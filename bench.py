@@ -342,6 +342,56 @@ def bench_score(device: int, peak: float, steps: int = 200, warmup: int = 5) -> 
             "frac": nbytes / m / 1e9 / peak, "rows_read": valid, "dtype": w.dtype}
 
 
+def bench_chain(device: int, peak: float, steps: int = 100, warmup: int = 5) -> dict:
+    """Times stochastic chain verification (lp_chain_verify) of the chain
+    workload: 128 groups x (3 drafts + 1) rows x 248,320 BF16, with FP32 draft
+    laws.  Algorithmic bytes: every row read once for its lse, and the drawn row
+    of each group read again for its weights (logits, plus the draft law when
+    the draw is from the residual), plus the small per-row and per-group
+    vectors."""
+    import torch
+    import logprob_epilogue_gb300 as lpe
+    w = W.chain()
+    dev = torch.device("cuda", device)
+    plan = lpe.Plan(max_rows=w.rows, max_groups=w.groups, k_max=w.k_max, V=w.V, V_padded=w.Vp, dtype=w.dtype,
+                    device=device)
+    ti = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.int32)).to(dev)  # noqa: E731
+    tf = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(dev)  # noqa: E731
+    m = w.meta
+    ins = dict(logits=torch.from_numpy(w.logits.view(np.int16)).view(torch.bfloat16).to(dev),
+               group_indptr=ti(w.group_indptr), draft_tokens=ti(w.draft_tokens), draft_probs=tf(m["draft_probs"]),
+               temperature=tf(m["temperature"]), u=tf(m["u"]), r=tf(m["r"]))
+    outs = dict(accepted=torch.zeros(w.groups, dtype=torch.int32, device=dev),
+                emitted=torch.zeros(w.rows, dtype=torch.int32, device=dev),
+                status=torch.zeros(1, dtype=torch.int32, device=dev))
+    flush = Flusher(dev)
+    stream = torch.cuda.current_stream(dev)
+    for i in range(warmup):
+        flush(i)
+        plan.chain_verify(**ins, **outs, stream=stream)
+    torch.cuda.synchronize(dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush(i)
+        starts[i].record(stream)
+        plan.chain_verify(**ins, **outs, stream=stream)
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    if int(outs["status"].item()) != 0:
+        raise RuntimeError(f"chain verification status {int(outs['status'].item()):#x}")
+    t = statistics.median(a.elapsed_time(b) * 1e-3 for a, b in zip(starts, ends))
+    acc = outs["accepted"].cpu().numpy()
+    k = w.k_max
+    rows_read = int((acc + 1).sum())
+    residual = int((acc < k).sum())
+    nbytes = (rows_read + w.groups) * w.V * 2 + residual * w.V * 4 + w.rows * 16 + w.groups * 16
+    plan.close()
+    return {"rows_per_s": w.rows / t, "us_per_step": t * 1e6, "hbm_gbs": nbytes / t / 1e9,
+            "frac": nbytes / t / 1e9 / peak, "rows_read": rows_read, "dtype": w.dtype,
+            "accepted_mean": float(acc.mean())}
+
+
 def run_e2e(args, w, plan, stream, dev, pg, local, world, accepted):
     """Same metric through lp_run_host: pinned host buffers, H2D and D2H inside the timed region."""
     import torch
@@ -468,8 +518,11 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cores = os.cpu_count() or 1
         v, dt, sample = time_oracle(w, cores)
+        v1, dt1, sample1 = time_oracle(w, 1, min_seconds=2.0, max_passes=1)
         line["cpu_baseline"] = {"value": v, "unit": "rows/s", "cores": cores, "kind": "oracle",
-                                "sample": sample, "seconds": dt}
+                                "sample": sample, "seconds": dt,
+                                "single_thread": {"value": v1, "unit": "rows/s", "cores": 1, "sample": sample1,
+                                                  "seconds": dt1}}
     plan.close()
     del ins, outs
     if rank == 0 and not args.no_per_workload:
@@ -497,6 +550,7 @@ def main():
             p2.close()
             del i2, o2, fl2
         per["prompt_score"] = bench_score(local, peak)
+        per["chain"] = bench_chain(local, peak)
         line["per_workload"] = per
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -104,6 +104,7 @@ enum {
 #define LP_STATUS_BAD_COUNT 0x4u /* id count outside [0, max_ids] or top_k outside [0, k_alt_max]: clamped */
 #define LP_STATUS_BAD_GROUP 0x8u /* group_indptr malformed: the run reads and writes nothing else */
 #define LP_STATUS_TIMEOUT 0x10u  /* a bounded device wait expired: outputs are incomplete */
+#define LP_STATUS_BAD_TEMPERATURE 0x20u /* lp_chain_verify: a temperature not in (0, inf): group skipped */
 
 /* Plan flags. */
 #define LP_PLAN_HOST_STAGING 0x1u     /* also allocate device staging so lp_run_host can be used */
@@ -250,6 +251,63 @@ typedef struct {
 } lp_score_io;
 
 int lp_score(lp_plan_t plan, const lp_score_io* io, void* stream);
+
+/* ---- Stochastic chain verification ----
+ *
+ * Source: "mtp-design.md", section "Sampling correctness".  A draft drawn
+ * from the draft law q is accepted with probability min(1, p/q); at the first
+ * rejection the next token is drawn from the positive residual max(p - q, 0),
+ * normalised; after every draft is accepted the bonus token is drawn from the
+ * target law of the bonus row.  For row j of group g (groups as in lp_bind:
+ * rows r0..r0+k-1 carry drafts, row r0+k is the bonus row):
+ *   p_j(v) = exp(x_j(v)/t - lse(x_j/t)) over the V unpadded lanes, t = temperature[g],
+ *            with lse accumulated in FP32;
+ *   draft j is accepted iff u[r0+j] * q_j(d_j) < p_j(d_j) (FP32), i.e. u < p/q;
+ *   a = the number of leading accepted drafts;
+ *   the last token is the smallest id v whose running sum of weights (ids in
+ *   ascending order, FP64 sums of FP32 weights) exceeds r[g] times their
+ *   total; the weights are max(p_a - q_a, 0) when a < k (p_a if that residual
+ *   has no mass) and p_k when a == k.
+ * The random numbers are inputs, so any generator (e.g. a counter-based
+ * stream of the caller) can drive it.  Rows past a group's emitted prefix are
+ * not read.  The plan's V, V_padded, dtype, k_max and device apply; its scratch
+ * is not used.
+ *
+ *   logits        [rows, V_padded] of the plan's dtype (device)
+ *   group_indptr  int32 [groups + 1]; group sizes 1..k_max + 1
+ *   draft_tokens  int32 [rows]; row r0+j carries d_j (j < k)
+ *   draft_probs   float [rows, V_padded]; row r0+j is q_j, the law that drew d_j
+ *                 (16-byte aligned; rows r0+k are not read)
+ *   temperature   float [groups] (> 0)
+ *   u             float [rows] in [0, 1): acceptance uniforms of the draft rows
+ *   r             float [groups] in [0, 1): the draw uniform of each group
+ *   accepted      int32 [groups] (output: a; -1 for a skipped group)
+ *   emitted       int32 [rows] (output: d_j for j < a, the drawn token at
+ *                 j = a, -1 after)
+ *   lse_out       float [rows] or NULL (output: lse(x_j/t) of every row read)
+ *   status        uint32 [1] (output: reset, then LP_STATUS_* bits:
+ *                 BAD_GROUP for a malformed group (skipped, accepted -1),
+ *                 BAD_TEMPERATURE (skipped, accepted and emitted -1), BAD_TOKEN
+ *                 for a draft >= V (rejected))
+ * Host errors as for lp_bind (LP_EALIGN: logits or draft_probs not 16-byte
+ * aligned).  Enqueues only; no allocation. */
+typedef struct {
+    const void* logits;
+    const int32_t* group_indptr;
+    const int32_t* draft_tokens;
+    const float* draft_probs;
+    const float* temperature;
+    const float* u;
+    const float* r;
+    int32_t* accepted;
+    int32_t* emitted;
+    float* lse_out;
+    uint32_t* status;
+    int32_t rows;
+    int32_t groups;
+} lp_chain_io;
+
+int lp_chain_verify(lp_plan_t plan, const lp_chain_io* io, void* stream);
 
 /* Debug: number of vocabulary tiles the last run read for each row (0 = the
  * row was never read), copied into host_tiles[0..rows).  With

@@ -42,6 +42,7 @@ STATIC_SCRATCH_BYTES = 4 << 20  # fixed device scratch of run_static
 EXPORTS = ("lp_plan_create", "lp_plan_destroy", "lp_plan_scratch_bytes", "lp_bind", "lp_run", "lp_run_host",
            "lp_run_host_bytes", "lp_debug_tiles_read", "lp_debug_poison_scratch", "lp_debug_trace",
            "lp_plan_tiles_per_row", "lp_run_static", "lp_score", "lp_bind_clip", "lp_debug_occupy",
+           "lp_chain_verify",
            "lp_strerror", "lp_last_cuda_error")
 
 
@@ -92,6 +93,24 @@ class ScoreIO(ctypes.Structure):
     ]
 
 
+class ChainIO(ctypes.Structure):
+    _fields_ = [
+        ("logits", ctypes.c_void_p),
+        ("group_indptr", ctypes.c_void_p),
+        ("draft_tokens", ctypes.c_void_p),
+        ("draft_probs", ctypes.c_void_p),
+        ("temperature", ctypes.c_void_p),
+        ("u", ctypes.c_void_p),
+        ("r", ctypes.c_void_p),
+        ("accepted", ctypes.c_void_p),
+        ("emitted", ctypes.c_void_p),
+        ("lse_out", ctypes.c_void_p),
+        ("status", ctypes.c_void_p),
+        ("rows", ctypes.c_int32),
+        ("groups", ctypes.c_int32),
+    ]
+
+
 _lib = None
 
 
@@ -125,6 +144,7 @@ def lib() -> ctypes.CDLL:
         L.lp_plan_tiles_per_row.argtypes = [P]
         L.lp_debug_trace.argtypes = [P, P, P, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]
         L.lp_debug_occupy.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, P]
+        L.lp_chain_verify.argtypes = [P, ctypes.POINTER(ChainIO), P]
         L.lp_run_static.argtypes = [ctypes.POINTER(PlanDesc), ctypes.POINTER(IO), P]
         L.lp_score.argtypes = [P, ctypes.POINTER(ScoreIO), P]
         L.lp_bind_clip.argtypes = [P, P, P]
@@ -297,6 +317,51 @@ class Plan:
         handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
         self._keep_score = t
         _check(lib().lp_score(self._h, ctypes.byref(io), ctypes.c_void_p(handle)), "lp_score")
+
+    def chain_verify(self, *, logits, group_indptr, draft_tokens, draft_probs, temperature, u, r, accepted,
+                     emitted, status, lse_out=None, stream=None) -> None:
+        """Enqueues stochastic chain verification: for each group, drafts
+        accepted with probability min(1, p/q), the residual or bonus token drawn
+        with the group's uniform r.  ``draft_probs`` is float32 [rows, V_padded]
+        (the law that drew each draft), ``temperature`` and ``r`` float32
+        [groups], ``u`` float32 [rows]; outputs ``accepted`` int32 [groups],
+        ``emitted`` int32 [rows], optional ``lse_out`` float32 [rows] (lse of
+        x / t).  The bound tensors are not used."""
+        import torch
+        want_logit = torch.bfloat16 if self.dtype == "bf16" else torch.float32
+        t = dict(logits=logits, group_indptr=group_indptr, draft_tokens=draft_tokens, draft_probs=draft_probs,
+                 temperature=temperature, u=u, r=r, accepted=accepted, emitted=emitted, status=status,
+                 lse_out=lse_out)
+        for name, x in t.items():
+            if x is None:
+                continue
+            if not isinstance(x, torch.Tensor) or not x.is_cuda or x.device.index != self.device:
+                raise ValueError(f"{name}: expected a CUDA tensor on device {self.device}")
+            if not x.is_contiguous():
+                raise ValueError(f"{name}: must be contiguous")
+        if logits.dtype != want_logit or logits.dim() != 2 or logits.shape[1] != self.desc.V_padded:
+            raise ValueError(f"logits: expected {want_logit} [rows, {self.desc.V_padded}]")
+        rows, groups = int(logits.shape[0]), int(group_indptr.numel()) - 1
+        if draft_probs.dtype != torch.float32 or tuple(draft_probs.shape) != tuple(logits.shape):
+            raise ValueError("draft_probs: expected float32 of the logits' shape")
+        for name in ("group_indptr", "draft_tokens", "accepted", "emitted"):
+            if t[name].dtype != torch.int32:
+                raise ValueError(f"{name}: expected int32")
+        for name in ("temperature", "u", "r"):
+            if t[name].dtype != torch.float32:
+                raise ValueError(f"{name}: expected float32")
+        if draft_tokens.numel() < rows or u.numel() < rows or emitted.numel() < rows:
+            raise ValueError("draft_tokens, u, emitted: expected [rows]")
+        if temperature.numel() < groups or r.numel() < groups or accepted.numel() < groups:
+            raise ValueError("temperature, r, accepted: expected [groups]")
+        io = ChainIO(logits.data_ptr(), group_indptr.data_ptr(), draft_tokens.data_ptr(), draft_probs.data_ptr(),
+                     temperature.data_ptr(), u.data_ptr(), r.data_ptr(), accepted.data_ptr(), emitted.data_ptr(),
+                     None if lse_out is None else lse_out.data_ptr(), status.data_ptr(), rows, groups)
+        if stream is None:
+            stream = torch.cuda.current_stream(self.device)
+        handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+        self._keep_chain = t
+        _check(lib().lp_chain_verify(self._h, ctypes.byref(io), ctypes.c_void_p(handle)), "lp_chain_verify")
 
     def host_io(self, arrays: dict) -> IO:
         rows = int(arrays["logits"].shape[0])

@@ -11,7 +11,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "liblp_epilogue.so")
-SOURCES = ["lp_plan.cu", "lp_kernels.cu"]
+SOURCES = ["lp_plan.cu", "lp_kernels.cu", "lp_chain.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 # Optional extra nvcc flags (e.g. -DLP_BF16_CTAS=2) for tuning builds.

@@ -138,6 +138,23 @@ struct Params {
     int trace_ctas;
 };
 
+// Stochastic chain verification (lp_chain.cu).
+struct ChainParams {
+    const void* logits;   // [rows, Vp] of the plan's dtype
+    long long V, Vp;
+    int rows, G, k_max;
+    const int* indptr;    // [G + 1]
+    const int* drafts;    // [rows]
+    const float* q;       // [rows, Vp] draft laws (FP32)
+    const float* temp;    // [G]
+    const float* u;       // [rows] acceptance uniforms
+    const float* r;       // [G] draw uniforms
+    int* accepted;        // [G]
+    int* emitted;         // [rows]
+    float* lse_out;       // [rows] or null: lse(x / t) of the rows read
+    unsigned int* status;
+};
+
 struct LaunchCfg {
     int grid;           // persistent CTAs
     int smem_bytes;     // dynamic shared memory of the stream kernel
@@ -146,6 +163,8 @@ struct LaunchCfg {
 
 // Enqueue the prepare, stream and record kernels (lp_kernels.cu).
 cudaError_t launch_epilogue(const Params& p, int dtype, const LaunchCfg& cfg, cudaStream_t stream);
+// Enqueue stochastic chain verification (one 1024-thread CTA per group at a time).
+cudaError_t launch_chain(const ChainParams& p, int dtype, int sms, cudaStream_t stream);
 // Test hook: `ctas` CTAs that each hold a multiprocessor's shared memory for `ns`.
 cudaError_t launch_occupy(int ctas, unsigned long long ns, cudaStream_t stream);
 // Occupancy-derived configuration for a dtype on the current device.

@@ -486,6 +486,49 @@ int lp_score(lp_plan_t plan, const lp_score_io* io, void* stream) {
     return LP_OK;
 }
 
+int lp_chain_verify(lp_plan_t plan, const lp_chain_io* io, void* stream) {
+    if (!plan || !io) return LP_EINVAL;
+    if (io->rows < 0 || io->groups < 0) return LP_ESHAPE;
+    if (io->rows > plan->d.max_rows || io->groups > plan->d.max_groups) return LP_ESHAPE;
+    if (!io->status) return LP_EINVAL;
+    if (io->groups > 0 && (!io->logits || !io->group_indptr || !io->draft_tokens || !io->draft_probs ||
+                           !io->temperature || !io->u || !io->r || !io->accepted || !io->emitted))
+        return LP_EINVAL;
+    if (!aligned(io->logits, 16) || !aligned(io->draft_probs, 16)) return LP_EALIGN;
+    const void* w4[] = {io->group_indptr, io->draft_tokens, io->temperature, io->u, io->r, io->accepted,
+                        io->emitted, io->status};
+    for (const void* q : w4)
+        if (!aligned(q, 4)) return LP_EALIGN;
+    if (io->lse_out && !aligned(io->lse_out, 4)) return LP_EALIGN;
+    DeviceGuard guard(plan->d.device);
+    if (!guard.ok) return cuda_fail(cudaGetLastError());
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(io->status, 0, sizeof(uint32_t), s);
+    if (e == cudaSuccess && io->groups > 0) {
+        lp::ChainParams c{};
+        c.logits = io->logits;
+        c.V = plan->d.V;
+        c.Vp = plan->d.V_padded;
+        c.rows = io->rows;
+        c.G = io->groups;
+        c.k_max = plan->d.k_max;
+        c.indptr = io->group_indptr;
+        c.drafts = io->draft_tokens;
+        c.q = io->draft_probs;
+        c.temp = io->temperature;
+        c.u = io->u;
+        c.r = io->r;
+        c.accepted = io->accepted;
+        c.emitted = io->emitted;
+        c.lse_out = io->lse_out;
+        c.status = io->status;
+        e = lp::launch_chain(c, plan->d.dtype, plan->cfg.sms, s);
+    }
+    if (e != cudaSuccess) return cuda_fail(e);
+    plan->last_stream = s;
+    return LP_OK;
+}
+
 int lp_debug_tiles_read(lp_plan_t plan, int32_t* host_tiles, int32_t rows) {
     if (!plan || !host_tiles || rows < 0 || rows > plan->d.max_rows) return LP_EINVAL;
     DeviceGuard guard(plan->d.device);

@@ -338,9 +338,44 @@ def commit_clip(w: Workload, seed: int):
     return eos, budgets
 
 
+def chain(seed: int = 6, groups: int = 128, k: int = 3, V: int = 248_320, Vp: int = 248_448,
+          dtype: str = "bf16", hot: int = 12) -> Workload:
+    """Stochastic chain verification inputs: groups of k drafts + 1 bonus row.
+
+    Each row has a small hot set of `hot` seed-drawn ids.  Its logits are N(0,1),
+    N(6,1) on the hot set; its draft law q is a Dirichlet(0.3) draw over the
+    hot set (zero elsewhere) mixed with 1% of uniform mass, and the row's draft
+    is drawn from q.  Temperatures are U[0.6, 1.4] per group; u (per row) and
+    r (per group) are U[0, 1).  Pad lanes hold +1e30 (logits) and 0 (q).
+    In meta: draft_probs float32 [rows, Vp], temperature, u, r."""
+    rng = np.random.default_rng(seed)
+    rows = groups * (k + 1)
+    vals = np.full((rows, Vp), np.float32(PAD_VALUE), np.float32)
+    vals[:, :V] = rng.standard_normal((rows, V), dtype=np.float32)
+    q = np.zeros((rows, Vp), np.float32)
+    drafts = np.full(rows, -1, np.int32)
+    for r in range(rows):
+        ids = rng.choice(V, size=min(hot, V), replace=False)
+        vals[r, ids] += np.float32(6.0)
+        law = np.full(V, 0.01 / V)
+        law[ids] += 0.99 * rng.dirichlet(np.full(ids.size, 0.3))
+        law /= law.sum()
+        q[r, :V] = law.astype(np.float32)
+        if r % (k + 1) != k:
+            drafts[r] = int(rng.choice(V, p=law))
+    gi = (np.arange(groups + 1) * (k + 1)).astype(np.int32)
+    G = groups
+    meta = {"draft_probs": q, "temperature": rng.uniform(0.6, 1.4, G).astype(np.float32),
+            "u": rng.random(rows, dtype=np.float32), "r": rng.random(G, dtype=np.float32)}
+    logits = bf16_bits(vals) if dtype == "bf16" else vals
+    return Workload("chain", dtype, V, Vp, k, logits, gi, drafts, np.full(G, -1, np.int32), np.zeros(G, np.int32),
+                    np.zeros(G, np.int32), np.full((G, MAX_IDS), -1, np.int32), np.zeros(G, np.int32),
+                    np.full(rows, -1, np.int32), meta)
+
+
 def make(name: str, **kw) -> Workload:
     return {"tiny": tiny, "decode": decode, "spec": spec, "large": large, "wide": wide,
-            "prompt": prompt}[name](**kw)
+            "prompt": prompt, "chain": chain}[name](**kw)
 
 
 def custom(rows_f32: np.ndarray, V: int, group_sizes, *, dtype: str = "f32", Vp: int | None = None,
