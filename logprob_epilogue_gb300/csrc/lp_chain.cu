@@ -10,7 +10,7 @@
 // (accept iff u * q(d) < p(d)) and r per group (the draw: the smallest id v
 // whose running sum of weights, in id order, exceeds r times the total).
 //
-// One CTA of 1024 threads walks a group's chain, one row at a time (the rows
+// One CTA of 512 threads walks a group's chain, one row at a time (the rows
 // of a group are dependent).  CTA b takes groups b, b + grid, ...  Per row:
 //   pass 1  the row's temperature-scaled maximum and exp-sum (FP32, base 2:
 //           a = x * log2(e) / t, L = log2 sum 2^a), 16-byte loads, each warp
@@ -18,7 +18,7 @@
 //   accept  u * q(d) < 2^(a_d - L) with the draft's logit and q gathered;
 //   draw    (first rejection, or the bonus row) pass 2 sums the weights in
 //           FP64 per warp range (the residual max(p - q, 0) in FP32, or p);
-//           the range holding r * total is split over the 1024 threads, an
+//           the range holding r * total is split over the 512 threads, an
 //           FP64 block scan of their sums finds the thread, and that thread
 //           walks its few lanes.  A residual without mass (possible only
 //           through rounding) falls back to p.
@@ -37,8 +37,9 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kNegInf = -__builtin_huge_valf();
 constexpr unsigned kStatusBadToken = 0x2u, kStatusBadGroup = 0x8u, kStatusBadTemperature = 0x20u;
-constexpr int kChainThreads = 1024;
+constexpr int kChainThreads = 512;
 constexpr int kChainWarps = kChainThreads / 32;
+constexpr int kUnroll = 4;  // 16-byte loads in flight per lane in the row passes
 
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -154,18 +155,27 @@ __global__ void __launch_bounds__(kChainThreads, 1) lp_chain_kernel(ChainParams 
             const void* xr = reinterpret_cast<const unsigned char*>(p.logits) + row * p.Vp * ELT;
             // pass 1: max and exp-sum of a = x * scale over the row
             float m = kNegInf, s = 0.0f;
-            for (long long v0 = w0 + lane * 8; v0 < w1; v0 += 32 * 8) {
-                float x[8];
-                load8<ELT>(xr, v0, V, x);
-                float vm = kNegInf;
+            for (long long vb = w0 + lane * 8; vb < w1; vb += kUnroll * 32 * 8) {
+                float x[kUnroll][8];  // kUnroll loads in flight per lane
 #pragma unroll
-                for (int e = 0; e < 8; ++e) vm = (v0 + e < V) ? fmaxf(vm, x[e] * scale) : vm;
-                if (vm > m) {
-                    s = (m > kNegInf) ? s * ex2(m - vm) : 0.0f;
-                    m = vm;
+                for (int i = 0; i < kUnroll; ++i) {
+                    const long long v0 = vb + (long long)i * 32 * 8;
+                    if (v0 < w1) load8<ELT>(xr, v0, V, x[i]);
                 }
 #pragma unroll
-                for (int e = 0; e < 8; ++e) s += (v0 + e < V && m > kNegInf) ? ex2(x[e] * scale - m) : 0.0f;
+                for (int i = 0; i < kUnroll; ++i) {
+                    const long long v0 = vb + (long long)i * 32 * 8;
+                    if (v0 >= w1) continue;
+                    float vm = kNegInf;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) vm = (v0 + e < V) ? fmaxf(vm, x[i][e] * scale) : vm;
+                    if (vm > m) {
+                        s = (m > kNegInf) ? s * ex2(m - vm) : 0.0f;
+                        m = vm;
+                    }
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) s += (v0 + e < V && m > kNegInf) ? ex2(x[i][e] * scale - m) : 0.0f;
+                }
             }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) ms2_merge(m, s, __shfl_xor_sync(kFull, m, o), __shfl_xor_sync(kFull, s, o));
@@ -209,15 +219,27 @@ __global__ void __launch_bounds__(kChainThreads, 1) lp_chain_kernel(ChainParams 
             // the draw: pass 2, FP64 weight totals of the warp ranges
             for (int attempt = 0; attempt < 2; ++attempt) {
                 double acc = 0.0;
-                for (long long v0 = w0 + lane * 8; v0 < w1; v0 += 32 * 8) {
-                    float x[8], qv[8];
-                    load8<ELT>(xr, v0, V, x);
-                    if (residual) loadq8(qr, v0, V, qv);
-                    float part = 0.0f;
+                for (long long vb = w0 + lane * 8; vb < w1; vb += kUnroll * 32 * 8) {
+                    float x[kUnroll][8], qv[kUnroll][8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        part += (v0 + e < V) ? weight(x[e] * scale, L, residual ? qv[e] : 0.0f, residual) : 0.0f;
-                    acc += (double)part;
+                    for (int i = 0; i < kUnroll; ++i) {
+                        const long long v0 = vb + (long long)i * 32 * 8;
+                        if (v0 < w1) {
+                            load8<ELT>(xr, v0, V, x[i]);
+                            if (residual) loadq8(qr, v0, V, qv[i]);
+                        }
+                    }
+#pragma unroll
+                    for (int i = 0; i < kUnroll; ++i) {
+                        const long long v0 = vb + (long long)i * 32 * 8;
+                        if (v0 >= w1) continue;
+                        float part = 0.0f;
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            part += (v0 + e < V) ? weight(x[i][e] * scale, L, residual ? qv[i][e] : 0.0f, residual)
+                                                 : 0.0f;
+                        acc += (double)part;
+                    }
                 }
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(kFull, acc, o);
@@ -253,7 +275,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) lp_chain_kernel(ChainParams 
                 residual = false;  // a residual without mass (rounding): draw from p
                 __syncthreads();
             }
-            // level 2: the range split over the 1024 threads (contiguous sub-ranges)
+            // level 2: the range split over the CTA's threads (contiguous sub-ranges)
             const int rw = sm.range;
             const double target = sm.before;
             const long long g0 = (long long)rw * R, g1 = (g0 + R < V) ? g0 + R : V;

@@ -163,7 +163,7 @@ struct LaunchCfg {
 
 // Enqueue the prepare, stream and record kernels (lp_kernels.cu).
 cudaError_t launch_epilogue(const Params& p, int dtype, const LaunchCfg& cfg, cudaStream_t stream);
-// Enqueue stochastic chain verification (one 1024-thread CTA per group at a time).
+// Enqueue stochastic chain verification (one 512-thread CTA per group at a time).
 cudaError_t launch_chain(const ChainParams& p, int dtype, int sms, cudaStream_t stream);
 // Test hook: `ctas` CTAs that each hold a multiprocessor's shared memory for `ns`.
 cudaError_t launch_occupy(int ctas, unsigned long long ns, cudaStream_t stream);

@@ -343,7 +343,8 @@ def chain(seed: int = 6, groups: int = 128, k: int = 3, V: int = 248_320, Vp: in
     """Stochastic chain verification inputs: groups of k drafts + 1 bonus row.
 
     Each row has a small hot set of `hot` seed-drawn ids.  Its logits are N(0,1),
-    N(6,1) on the hot set; its draft law q is a Dirichlet(0.3) draw over the
+    N(16,1) on the hot set (so that most of the target law's mass is there, as
+    when a draft model agrees with the target); its draft law q is a Dirichlet(0.3) draw over the
     hot set (zero elsewhere) mixed with 1% of uniform mass, and the row's draft
     is drawn from q.  Temperatures are U[0.6, 1.4] per group; u (per row) and
     r (per group) are U[0, 1).  Pad lanes hold +1e30 (logits) and 0 (q).
@@ -356,7 +357,7 @@ def chain(seed: int = 6, groups: int = 128, k: int = 3, V: int = 248_320, Vp: in
     drafts = np.full(rows, -1, np.int32)
     for r in range(rows):
         ids = rng.choice(V, size=min(hot, V), replace=False)
-        vals[r, ids] += np.float32(6.0)
+        vals[r, ids] += np.float32(16.0)
         law = np.full(V, 0.01 / V)
         law[ids] += 0.99 * rng.dirichlet(np.full(ids.size, 0.3))
         law /= law.sum()
