@@ -109,6 +109,7 @@ enum {
 /* Plan flags. */
 #define LP_PLAN_HOST_STAGING 0x1u     /* also allocate device staging so lp_run_host can be used */
 #define LP_PLAN_READ_AHEAD 0x2u       /* idle producers may read the row after one being decided */
+#define LP_PLAN_VOCAB_SHARDS 0x4u     /* also allocate the exchange buffers of lp_run_sharded */
 #define LP_PLAN_DEBUG_FORCE_TIMEOUT 0x100u /* test hook: every bounded wait runs out (no reads) */
 #define LP_PLAN_DEBUG_TRACE 0x200u    /* record a device timeline of each run (see lp_debug_trace) */
 
@@ -251,6 +252,31 @@ typedef struct {
 } lp_score_io;
 
 int lp_score(lp_plan_t plan, const lp_score_io* io, void* stream);
+
+/* ---- Vocabulary-sharded records ----
+ *
+ * Source: "logprobs-design.md", the vocabulary-sharded speculative
+ * verification paragraph.  Each rank holds a vocabulary shard of the target
+ * logits.  A first exchange carries each shard's maximum and exponential mass
+ * (the global normalisation); a second carries the chosen token's raw logit
+ * from its owning rank and either the shard's best 32 sort keys or the selected
+ * ids' raw logits, 256 words per position per rank; a final merge writes the
+ * same packed record.
+ *
+ * lp_run_sharded runs the bound epilogue (as lp_run, same outputs) with the
+ * records built that way over `shards` vocabulary shards of one block on one
+ * GPU: shard s of a row is the column range of tiles [s*T/S, (s+1)*T/S) (T =
+ * lp_plan_tiles_per_row).  Acceptance is decided first, as verification does
+ * before the reduction.  Each shard's part touches only its own columns and
+ * its own slot of two exchange buffers (plan memory, allocated at creation
+ * with LP_PLAN_VOCAB_SHARDS: 8 + 1,024 bytes per row per shard for up to 8
+ * shards); the gathers are the buffers read by the next launch.  Natural
+ * alternatives are exact: each shard's 32 keys are its best 32 by (logprob
+ * desc, id asc) under the global normalisation, so the merged K <= 32 are the
+ * row's.  lse may differ from lp_run's in its last bit (another summation
+ * order).  LP_ESTATE without LP_PLAN_VOCAB_SHARDS or a bind; LP_EINVAL unless
+ * 1 <= shards <= min(8, T).  Enqueues only. */
+int lp_run_sharded(lp_plan_t plan, int32_t shards, void* stream);
 
 /* ---- Stochastic chain verification ----
  *

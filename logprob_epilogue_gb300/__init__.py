@@ -31,6 +31,7 @@ STATUS_BAD_GROUP = 0x8
 STATUS_TIMEOUT = 0x10
 PLAN_HOST_STAGING = 0x1
 PLAN_READ_AHEAD = 0x2
+PLAN_VOCAB_SHARDS = 0x4
 PLAN_DEBUG_FORCE_TIMEOUT = 0x100
 PLAN_DEBUG_TRACE = 0x200
 
@@ -42,7 +43,7 @@ STATIC_SCRATCH_BYTES = 4 << 20  # fixed device scratch of run_static
 EXPORTS = ("lp_plan_create", "lp_plan_destroy", "lp_plan_scratch_bytes", "lp_bind", "lp_run", "lp_run_host",
            "lp_run_host_bytes", "lp_debug_tiles_read", "lp_debug_poison_scratch", "lp_debug_trace",
            "lp_plan_tiles_per_row", "lp_run_static", "lp_score", "lp_bind_clip", "lp_debug_occupy",
-           "lp_chain_verify",
+           "lp_chain_verify", "lp_run_sharded",
            "lp_strerror", "lp_last_cuda_error")
 
 
@@ -145,6 +146,7 @@ def lib() -> ctypes.CDLL:
         L.lp_debug_trace.argtypes = [P, P, P, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]
         L.lp_debug_occupy.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, P]
         L.lp_chain_verify.argtypes = [P, ctypes.POINTER(ChainIO), P]
+        L.lp_run_sharded.argtypes = [P, ctypes.c_int32, P]
         L.lp_run_static.argtypes = [ctypes.POINTER(PlanDesc), ctypes.POINTER(IO), P]
         L.lp_score.argtypes = [P, ctypes.POINTER(ScoreIO), P]
         L.lp_bind_clip.argtypes = [P, P, P]
@@ -165,9 +167,10 @@ def _check(rc: int, what: str) -> None:
 
 def make_desc(*, max_rows, max_groups, k_max, V, V_padded=None, dtype="bf16", k_alt_max=20, max_ids=128,
               device=0, host_staging=False, timeout_ns=0, debug_force_timeout=False, trace=False,
-              read_ahead=False) -> PlanDesc:
+              read_ahead=False, vocab_shards=False) -> PlanDesc:
     flags = (PLAN_HOST_STAGING if host_staging else 0) | (PLAN_DEBUG_FORCE_TIMEOUT if debug_force_timeout else 0)
     flags |= (PLAN_DEBUG_TRACE if trace else 0) | (PLAN_READ_AHEAD if read_ahead else 0)
+    flags |= PLAN_VOCAB_SHARDS if vocab_shards else 0
     return PlanDesc(int(max_rows), int(max_groups), int(k_max), int(V), int(V if V_padded is None else V_padded),
                     LP_BF16 if dtype == "bf16" else (LP_F32 if dtype == "f32" else 99), int(k_alt_max),
                     int(max_ids), int(device), flags, int(timeout_ns))
@@ -282,6 +285,15 @@ class Plan:
             stream = torch.cuda.current_stream(self.device)
         handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
         _check(lib().lp_run(self._h, ctypes.c_void_p(handle)), "lp_run")
+
+    def run_sharded(self, shards: int, stream=None) -> None:
+        """Enqueues the bound epilogue with the records built over ``shards``
+        vocabulary shards (plan created with ``vocab_shards=True``)."""
+        import torch
+        if stream is None:
+            stream = torch.cuda.current_stream(self.device)
+        handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+        _check(lib().lp_run_sharded(self._h, int(shards), ctypes.c_void_p(handle)), "lp_run_sharded")
 
     def score(self, *, logits, target_tokens, records, status, lse_out=None, stream=None) -> None:
         """Enqueues prompt scoring of ``target_tokens`` (int32 [rows]) against

@@ -18,6 +18,8 @@ constexpr int kRecordWords = 258;
 constexpr int kScoreWords = 43;        // prompt-scoring record: id, lp bits, rank, 20 pairs
 constexpr int kScoreAlts = 20;
 constexpr int kMaxIds = 128;
+constexpr int kMaxShards = 8;          // vocabulary shards of lp_run_sharded
+constexpr int kShardWords = 256;       // exchange-2 words per position per shard
 
 // Pipeline stages per CTA and CTAs per SM, per element type: three CTAs of two
 // 32 KiB stages fill the SM's shared memory and give 24 compute warps per SM.
@@ -87,6 +89,7 @@ struct Params {
     const void* logits;
     long long V, Vp;      // elements
     int rows, G, T;       // T = tiles per row
+    int elt;              // bytes per logit (2 or 4)
     int stream_grid;      // CTAs of the stream kernel
     int k_max, k_alt_max, max_ids;
     // inputs
@@ -161,8 +164,14 @@ struct LaunchCfg {
     int sms;            // multiprocessors of the device
 };
 
-// Enqueue the prepare, stream and record kernels (lp_kernels.cu).
-cudaError_t launch_epilogue(const Params& p, int dtype, const LaunchCfg& cfg, cudaStream_t stream);
+// Enqueue the prepare, stream and record kernels (lp_kernels.cu); records =
+// false leaves the record kernel out (the sharded path builds the records).
+cudaError_t launch_epilogue(const Params& p, int dtype, const LaunchCfg& cfg, cudaStream_t stream,
+                            bool records = true);
+// Enqueue the vocabulary-sharded record kernels after launch_epilogue(..., false):
+// exchange 1 into x1 [rows * S], exchange 2 into x2 [rows * S * 256], the merge.
+cudaError_t launch_shard_records(const Params& p, int dtype, const LaunchCfg& cfg, int S, float2* x1, int* x2,
+                                 cudaStream_t stream);
 // Enqueue stochastic chain verification (one 512-thread CTA per group at a time).
 cudaError_t launch_chain(const ChainParams& p, int dtype, int sms, cudaStream_t stream);
 // Test hook: `ctas` CTAs that each hold a multiprocessor's shared memory for `ns`.

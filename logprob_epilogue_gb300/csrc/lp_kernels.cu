@@ -1285,16 +1285,23 @@ __device__ __forceinline__ unsigned long long lp_key(float x, float lse, uint32_
     return (static_cast<unsigned long long>(ord32(logprob(x, lse))) << 32) | static_cast<unsigned long long>(~id);
 }
 
-// Warp 0 writes, from pair slot `from` on, the lanes whose logprob equals L,
-// smallest ids first, until keff pairs are written (a walk over the row).
+// The part of a row a natural selection covers: tiles [t0, t1), ids [v0, v1)
+// (the whole row, or one vocabulary shard of whole tiles).
+struct Span {
+    int t0, t1;
+    long long v0, v1;
+};
+
+// Warp 0 writes, from pair slot `from` on, the lanes of the span whose
+// logprob equals L, smallest ids first, until keff pairs are written.
 template <int ELT>
-__device__ __forceinline__ void fill_equal_lanes(const Params& p, int* rec, int row, float lse, float L, int from,
-                                                 int keff, int lane) {
+__device__ __forceinline__ void fill_equal_lanes(const Params& p, int* rec, int row, const Span& sp, float lse, float L,
+                                                 int from, int keff, int lane) {
     const unsigned lbits = __float_as_uint(L);
     int got = from;
-    for (long long v0 = 0; v0 < p.V && got < keff; v0 += 32) {
+    for (long long v0 = sp.v0; v0 < sp.v1 && got < keff; v0 += 32) {
         const long long v = v0 + lane;
-        const bool m = v < p.V && logprob(load_logit<ELT>(p, row, v), lse) == L;
+        const bool m = v < sp.v1 && logprob(load_logit<ELT>(p, row, v), lse) == L;
         const unsigned bb = __ballot_sync(kFull, m);
         const int before = __popc(bb & ((1u << lane) - 1u));
         if (m && got + before < keff) {
@@ -1311,15 +1318,15 @@ __device__ __forceinline__ void fill_equal_lanes(const Params& p, int* rec, int 
 // logits, each step a count over the row); then the lanes above L (fewer than
 // K, sorted by one warp) and the smallest ids equal to L.
 template <int ELT>
-__device__ __noinline__ void natural_exact(const Params& p, RecShared& sm, int row, int keff, float lse) {
+__device__ __noinline__ void natural_exact(const Params& p, RecShared& sm, int row, const Span& sp, int keff, float lse) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const long long V = p.V;
     // the largest o with count(ord32(x) >= o) >= keff
     uint32_t lo = ord32(kNegInf), hi = ord32(kPosInf);
     while (lo < hi) {
         const uint32_t mid = lo + ((hi - lo + 1u) >> 1);
         int c = 0;
-        for (long long v = tid; v < V; v += kConsumerThreads) c += ord32(__fadd_rn(load_logit<ELT>(p, row, v), 0.0f)) >= mid;
+        for (long long v = sp.v0 + tid; v < sp.v1; v += kConsumerThreads)
+            c += ord32(__fadd_rn(load_logit<ELT>(p, row, v), 0.0f)) >= mid;
         c = (int)__reduce_add_sync(kFull, (unsigned)c);
         if (lane == 0) sm.red_x[warp] = c;
         cbar();
@@ -1334,7 +1341,7 @@ __device__ __noinline__ void natural_exact(const Params& p, RecShared& sm, int r
     // lanes reported above L: fewer than keff
     if (tid == 0) sm.n_keys = 0;
     cbar();
-    for (long long v = tid; v < V; v += kConsumerThreads) {
+    for (long long v = sp.v0 + tid; v < sp.v1; v += kConsumerThreads) {
         const float x = load_logit<ELT>(p, row, v);
         if (logprob(x, lse) > L) {
             const int i = atomicAdd(&sm.n_keys, 1);
@@ -1349,7 +1356,7 @@ __device__ __noinline__ void natural_exact(const Params& p, RecShared& sm, int r
             sm.rec[2 + 2 * lane] = (int)key_id(k);
             sm.rec[3 + 2 * lane] = (int)__float_as_uint(key_value(k));
         }
-        fill_equal_lanes<ELT>(p, sm.rec, row, lse, L, c_gt, keff, lane);
+        fill_equal_lanes<ELT>(p, sm.rec, row, sp, lse, L, c_gt, keff, lane);
     }
     cbar();
 }
@@ -1363,11 +1370,11 @@ constexpr int kCachedShares = 2;
 // entry values go to sm.wtop[w] (0: none).  The 32nd largest of those 64
 // values is a threshold with at least 32 entries at or above it.
 constexpr int kWarpTop = 8;
-__device__ __forceinline__ void summary_top(const Params& p, RecShared& sm, long long base, int warp, int lane,
-                                            unsigned long long (&cache)[kCachedShares][4]) {
+__device__ __forceinline__ void summary_top(const Params& p, RecShared& sm, long long base, const Span& sp, int warp,
+                                            int lane, unsigned long long (&cache)[kCachedShares][4]) {
     uint32_t top[4] = {0u, 0u, 0u, 0u};  // this thread's 4 largest entry values, descending
     int i = 0;
-    for (int t = lane; t < p.T; t += 32, ++i) {
+    for (int t = sp.t0 + lane; t < sp.t1; t += 32, ++i) {
         const ulonglong2* q = reinterpret_cast<const ulonglong2*>(p.part_keys + (base + t) * kKeysPerTile + warp * 4);
         const ulonglong2 a = __ldcg(q), b = __ldcg(q + 1);
         const unsigned long long e[4] = {a.x, a.y, b.x, b.y};
@@ -1412,29 +1419,31 @@ __device__ __forceinline__ void summary_top(const Params& p, RecShared& sm, long
 // is a candidate) and sm.lse: candidates, their logprob keys, the best keff by
 // rank, the subtraction-tie check.  Writes the natural pairs into sm.rec.
 template <int ELT>
-__device__ __noinline__ void natural_record(const Params& p, RecShared& sm, int row, long long base, int keff,
-                                            const unsigned long long (&cache)[kCachedShares][4]) {
+__device__ __noinline__ void natural_record(const Params& p, RecShared& sm, int row, long long base, const Span& sp,
+                                            int keff, const unsigned long long (&cache)[kCachedShares][4]) {
     constexpr int TE = tile_elems<ELT>(), EPV = 16 / ELT, NCH = TileLayout<ELT>::NCH;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const float lse = sm.lse;
     const uint32_t th = sm.theta_o;
     const float theta = th ? unord32(th) : kNegInf;
-    const long long V = p.V;
+    const long long V = sp.v1;  // lanes at or past it are not the span's
     const unsigned char* rowp = reinterpret_cast<const unsigned char*>(p.logits) + (long long)row * p.Vp * ELT;
     bool overflow = false;
     if (th == 0u) {
         // no threshold (a tiny vocabulary): every lane is a candidate
-        if (V > kCandKeys) {
+        const long long n = sp.v1 - sp.v0;
+        if (n > kCandKeys) {
             overflow = true;
         } else {
-            for (int v = tid; v < V; v += kConsumerThreads) sm.ckeys[v] = lp_key(load_logit<ELT>(p, row, v), lse, (uint32_t)v);
-            if (tid == 0) sm.n_keys = (int)V;
+            for (int i = tid; i < n; i += kConsumerThreads)
+                sm.ckeys[i] = lp_key(load_logit<ELT>(p, row, sp.v0 + i), lse, (uint32_t)(sp.v0 + i));
+            if (tid == 0) sm.n_keys = (int)n;
         }
         cbar();
     } else {
         // 2. candidate threads: entries >= theta, and whole shares whose 4th entry reaches it
         int i = 0;
-        for (int t = lane; t < p.T; t += 32, ++i) {
+        for (int t = sp.t0 + lane; t < sp.t1; t += 32, ++i) {
             unsigned long long e[4];
             if (i < kCachedShares) {
 #pragma unroll
@@ -1519,7 +1528,7 @@ __device__ __noinline__ void natural_record(const Params& p, RecShared& sm, int 
         }
     }
     if (overflow) {
-        natural_exact<ELT>(p, sm, row, keff, lse);
+        natural_exact<ELT>(p, sm, row, sp, keff, lse);
         return;
     }
     // 4. the best keff keys by rank (keys are distinct: they carry the id)
@@ -1558,7 +1567,7 @@ __device__ __noinline__ void natural_record(const Params& p, RecShared& sm, int 
         gt = (int)__reduce_add_sync(kFull, (unsigned)gt);
         if (lane == 0 && gt) atomicAdd(&sm.n_thr, gt);
         cbar();
-        if (warp == 0) fill_equal_lanes<ELT>(p, sm.rec, row, lse, L, sm.n_thr, keff, lane);
+        if (warp == 0) fill_equal_lanes<ELT>(p, sm.rec, row, sp, lse, L, sm.n_thr, keff, lane);
         cbar();
     }
 }
@@ -1631,7 +1640,8 @@ __device__ __noinline__ void record_block(const Params& p, RecShared& sm, int ro
         if (id >= 0 && id < p.V) xi = load_logit<ELT>(p, row, id);
     }
     unsigned long long cache[kCachedShares][4];
-    if (natural) summary_top(p, sm, base, warp, lane, cache);
+    const Span whole = {0, T, 0, p.V};
+    if (natural) summary_top(p, sm, base, whole, warp, lane, cache);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         const float m2 = __shfl_xor_sync(kFull, m, o), s2 = __shfl_xor_sync(kFull, s, o);
@@ -1686,7 +1696,7 @@ __device__ __noinline__ void record_block(const Params& p, RecShared& sm, int ro
     }
     cbar();
     rtrace(p, kTrRecB, row);
-    if (natural) natural_record<ELT>(p, sm, row, base, (long long)kc < p.V ? kc : (int)p.V, cache);
+    if (natural) natural_record<ELT>(p, sm, row, base, whole, (long long)kc < p.V ? kc : (int)p.V, cache);
     rtrace(p, kTrRecC, row);
     if (ids && tid < kc) {
         int bits = (int)kUnusedBits;
@@ -1765,6 +1775,204 @@ __global__ void lp_occupy_kernel(unsigned long long ns) {
     while (globaltimer() - t0 < ns) __nanosleep(1000);
 }
 
+// ------------------------------------------------------------------ vocabulary-sharded records
+//
+// Source: "logprobs-design.md", the vocabulary-sharded speculative
+// verification paragraph: each rank holds a vocabulary shard of the target
+// logits; a first all-gather carries each shard's maximum and exponential mass
+// (the global normalisation), a second the chosen token's raw logit from its
+// owning rank and either the shard's best 32 sort keys or the selected ids' raw
+// logits (256 words per position per rank); a final launch merges the gathered
+// candidates into the same packed record.
+//
+// Here the shards are S column ranges of whole tiles of one block on one GPU:
+// shard s of a row covers tiles [s*T/S, (s+1)*T/S).  Acceptance and the tile
+// partials come from the stream kernel (on several GPUs that is the
+// verification step, which decides the emitted prefix before the reduction).
+// For record task i, shard s writes exchange 1 at x1[i*S + s] and exchange 2 at
+// x2[(i*S + s)*256]; the kernels read another shard's payload only after the
+// launch that wrote it has completed, as the all-gathers order them.
+
+__device__ __forceinline__ Span shard_span(const Params& p, int s, int S) {
+    Span sp;
+    sp.t0 = (int)((long long)s * p.T / S);
+    sp.t1 = (int)((long long)(s + 1) * p.T / S);
+    const long long te = p.elt == 2 ? tile_elems<2>() : tile_elems<4>();
+    sp.v0 = (long long)sp.t0 * te;
+    const long long e1 = (long long)sp.t1 * te;
+    sp.v1 = e1 < p.V ? e1 : p.V;
+    return sp;
+}
+
+// Exchange 1: warp s (< S) of the CTA of task i merges the (max, exp-sum)
+// partials of shard s's tiles.
+__global__ void __launch_bounds__(kConsumerThreads) lp_shard_stage1_kernel(Params p, int S, float2* x1) {
+    const unsigned n = __ldcg(&p.ctrl->rec_count);
+    const int lane = threadIdx.x & 31, s = threadIdx.x >> 5;
+    if (s >= S || vload(&p.ctrl->abort) != 0u) return;
+    for (unsigned i = blockIdx.x; i < n; i += gridDim.x) {
+        const int row = __ldcg(&p.rec_tasks[i]).y;
+        const Span sp = shard_span(p, s, S);
+        const long long base = (long long)row * p.T;
+        float m = kNegInf, sum = 0.0f;
+        for (int q = sp.t0 * kWarps + lane; q < sp.t1 * kWarps; q += 32) {
+            const float2 ms = __ldcg(&p.part_ms[base * kWarps + q]);
+            ms_merge(m, sum, ms.x, ms.y);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ms_merge(m, sum, __shfl_xor_sync(kFull, m, o), __shfl_xor_sync(kFull, sum, o));
+        if (lane == 0) x1[(size_t)i * S + s] = make_float2(m, sum);
+    }
+}
+
+// lse of task i from the gathered exchange 1 (every shard merges in the same
+// order, so every shard gets the same bits).
+__device__ __forceinline__ float shard_lse(const float2* x1, unsigned i, int S) {
+    float M = kNegInf, T = 0.0f;
+    for (int s = 0; s < S; ++s) {
+        const float2 ms = __ldcg(&x1[(size_t)i * S + s]);
+        ms_merge(M, T, ms.x, ms.y);
+    }
+    return M + logf(T);
+}
+
+// Exchange 2: CTA (i, s) writes shard s's 256-word payload of task i:
+//   [0]           raw logit bits of the chosen token if the shard owns it, else NaN bits
+//   natural rows: [1 + 2r], [2 + 2r] = (high, low) word of the shard's r-th best
+//                 sort key (ord32(logprob) << 32 | ~id), r < 32, 0 = none
+//   explicit ids: [1 + c] = raw logit bits of id c if the shard owns it, else NaN bits
+template <int ELT>
+__global__ void __launch_bounds__(kConsumerThreads, 3) lp_shard_stage2_kernel(Params p, int S, const float2* x1, int* x2) {
+    __shared__ RecShared sm;
+    const unsigned n = __ldcg(&p.ctrl->rec_count);
+    if (vload(&p.ctrl->abort) != 0u) return;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (unsigned bi = blockIdx.x; bi < n * (unsigned)S; bi += gridDim.x) {
+        const unsigned i = bi / S;
+        const int s = (int)(bi % S);
+        const int4 t = __ldcg(&p.rec_tasks[i]);  // (chosen, row, descriptor word | flags | count << 16, group)
+        const int row = t.y, chosen = t.x, g = t.w, dy = t.z & 0x7FFF, kc = t.z >> 16;
+        const int mode = (dy >> 8) & 3, ids = (dy >> 12) & 1;
+        const bool natural = !ids && mode == kModeNatural && kc > 0;
+        const Span sp = shard_span(p, s, S);
+        const long long base = (long long)row * p.T;
+        int* out = x2 + ((size_t)i * S + s) * kShardWords;
+        // each thread writes one word: the chosen logit, an id's logit, or the fill
+        static_assert(kShardWords == kConsumerThreads, "one payload word per thread");
+        {
+            const int w = tid;
+            int v = natural ? 0 : (int)kUnusedBits;
+            if (w == 0) {
+                v = (chosen >= sp.v0 && chosen < sp.v1) ? (int)__float_as_uint(load_logit<ELT>(p, row, chosen))
+                                                         : (int)kUnusedBits;
+            } else if (ids && w - 1 < kc) {
+                const int id = __ldg(&p.token_ids[(long long)g * kMaxIds + (w - 1)]);
+                v = (id >= sp.v0 && id < sp.v1) ? (int)__float_as_uint(load_logit<ELT>(p, row, id)) : (int)kUnusedBits;
+            }
+            out[w] = v;
+        }
+        if (tid == 0) {
+            sm.n_thr = sm.n_sh = sm.n_keys = 0;
+            sm.lse = shard_lse(x1, i, S);
+        }
+        unsigned long long cache[kCachedShares][4];
+        if (natural) summary_top(p, sm, base, sp, warp, lane, cache);
+        cbar();
+        if (natural) {
+            if (warp == 0) {
+                const uint32_t* wt = &sm.wtop[0][0];
+                const uint32_t a = wt[lane], b = wt[lane + 32];
+                int ra = 0, rb = 0;
+#pragma unroll 8
+                for (int j = 0; j < 64; ++j) {
+                    const uint32_t v = wt[j];
+                    ra += v > a || (v == a && j < lane);
+                    rb += v > b || (v == b && j < lane + 32);
+                }
+                if (ra == 31) sm.theta_o = a;
+                if (rb == 31) sm.theta_o = b;
+            }
+            for (int w = tid; w < 66; w += kConsumerThreads) sm.rec[w] = (w >= 2 && (w & 1) == 0) ? -1 : (int)kUnusedBits;
+            cbar();
+            const long long len = sp.v1 - sp.v0;
+            natural_record<ELT>(p, sm, row, base, sp, len < 32 ? (int)len : 32, cache);
+            // the shard's best keys, from the pairs in rank order
+            if (warp == 0) {
+                const int id = sm.rec[2 + 2 * lane];
+                const float lp = __uint_as_float((uint32_t)sm.rec[3 + 2 * lane]);
+                const unsigned long long key =
+                    id >= 0 ? ((unsigned long long)ord32(lp) << 32) | (unsigned long long)(~(uint32_t)id) : 0ull;
+                out[1 + 2 * lane] = (int)(uint32_t)(key >> 32);
+                out[2 + 2 * lane] = (int)(uint32_t)key;
+            }
+        }
+        cbar();
+    }
+}
+
+// Final merge: CTA of task i gathers the S payloads into the packed record.
+__global__ void __launch_bounds__(kConsumerThreads) lp_shard_merge_kernel(Params p, int S, const float2* x1, const int* x2) {
+    __shared__ unsigned long long lists[kMaxShards][32];
+    __shared__ int rec[kRecordWords];
+    __shared__ float lse_s;
+    const unsigned n = __ldcg(&p.ctrl->rec_count);
+    if (vload(&p.ctrl->abort) != 0u) return;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (unsigned i = blockIdx.x; i < n; i += gridDim.x) {
+        const int4 t = __ldcg(&p.rec_tasks[i]);
+        const int row = t.y, chosen = t.x, dy = t.z & 0x7FFF, kc = t.z >> 16, g = t.w;
+        const int mode = (dy >> 8) & 3, ids = (dy >> 12) & 1;
+        const bool natural = !ids && mode == kModeNatural && kc > 0;
+        const int* pay = x2 + (size_t)i * S * kShardWords;
+        for (int w = tid; w < kRecordWords; w += kConsumerThreads) rec[w] = (w >= 2 && (w & 1) == 0) ? -1 : (int)kUnusedBits;
+        if (tid == 0) lse_s = shard_lse(x1, i, S);
+        if (natural && warp < S) {
+            lists[warp][lane] = ((unsigned long long)(uint32_t)__ldcg(&pay[warp * kShardWords + 1 + 2 * lane]) << 32) |
+                                (uint32_t)__ldcg(&pay[warp * kShardWords + 2 + 2 * lane]);
+        }
+        __syncthreads();
+        const float lse = lse_s;
+        if (tid == 0) {
+            float xc = kNegInf;
+            bool found = false;
+            for (int s = 0; s < S; ++s) {
+                const int w = __ldcg(&pay[s * kShardWords]);
+                if ((uint32_t)w != kUnusedBits) {
+                    xc = __uint_as_float((uint32_t)w);
+                    found = true;
+                }
+            }
+            rec[0] = chosen;
+            rec[1] = found ? (int)__float_as_uint(logprob(xc, lse)) : (int)kUnusedBits;
+            if (p.lse_out) p.lse_out[row] = lse;
+        }
+        if (natural && warp == 0) {
+            unsigned long long r = lists[0][lane];
+            for (int s = 1; s < S; ++s) r = merge_lists(r, lists[s][lane], lane);
+            const int keff = (long long)kc < p.V ? kc : (int)p.V;
+            if (lane < keff && r != 0ull) {
+                rec[2 + 2 * lane] = (int)key_id(r);
+                rec[3 + 2 * lane] = (int)__float_as_uint(key_value(r));
+            }
+        }
+        if (ids && tid < kc) {
+            const int id = __ldg(&p.token_ids[(long long)g * kMaxIds + tid]);
+            int bits = (int)kUnusedBits;
+            for (int s = 0; s < S; ++s) {
+                const int w = __ldcg(&pay[s * kShardWords + 1 + tid]);
+                if ((uint32_t)w != kUnusedBits) bits = (int)__float_as_uint(logprob(__uint_as_float((uint32_t)w), lse));
+            }
+            if (id < 0 || id >= p.V) atomicOr(p.status, kStatusBadId);
+            rec[2 + 2 * tid] = id;
+            rec[3 + 2 * tid] = bits;
+        }
+        __syncthreads();
+        int* o = p.records + (long long)row * kRecordWords;
+        for (int w = tid; w < kRecordWords; w += kConsumerThreads) o[w] = rec[w];
+        __syncthreads();
+    }
+}
+
 template <int ELT>
 constexpr int stream_smem_bytes() {
     return StageCfg<ELT>::kStages * kTileBytes + (int)sizeof(Shared);
@@ -1812,7 +2020,24 @@ cudaError_t launch_occupy(int ctas, unsigned long long ns, cudaStream_t stream) 
     return cudaGetLastError();
 }
 
-cudaError_t launch_epilogue(const Params& p_in, int dtype, const LaunchCfg& cfg, cudaStream_t stream) {
+cudaError_t launch_shard_records(const Params& p, int dtype, const LaunchCfg& cfg, int S, float2* x1, int* x2,
+                                 cudaStream_t stream) {
+    int grid = cfg.sms * 3;
+    if (grid > p.rows) grid = p.rows > 0 ? p.rows : 1;
+    lp_shard_stage1_kernel<<<grid, kConsumerThreads, 0, stream>>>(p, S, x1);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    int grid2 = cfg.sms * 3;
+    if ((long long)grid2 > (long long)p.rows * S) grid2 = p.rows * S > 0 ? p.rows * S : 1;
+    if (dtype == 1) lp_shard_stage2_kernel<2><<<grid2, kConsumerThreads, 0, stream>>>(p, S, x1, x2);
+    else lp_shard_stage2_kernel<4><<<grid2, kConsumerThreads, 0, stream>>>(p, S, x1, x2);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    lp_shard_merge_kernel<<<grid, kConsumerThreads, 0, stream>>>(p, S, x1, x2);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_epilogue(const Params& p_in, int dtype, const LaunchCfg& cfg, cudaStream_t stream, bool records) {
     long long work = (long long)p_in.rows * p_in.T;
     int grid = cfg.grid;
     if (work < grid) grid = work > 0 ? (int)work : 1;
@@ -1837,7 +2062,7 @@ cudaError_t launch_epilogue(const Params& p_in, int dtype, const LaunchCfg& cfg,
     } else {
         e = score ? cudaLaunchKernelEx(&lc, lp_stream_kernel<4, true>, p) : cudaLaunchKernelEx(&lc, lp_stream_kernel<4, false>, p);
     }
-    if (e != cudaSuccess) return e;
+    if (e != cudaSuccess || !records) return e;
     // records: CTA b builds tasks b, b + grid, ... of the compact task list
     // (at most one per row); three 256-thread CTAs per SM are resident
     int rgrid = cfg.sms * 3;

@@ -42,6 +42,9 @@ struct lp_plan_s {
     size_t staging_bytes;
     lp_io stage_io;
     cudaStream_t last_stream;
+    // optional vocabulary-shard exchange buffers (LP_PLAN_VOCAB_SHARDS)
+    float2* shard_x1;   // [max_rows * kMaxShards]
+    int* shard_x2;      // [max_rows * kMaxShards * 256]
     // optional timeline (LP_PLAN_DEBUG_TRACE)
     unsigned long long* trace;
     unsigned int* trace_count;
@@ -182,6 +185,7 @@ lp::Params make_params(const lp_plan_s* plan, const lp_io& io) {
     p.rows = io.rows;
     p.G = io.groups;
     p.T = plan->T;
+    p.elt = plan->elt;
     p.k_max = plan->d.k_max;
     p.k_alt_max = plan->d.k_alt_max;
     p.max_ids = plan->d.max_ids;
@@ -304,6 +308,11 @@ int lp_plan_create(lp_plan_t* out, const lp_plan_desc* desc) {
             s.status = reinterpret_cast<uint32_t*>(plan->staging + S.status);
         }
     }
+    if (e == cudaSuccess && (desc->flags & LP_PLAN_VOCAB_SHARDS)) {
+        const size_t rows = (size_t)desc->max_rows;
+        e = cudaMalloc(&plan->shard_x1, rows * lp::kMaxShards * sizeof(float2));
+        if (e == cudaSuccess) e = cudaMalloc(&plan->shard_x2, rows * lp::kMaxShards * lp::kShardWords * sizeof(int));
+    }
     if (e == cudaSuccess && (desc->flags & LP_PLAN_DEBUG_TRACE)) {
         plan->trace_cap = 2048;
         plan->trace_ctas = plan->cfg.grid;
@@ -317,6 +326,8 @@ int lp_plan_create(lp_plan_t* out, const lp_plan_desc* desc) {
     if (e != cudaSuccess) {
         if (plan->trace) cudaFree(plan->trace);
         if (plan->trace_count) cudaFree(plan->trace_count);
+        if (plan->shard_x1) cudaFree(plan->shard_x1);
+        if (plan->shard_x2) cudaFree(plan->shard_x2);
         if (plan->staging) cudaFree(plan->staging);
         cudaFree(plan->scratch);
         delete plan;
@@ -332,6 +343,8 @@ int lp_plan_destroy(lp_plan_t plan) {
     cudaError_t e = cudaSuccess;
     if (plan->trace) cudaFree(plan->trace);
     if (plan->trace_count) cudaFree(plan->trace_count);
+    if (plan->shard_x1) cudaFree(plan->shard_x1);
+    if (plan->shard_x2) cudaFree(plan->shard_x2);
     if (plan->staging) e = cudaFree(plan->staging);
     cudaError_t e2 = cudaFree(plan->scratch);
     delete plan;
@@ -348,6 +361,24 @@ int lp_bind(lp_plan_t plan, const lp_io* io) {
     plan->bound = true;
     plan->clip_eos = nullptr;
     plan->clip_budget = nullptr;
+    return LP_OK;
+}
+
+int lp_run_sharded(lp_plan_t plan, int32_t shards, void* stream) {
+    if (!plan) return LP_EINVAL;
+    if (!plan->bound || !plan->shard_x1) return LP_ESTATE;
+    if (shards < 1 || shards > lp::kMaxShards || shards > plan->T) return LP_EINVAL;
+    DeviceGuard guard(plan->d.device);
+    if (!guard.ok) return cuda_fail(cudaGetLastError());
+    lp::Params p = make_params(plan, plan->io);
+    p.eos = plan->clip_eos;
+    p.budget = plan->clip_budget;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = lp::launch_epilogue(p, plan->d.dtype, plan->cfg, s, false);
+    if (e == cudaSuccess) e = lp::launch_shard_records(p, plan->d.dtype, plan->cfg, shards, plan->shard_x1,
+                                                        plan->shard_x2, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    plan->last_stream = s;
     return LP_OK;
 }
 
