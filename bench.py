@@ -432,6 +432,8 @@ def main():
     ap.add_argument("--no-per-workload", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--groups", type=int, default=0,
+                    help="verify groups of the timed workload (0: its own count); a smaller block for profiling")
     args = ap.parse_args()
     world, rank, local, pg = dist_setup(args)
     if args.impl == "reference":
@@ -449,7 +451,7 @@ def main():
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
 
-    w = W.make(args.config)
+    w = W.make(args.config, **({"groups": args.groups} if args.groups > 0 and args.config in ("spec", "large") else {}))
     plan, ins, outs, flush, starts, ends, stream = bench_device(w, args.steps, args.warmup, local,
                                                                staging=not args.no_e2e)
 
