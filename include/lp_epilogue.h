@@ -388,7 +388,7 @@ int lp_plan_tiles_per_row(lp_plan_t plan);
  *   stream  a cudaStream_t (NULL = legacy default stream).
  *
  * The scratch a run needs grows with io->rows * ceil(V / tile elements)
- * (about 384 bytes per row tile, plus 48 bytes per row and 16 per group);
+ * (384 bytes per row tile, plus 40 bytes per row and 16 per group);
  * a run that needs more than LP_STATIC_SCRATCH_BYTES is rejected with
  * LP_ESCRATCH before anything is enqueued.  4 MiB covers, for example, 512
  * rows of a 248,448-lane BF16 vocabulary.

@@ -171,8 +171,12 @@ def compare(w: W.Workload, gpu: dict, orc: dict, check_invariant: bool = True) -
 
 
 def row_tol(lse) -> float:
-    """2e-5, or two FP32 ulps of lse where the format is coarser than that."""
-    return max(TOL, 2.0 * float(np.spacing(np.abs(np.float32(lse)))))
+    """2e-5, or one FP32 ulp of lse where the format is coarser than that: two
+    correctly rounded lse values of nearly the same real differ by one ulp, and
+    then fl32(x - lse) differs by at most that ulp (both roundings of the
+    subtraction land on the same grid when |x - lse| is in lse's binade, and
+    are exact or finer below it)."""
+    return max(TOL, float(np.spacing(np.abs(np.float32(lse)))))
 
 
 def _cmp_lp(r, what, gb, ob, stats, tol=TOL):
