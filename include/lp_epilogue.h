@@ -61,6 +61,10 @@
  * the whole GPU: beside another kernel on another stream (or in a parallel
  * graph branch), the CTAs that are resident do all the work and the others,
  * when they start, find none.  The run then takes longer; it does not stall.
+ * The records are built by a second persistent kernel while the stream
+ * kernel runs; it is scheduled only once every stream CTA has started, takes
+ * the room the stream kernel leaves, and waits on the stream kernel's
+ * decisions, never the other way round.
  *
  * Errors: every function returns LP_OK (0) or a negative LP_E* code and never
  * aborts.  Conditions only visible on the device are reported in the bound
@@ -347,11 +351,12 @@ int lp_debug_tiles_read(lp_plan_t plan, int32_t* host_tiles, int32_t rows);
 int lp_debug_poison_scratch(lp_plan_t plan, void* stream);
 
 /* Debug: the device timeline of the last run of a plan created with
- * LP_PLAN_DEBUG_TRACE.  *ctas and *cap receive the geometry: (ctas * 3 + 1)
+ * LP_PLAN_DEBUG_TRACE.  *ctas and *cap receive the geometry: (ctas * 4 + 1)
  * rings of cap events, each event two uint64 words (globaltimer ns,
- * type << 56 | row << 24 | tile); ring (cta, role) holds counts[cta * 3 + role]
- * events (roles: 0 producer, 1 compute, 2 merge); the last ring holds the
- * prepare kernel's start and end.  With events == NULL only the geometry is
+ * type << 56 | row << 24 | tile); ring (cta, role) holds counts[cta * 4 + role]
+ * events (roles: 0 producer, 1 compute, 2 merge, 3 record kernel); the last
+ * ring holds the prepare kernel's start and end and the record kernel's first
+ * start and last end.  With events == NULL only the geometry is
  * returned.  Synchronises the plan's last stream.  LP_ESTATE without tracing. */
 int lp_debug_trace(lp_plan_t plan, uint64_t* events, uint32_t* counts, int32_t* ctas, int32_t* cap);
 
@@ -388,7 +393,7 @@ int lp_plan_tiles_per_row(lp_plan_t plan);
  *   stream  a cudaStream_t (NULL = legacy default stream).
  *
  * The scratch a run needs grows with io->rows * ceil(V / tile elements)
- * (384 bytes per row tile, plus 40 bytes per row and 16 per group);
+ * (448 bytes per row tile, plus 56 bytes per row and 16 per group);
  * a run that needs more than LP_STATIC_SCRATCH_BYTES is rejected with
  * LP_ESCRATCH before anything is enqueued.  4 MiB covers, for example, 512
  * rows of a 248,448-lane BF16 vocabulary.
@@ -396,8 +401,10 @@ int lp_plan_tiles_per_row(lp_plan_t plan);
  * The first call on a device sets that device up (it looks up the array's
  * device address and the kernels' launch shape); make that first call before
  * any stream capture on the device.  Each call clears the array's control
- * block on `stream` before its kernels; everything else in the array is
- * written before it is read.  All calls share the one array, so calls whose
+ * block on `stream` before its kernels, all but its run counter, which keeps
+ * counting across calls: the per-tile results and record tasks that cross
+ * thread blocks during a run carry the run's number, so nothing an earlier
+ * call left in the array is taken for the current call's.  All calls share the one array, so calls whose
  * work can overlap on the GPU (different streams, or different host threads)
  * race and corrupt each other: serialise them on one stream.
  *

@@ -413,15 +413,16 @@ class Plan:
         return out[:rows]
 
     def trace(self):
-        """Device timeline of the last run: (events uint64 [ctas*3+1, cap, 2], counts uint32 [ctas, 3]).
+        """Device timeline of the last run: (events uint64 [ctas*4+1, cap, 2], counts uint32 [ctas, 4]).
 
-        Event word 1 = type << 56 | row << 24 | tile (types: 1 kernel start, 2 claim, 3 TMA issue,
-        4 tile start, 5 tile end, 6 tile published, 7 merge start, 8 acceptance decided,
-        9 merge end, 10/11 prepare start/end, 12 producer exit)."""
+        Rings per CTA: producer, compute, merge (decisions), record kernel.  Event word 1 =
+        type << 56 | row << 24 | tile (types: 1 kernel start, 2 claim, 3 TMA issue, 4 tile start,
+        5 tile end, 6 tile published, 7 merge start, 8 acceptance decided, 9 merge end, 10/11
+        prepare start/end, 12 producer exit, 17/18 record start/end, 19-21 record phases)."""
         ctas, cap = ctypes.c_int32(), ctypes.c_int32()
         _check(lib().lp_debug_trace(self._h, None, None, ctypes.byref(ctas), ctypes.byref(cap)), "lp_debug_trace")
-        ev = np.zeros(((ctas.value * 3 + 1), cap.value, 2), np.uint64)
-        cnt = np.zeros((ctas.value, 3), np.uint32)
+        ev = np.zeros(((ctas.value * 4 + 1), cap.value, 2), np.uint64)
+        cnt = np.zeros((ctas.value, 4), np.uint32)
         _check(lib().lp_debug_trace(self._h, ev.ctypes.data, cnt.ctypes.data, ctypes.byref(ctas), ctypes.byref(cap)),
                "lp_debug_trace")
         return ev, cnt

@@ -20,17 +20,21 @@ constexpr int kScoreAlts = 20;
 constexpr int kMaxIds = 128;
 constexpr int kMaxShards = 8;          // vocabulary shards of lp_run_sharded
 constexpr int kShardWords = 256;       // exchange-2 words per position per shard
+constexpr int kTraceRoles = 4;         // debug timeline rings per CTA: producer, compute, merge, record
 
-// Pipeline stages per CTA and CTAs per SM, per element type: three CTAs of two
-// 32 KiB stages fill the SM's shared memory and give 24 compute warps per SM.
+// Pipeline stages per CTA and CTAs per SM, per element type: three CTAs of one
+// 32 KiB stage per SM give 24 compute warps per SM and keep about 14 MB of
+// copies in flight, enough for the full HBM bandwidth: more stages only
+// lengthen the memory queue that every dependent read (the next row of a
+// verify chain, a record's gathers) waits in.
 #ifndef LP_BF16_STAGES
-#define LP_BF16_STAGES 2
+#define LP_BF16_STAGES 1
 #endif
 #ifndef LP_BF16_CTAS
 #define LP_BF16_CTAS 3
 #endif
 #ifndef LP_F32_STAGES
-#define LP_F32_STAGES 2
+#define LP_F32_STAGES 1
 #endif
 #ifndef LP_F32_CTAS
 #define LP_F32_CTAS 3
@@ -79,9 +83,15 @@ struct Ctrl {
     unsigned int fresh_rows;  // depth-0 rows (set by the prepare kernel)
     unsigned int abort;       // 1: malformed groups, the stream kernel does nothing
     unsigned int never;       // never written: the forced-timeout test hook waits on it
-    unsigned int pad4[29];
+    unsigned int chain_max;   // rows that acceptances can append at most (the read groups' drafts)
+    unsigned int pad4[28];
     unsigned int rec_count;   // record tasks appended (rec_tasks[0, rec_count))
     unsigned int pad5[31];
+    unsigned int rec_claim;   // record tasks claimed by producers (a claim may run ahead of rec_count)
+    unsigned int pad6[31];
+    unsigned int epoch;       // run number, advanced by the prepare kernel (never 0 or all ones); the
+                              // tile partials and record tasks of a run carry it
+    unsigned int pad7[31];
 };
 
 struct Params {
@@ -116,15 +126,18 @@ struct Params {
     unsigned long long* row_best;   // [max_rows] best (argmax) key over the finished tiles
     int4* gdesc;          // [max_groups] x = first row, y = k | mode << 8 | explicit << 12 |
                           // requested << 13, z = top_k or id count, w = sampled token
-    int4* rec_tasks;      // [max_rows] compact list of the records to build: (chosen token, row,
-                          // group descriptor word | count << 16, group), appended by the deciders
-    float2* part_ms;      // [max_rows * T * 8] (max, exp-sum) of each compute warp's share of a tile
+    ulonglong2* rec_tasks;  // [max_rows * 2] compact list of the records to build, appended by the
+                            // deciders: words epoch << 32 | (chosen token, row, group descriptor word |
+                            // count << 16, group)
+    ulonglong2* part_ms;  // [max_rows * T * 8] (epoch << 32 | max bits, epoch << 32 | exp-sum bits) of
+                          // each compute warp's share of a tile
     int2* part_rank;      // [max_rows * T * 8] prompt scoring: (lanes above the target's logit, the
                           // smallest such logit's bits) of each compute warp's share of a tile
     unsigned long long* part_keys;  // [max_rows * T * 32] natural tiles: each compute warp's 4 largest
                                     // thread maxima, (ord32 << 32) | (tile << 8) | thread; 0 = none
     unsigned long long timeout_ns;
     unsigned int debug_flags;
+    int build_records;    // 1: the stream kernel builds the records (0: the sharded kernels do)
     int read_ahead;       // 0: rows past a group's emitted prefix are never read
     // prompt scoring (targets != nullptr): group g is row g alone, k = 0, 20
     // natural alternatives, chosen token targets[g]; records go to score_records

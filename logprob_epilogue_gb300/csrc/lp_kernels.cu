@@ -1,55 +1,52 @@
 // lp_kernels.cu -- sm_103a kernels of the logprob / greedy-acceptance epilogue.
 //
-// Three launches per run, all on the caller's stream:
+// Three launches per run, all on the caller's stream, each of the last two
+// with programmatic dependent launch:
 //
 //  lp_prepare_kernel (1 CTA of 1024 threads)
 //    validates group_indptr, resolves each group's request (natural
 //    alternatives, explicit ids or argmax only), finishes groups that need no
-//    logits, resets the per-row counters and writes the depth-0 work queue:
-//    row 0 of every group that must be read.
+//    logits, resets the per-row counters, advances the run epoch and writes
+//    the depth-0 work queue: row 0 of every group that must be read.
 //
-//  lp_stream_kernel (persistent, 3 CTAs per SM, launched with programmatic
-//  dependent launch so its set-up overlaps the prepare kernel), CTAs of 10
-//  specialised warps:
-//    - producer warp (one lane): takes work items (queue position, tile) --
+//  lp_stream_kernel (persistent, 3 CTAs per SM, a few slots left to the
+//  record kernel), CTAs of 10 specialised warps:
+//    - producer warp (one lane): claims work items (queue position, tile) --
 //      the depth-0 rows' tiles first, then rows appended after an acceptance
 //      -- and streams each 32 KiB vocabulary tile (16384 BF16 or 8192 FP32
-//      elements) into one of two shared-memory stages with a TMA bulk copy
-//      (cp.async.bulk, mbarrier completion, L2 evict-first);
-//    - 8 compute warps: each reduces its share of a tile to its FP32 max,
-//      the argmax key (atomicMax into the row's best key), the exp-sum (ex2)
-//      relative to its max and, for rows that report natural alternatives,
-//      its elements >= a tile threshold exchanged between the 8 warps (packed
-//      sort keys  key = ord32(x) << 32 | (0xFFFFFFFF - id), ord32 being the
-//      monotone float -> uint map with -0 folded into +0); the partials go to
-//      global memory and the tile to the helper warp through a done slot;
-//    - helper warp: counts every tile for its row, decides a row when its
-//      count completes it (argmax -> greedy acceptance; on acceptance the
-//      next row of the group is appended to the queue, so by default rows
-//      past the accepted prefix are never read), and writes a natural tile's
-//      best 32 keys from the 8 warps' candidates.
+//      elements) into the CTA's stage with a TMA bulk copy (cp.async.bulk,
+//      mbarrier completion, L2 evict-first);
+//    - 8 compute warps: each reduces its share of a tile to its FP32 max, the
+//      argmax key (atomicMax into the row's best key), the exp-sum (ex2)
+//      relative to its max and, for rows that report natural alternatives, a
+//      summary of its 4 largest thread maxima; the partials go to global
+//      memory and the tile to the helper warp through a done slot;
+//    - helper warp: counts every tile for its row and decides a row when its
+//      count completes it (argmax -> greedy acceptance; on acceptance the next
+//      row of the group is appended to the queue, so rows past the accepted
+//      prefix are never read; a requesting row gets a record task).
 //
-//  lp_record_kernel (one CTA per row, dependent launch): for every decided
-//    row of a requesting group, lse = M + log(sum s_t exp(m_t - M)) from the
-//    tile partials, the chosen token's logprob, the top-K natural
-//    alternatives or the explicit-id gather, and the 258-word record.
+//  lp_record_kernel (persistent, scheduled once every stream CTA has started:
+//    it takes the slots the stream grid leaves and those of stream CTAs that
+//    exit): claims record tasks as the deciders append them and builds each
+//    record while the stream kernel runs -- lse = M + log(sum s_t exp(m_t -
+//    M)) from the tile partials, the chosen token's logprob, the top-K
+//    natural alternatives or the explicit-id gather, the 258-word record.
 //
 // Sources: "logprobs-design.md" (generation-logprob contract; the four-launch
 // reduction paragraph: FP32 tile maxima and exponential sums, a per-position
-// normalisation, tiles keeping their best 32 integer sort keys over reported
-// FP32 logprobs and inverse ids, ties from the subtraction included, equal
-// values at the cutoff taking the smallest ids, signed zero normalised, padded
-// lanes excluded, explicit ids gathered from raw logits) and "mtp-design.md"
-// ("A speculative round is a state transaction", steps 2-3).
+// normalisation, best-32 integer sort keys over reported FP32 logprobs and
+// inverse ids, ties from the subtraction included, equal values at the cutoff
+// taking the smallest ids, signed zero normalised, padded lanes excluded,
+// explicit ids gathered from raw logits) and "mtp-design.md" ("A speculative
+// round is a state transaction", steps 2-3).
 //
-// Exactness of the natural alternatives with per-tile top-32 by RAW key:
-// fl32(x - lse) is non-decreasing in x, so the global raw top-32 holds every
-// lane whose logprob exceeds the K-th value L; lanes with logprob == L may sit
-// below it (ties created by the subtraction).  If the 32nd raw key's logprob
-// is below L, every lane with logprob >= L is inside the raw top-32 and a sort
-// of those 32 by (logprob, inverse id) is exact.  Otherwise the lanes equal to
-// L are collected tile by tile in id order; a tile can hide such a lane only
-// if its own 32nd key has logprob == L, and only such tiles are re-read.
+// Exactness of the natural alternatives (natural_record): fl32(x - lse) is
+// non-decreasing in x, so a candidate set holding every lane >= a threshold
+// theta with at least 32 lanes above it holds the row's best K by logprob,
+// except lanes below theta that tie with the K-th value after the
+// subtraction; those exist only if the float just below theta already reports
+// that value, and are then collected in id order.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -110,6 +107,27 @@ __device__ __forceinline__ T vload(const T* p) { return *reinterpret_cast<const 
 template <typename T>
 __device__ __forceinline__ void vstore(T* p, T v) { *reinterpret_cast<volatile T*>(p) = v; }
 
+// Run-tagged words: epoch << 32 | payload.  The tile partials and record tasks
+// that the record kernel reads while the stream kernel still runs are written
+// as pairs of such words with relaxed 64-bit stores (each word is single-copy
+// atomic), and a reader takes a pair only once both words carry the run's
+// epoch: a word still in flight, or left by an earlier run, is never mistaken
+// for this run's.
+__device__ __forceinline__ unsigned long long tagged(uint32_t ep, uint32_t v) {
+    return ((unsigned long long)ep << 32) | (unsigned long long)v;
+}
+__device__ __forceinline__ bool has_epoch(const ulonglong2& w, uint32_t ep) {
+    return (uint32_t)(w.x >> 32) == ep && (uint32_t)(w.y >> 32) == ep;
+}
+__device__ __forceinline__ void st_tagged(ulonglong2* p, unsigned long long a, unsigned long long b) {
+    asm volatile("st.relaxed.gpu.global.v2.b64 [%0], {%1, %2};" ::"l"(p), "l"(a), "l"(b) : "memory");
+}
+__device__ __forceinline__ ulonglong2 ld_tagged(const ulonglong2* p) {
+    ulonglong2 v;
+    asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(v.x), "=l"(v.y) : "l"(p) : "memory");
+    return v;
+}
+
 // ---- optional device timeline (plans created with the trace flag)
 //
 // Each CTA has three event rings (producer, compute, merge warp) of
@@ -118,7 +136,7 @@ enum : unsigned { kTrKernel = 1, kTrClaim, kTrIssue, kTrTileStart, kTrTileEnd, k
                   kTrDecision, kTrMergeEnd, kTrPrepStart, kTrPrepEnd, kTrExit, kTrTileB1, kTrTileB2,
                   kTrWarpAppend, kTrWarpDone, kTrRecStart, kTrRecEnd, kTrRecA, kTrRecB, kTrRecC, kTrRecD };
 
-__shared__ unsigned g_trace_n[3];  // per-CTA event counts (producer, compute, merge)
+__shared__ unsigned g_trace_n[kTraceRoles];  // per-CTA event counts (producer, compute, merge, record)
 
 __device__ __forceinline__ void trace(const Params& p, unsigned type, int row, int tile, bool writer) {
     if (p.trace == nullptr || !writer) return;
@@ -128,20 +146,20 @@ __device__ __forceinline__ void trace(const Params& p, unsigned type, int row, i
     unsigned* cnt = g_trace_n + role;
     const unsigned i = atomicAdd(cnt, 1u);  // several warps may record into one ring
     if (i >= (unsigned)p.trace_cap) return;
-    atomicMax(&p.trace_count[blockIdx.x * 3 + role], i + 1);
-    unsigned long long* e = p.trace + (((size_t)blockIdx.x * 3 + role) * p.trace_cap + i) * 2;
+    atomicMax(&p.trace_count[blockIdx.x * kTraceRoles + role], i + 1);
+    unsigned long long* e = p.trace + (((size_t)blockIdx.x * kTraceRoles + role) * p.trace_cap + i) * 2;
     e[0] = globaltimer();
     e[1] = ((unsigned long long)type << 56) | ((unsigned long long)(row & 0xFFFFFFFF) << 24) |
            (unsigned long long)(tile & 0xFFFFFF);
 }
 
-// Record-kernel events go to the merge-role ring of CTA blockIdx.x (after the
-// stream kernel's events of that CTA).
+// Record-kernel events go to the record-role ring of CTA blockIdx.x.
 __device__ __forceinline__ void rtrace(const Params& p, unsigned type, int row) {
     if (p.trace == nullptr || threadIdx.x != 0 || (int)blockIdx.x >= p.trace_ctas) return;
-    const unsigned i = atomicAdd(&p.trace_count[blockIdx.x * 3 + 2], 1u);
+    const unsigned i = g_trace_n[3]++;  // thread 0 alone records: no round trip on the record's path
     if (i >= (unsigned)p.trace_cap) return;
-    unsigned long long* e = p.trace + (((size_t)blockIdx.x * 3 + 2) * p.trace_cap + i) * 2;
+    atomicMax(&p.trace_count[blockIdx.x * kTraceRoles + 3], i + 1);
+    unsigned long long* e = p.trace + (((size_t)blockIdx.x * kTraceRoles + 3) * p.trace_cap + i) * 2;
     e[0] = globaltimer();
     e[1] = ((unsigned long long)type << 56) | ((unsigned long long)(row & 0xFFFFFFFF) << 24);
 }
@@ -274,7 +292,7 @@ struct Shared {
     uint64_t dfree[kDoneRing];       // done slot: read by the helper warp
     int4 dslot[kDoneRing];           // done slot: (row, queue entry, 0, 0) of the tile
     int sel_exit;                    // compute warps that have finished (the helper stops at 8)
-    unsigned long long wbest[kWarps];  // each warp's last best-key atomic result (an issue dependency)
+    unsigned long long wbest[kWarps];  // each warp's last atomic results (an issue dependency)
     int4 info[kMaxStages];           // work item of each stage
 };
 
@@ -294,7 +312,9 @@ struct RecShared {
     float xlim;                             // prompt scoring: largest logit whose lp is the target's
     int corr;                               // prompt scoring: logits in (target's, xlim]
     uint32_t theta_o;                       // natural: ord32 of the candidate threshold (0: none)
+    int slow;                               // natural: some candidate thread was not prefetched
     uint32_t wtop[kWarps][8];               // natural: each warp's 8 largest summary entry values
+    unsigned long long wsel[kWarps][8];     // natural: those entries (record fast path)
     unsigned long long lkey;                // natural: the keff-th best logprob key
     int n_thr, n_sh, n_keys;                // natural: candidate threads, shares and keys
     int rec[kRecordWords + 2];              // record being assembled
@@ -534,7 +554,7 @@ __device__ __forceinline__ GroupIn load_group(const Params& p, int g) {
 __global__ void __launch_bounds__(1024) lp_prepare_kernel(Params p) {
     asm volatile("griddepcontrol.launch_dependents;");
     if (p.trace != nullptr && threadIdx.x == 0) {
-        unsigned long long* e = p.trace + ((size_t)p.trace_ctas * 3) * p.trace_cap * 2;
+        unsigned long long* e = p.trace + ((size_t)p.trace_ctas * kTraceRoles) * p.trace_cap * 2;
         e[0] = globaltimer();
         e[1] = (unsigned long long)kTrPrepStart << 56;
         e[4] = ~0ull;  // first record-kernel start (atomicMin)
@@ -542,9 +562,16 @@ __global__ void __launch_bounds__(1024) lp_prepare_kernel(Params p) {
         e[6] = 0ull;   // last record-kernel end (atomicMax)
         e[7] = (unsigned long long)kTrRecEnd << 56;
     }
+    if (threadIdx.x == 0) {
+        // the run's epoch: never 0 (zeroed scratch) nor all ones (poisoned scratch)
+        unsigned ep = p.ctrl->epoch + 1u;
+        if (ep == 0xFFFFFFFFu || ep == 0u) ep = 1u;
+        p.ctrl->epoch = ep;
+    }
     __shared__ int s_warp[32];
     __shared__ int s_total;
     __shared__ int s_base;
+    __shared__ unsigned s_chain;  // drafts of the groups that are read: the most rows acceptances can append
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
     const int G = p.G;
@@ -582,12 +609,17 @@ __global__ void __launch_bounds__(1024) lp_prepare_kernel(Params p) {
             p.ctrl->chain_next = 0u;
             p.ctrl->chain_tail = 0u;
             p.ctrl->fresh_rows = 0u;
+            p.ctrl->chain_max = 0u;
             p.ctrl->outstanding = 0;
             p.ctrl->rec_count = 0u;
+            p.ctrl->rec_claim = 0u;
         }
         return;
     }
-    if (tid == 0) s_base = 0;
+    if (tid == 0) {
+        s_base = 0;
+        s_chain = 0u;
+    }
     __syncthreads();
     // without read-ahead a row is decided when its tiles are counted; with it,
     // also only once its parent accepted (depth-0 rows: from the start)
@@ -686,6 +718,7 @@ __global__ void __launch_bounds__(1024) lp_prepare_kernel(Params p) {
             p.queue[s_base + s_warp[warp] + pos_in_warp] =
                 queue_entry(g << 4, row0, mode0) | (k0 >= 1 ? kEntryNext : 0ull);
             p.done[row0] = parent_bias;
+            if (k0 > 0) atomicAdd(&s_chain, (unsigned)k0);
         }
         __syncthreads();
         if (tid == 0) s_base += s_total;
@@ -693,11 +726,11 @@ __global__ void __launch_bounds__(1024) lp_prepare_kernel(Params p) {
     }
     if (st) atomicOr(p.status, st);
     if (p.trace != nullptr) {
-        for (int i = tid; i < p.trace_ctas * 3; i += nthr) p.trace_count[i] = 0u;
+        for (int i = tid; i < p.trace_ctas * kTraceRoles; i += nthr) p.trace_count[i] = 0u;
     }
     if (tid == 0) {
         if (p.trace != nullptr) {
-            unsigned long long* e = p.trace + ((size_t)p.trace_ctas * 3) * p.trace_cap * 2;
+            unsigned long long* e = p.trace + ((size_t)p.trace_ctas * kTraceRoles) * p.trace_cap * 2;
             e[2] = globaltimer();
             e[3] = (unsigned long long)kTrPrepEnd << 56;
         }
@@ -705,8 +738,10 @@ __global__ void __launch_bounds__(1024) lp_prepare_kernel(Params p) {
         p.ctrl->chain_next = 0u;
         p.ctrl->chain_tail = 0u;
         p.ctrl->fresh_rows = static_cast<unsigned>(s_base);
+        p.ctrl->chain_max = s_chain;
         p.ctrl->outstanding = s_base;
         p.ctrl->rec_count = 0u;
+        p.ctrl->rec_claim = 0u;
         p.ctrl->abort = 0u;
     }
 }
@@ -723,6 +758,15 @@ __global__ void __launch_bounds__(1024) lp_prepare_kernel(Params p) {
 // entry of its row is published.  Single-item claims spread a row's tiles over
 // many CTAs.
 constexpr unsigned kNone = 0xFFFFFFFFu;
+// Stream-CTA slots of the device left to the record kernel from the start of a run.
+#ifndef LP_RECORD_SLOTS
+#define LP_RECORD_SLOTS 24
+#endif
+// 0: stream CTAs exit only when no chained item can come; k > 0: also when the
+// waiting chained claims cover k/4 of the next row of every outstanding group.
+#ifndef LP_SURPLUS_EXIT
+#define LP_SURPLUS_EXIT 0
+#endif
 // A producer reads ahead only after waiting this long for a chained item.
 #ifndef LP_READ_AHEAD_IDLE_NS
 #define LP_READ_AHEAD_IDLE_NS 1000
@@ -747,8 +791,29 @@ __device__ __noinline__ void producer_loop(const Params& p, Shared& sm, unsigned
     unsigned long long idle_t0 = 0;   // start of the current wait for a chained item (0: not waiting)
     unsigned fresh_ahead = atomicAdd(&ctrl->fresh_next, 1u);
     const unsigned F = vload(&ctrl->fresh_rows);
+    const unsigned CM = vload(&ctrl->chain_max);
     const unsigned fresh_items = F * T;
+    // A chained claim at or past CM rows can never be taken (no more rows can
+    // be appended): once this producer holds one it has no work left, and
+    // (without read-ahead) its CTA exits, which leaves the multiprocessor to
+    // the record kernel.
     bool fresh_done = fresh_ahead >= fresh_items;
+    bool chains_over = false;
+    // Retiring early (LP_SURPLUS_EXIT): a producer whose last poll found the
+    // chained claims already waiting to cover the next row of every outstanding
+    // group (scaled) takes no new claim, and its CTA exits.
+    bool surplus = false;
+    auto claim_chain = [&]() {
+        if (LP_SURPLUS_EXIT && surplus && fresh_done && !p.read_ahead) {
+            chains_over = true;
+            return;
+        }
+        chain_claim = atomicAdd(&ctrl->chain_next, 1u);
+        if (chain_claim / T >= CM) {
+            chain_claim = kNone;
+            chains_over = true;
+        }
+    };
     unsigned long long fresh_entry = fresh_done ? ~0ull : vload(&p.queue[fresh_ahead / T]);
     int stage = 0;
     uint32_t phase = 0;
@@ -778,6 +843,10 @@ __device__ __noinline__ void producer_loop(const Params& p, Shared& sm, unsigned
                 unsigned long long ce = ~0ull;
                 if (cpos < (unsigned)p.rows) ce = vload(&p.queue[cpos]);
                 const int out = fresh_done ? vload(&ctrl->outstanding) : 1;
+                if (LP_SURPLUS_EXIT && fresh_done) {
+                    const long long waiting = (long long)vload(&ctrl->chain_next) - (long long)vload(&ctrl->chain_tail) * T;
+                    surplus = waiting * 4 >= (long long)(out > 0 ? out : 0) * T * LP_SURPLUS_EXIT;
+                }
                 // the chained item, once the queue entry of its row is published
                 if ((long long)ce >= 0) {
                     e = ce;
@@ -804,9 +873,13 @@ __device__ __noinline__ void producer_loop(const Params& p, Shared& sm, unsigned
                     if (!fresh_done) fresh_entry = vload(&p.queue[fresh_ahead / T]);
                     continue;
                 }
-                if (chain_claim == kNone) {
-                    chain_claim = atomicAdd(&ctrl->chain_next, 1u);
+                if (chain_claim == kNone && !chains_over) {
+                    claim_chain();
                     continue;
+                }
+                if (chains_over && !p.read_ahead) {
+                    e = ~0ull;
+                    break;
                 }
                 // nothing to take yet.  After a while without chained items
                 // (their queue has run dry, the verify chains are the work
@@ -874,7 +947,7 @@ __device__ __noinline__ void producer_loop(const Params& p, Shared& sm, unsigned
         }
         // the next chained claim, and the next fresh item with its entry (depth-0
         // entries are all published), overlapping the next stage wait
-        if (chain_claim == kNone) chain_claim = atomicAdd(&ctrl->chain_next, 1u);
+        if (chain_claim == kNone && !chains_over) claim_chain();
         if (!fresh_done && fresh_ahead == kNone) {
             fresh_ahead = atomicAdd(&ctrl->fresh_next, 1u);
             fresh_done = fresh_ahead >= fresh_items;
@@ -937,7 +1010,7 @@ __device__ __forceinline__ T merge_lists(T a, T b, int lane) {
     return warp_bitonic_clean_desc(rev > a ? rev : a, lane);
 }
 
-__device__ __noinline__ bool decide_row(const Params& p, int2* cur);
+__device__ __noinline__ bool decide_row(const Params& p, int2* cur, uint32_t ep);
 
 // The compute warp's share of one tile: passes, the summary of its thread
 // maxima (natural tiles), its partial results published to global memory
@@ -950,12 +1023,12 @@ __device__ __noinline__ bool decide_row(const Params& p, int2* cur);
 template <int ELT, bool FULL, bool SCORE>
 __device__ __forceinline__ bool tile_work(const Params& p, Shared& sm, const unsigned char* sp, int nv, int tbase,
                                           const int4& info, int stage, int& ds, uint32_t& dphase,
-                                          unsigned long long deadline) {
+                                          unsigned long long deadline, uint32_t ep) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int mode = info.w;
     const bool natural = mode == kModeNatural;
     const long long tslot = (long long)info.x * p.T + info.y;
-    // prompt scoring: the target's logit, loaded now and used after the passes
+    // prompt scoring: the target's logit, loaded now and used after pass 1
     float xt = 0.0f;
     if (SCORE && lane == 0) xt = load_logit<ELT>(p, info.x, __ldg(&p.targets[info.x]));
     // pass 1: maxima (per vector for a full tile)
@@ -972,19 +1045,17 @@ __device__ __forceinline__ bool tile_work(const Params& p, Shared& sm, const uns
     // handed over (below), long after it returned
     unsigned long long prev_best = 0ull;
     if (lane == 0) prev_best = atomicMax(&p.row_best[info.x], wkey);
+    // Partials that the record kernel reads are published with atomic
+    // exchanges issued here and waited for before the tile is handed over
+    // (below), so they are performed at their point of coherence before the
+    // tile is counted, like the best key; their latency overlaps pass 2.  (The
+    // (max, exp-sum) pair, known only after pass 2, is run-tagged instead.)
+    unsigned long long prev_pub = 0ull;
     if (natural) {
         // the warp's four largest thread maxima, with their positions
         const unsigned long long e =
             warp_summary(m > kNegInf ? om : 0u, lane, ((uint32_t)info.y << 8) | (uint32_t)(warp * 32));
-        if (lane < 4) p.part_keys[tslot * kKeysPerTile + warp * 4 + lane] = e;
-    }
-    // pass 2: sum exp(x - m) = 2^(x*log2e - mb - mb_lo): mb_lo, the rounding
-    // residual of m*log2e, is applied once, so large |m| costs no accuracy
-    float s = 0.0f;
-    if (mode != kModeArgmax && m > kNegInf) {
-        const float mb = m * kLog2e;
-        const float mb_lo = fmaf(m, kLog2e, -mb);
-        s = stage_expsum<ELT, FULL>(sp, tid, nv, mb) * ex2(-mb_lo);
+        if (lane < 4) prev_pub = atomicExch(&p.part_keys[tslot * kKeysPerTile + warp * 4 + lane], e);
     }
     if constexpr (SCORE) {
         if (natural) {
@@ -1012,8 +1083,18 @@ __device__ __forceinline__ bool tile_work(const Params& p, Shared& sm, const uns
             }
             cnt = (int)__reduce_add_sync(kFull, (unsigned)cnt);
             mn = warp_min_f(mn);
-            if (lane == 0) p.part_rank[tslot * kWarps + warp] = make_int2(cnt, (int)__float_as_uint(mn));
+            if (lane == 4)
+                prev_pub = atomicExch(reinterpret_cast<unsigned long long*>(&p.part_rank[tslot * kWarps + warp]),
+                                      ((unsigned long long)__float_as_uint(mn) << 32) | (uint32_t)cnt);
         }
+    }
+    // pass 2: sum exp(x - m) = 2^(x*log2e - mb - mb_lo): mb_lo, the rounding
+    // residual of m*log2e, is applied once, so large |m| costs no accuracy
+    float s = 0.0f;
+    if (mode != kModeArgmax && m > kNegInf) {
+        const float mb = m * kLog2e;
+        const float mb_lo = fmaf(m, kLog2e, -mb);
+        s = stage_expsum<ELT, FULL>(sp, tid, nv, mb) * ex2(-mb_lo);
     }
     // partial results of the warp, then the tile goes to the helper warp
     // through a done slot: once the 8 warps arrived, it counts the tile for
@@ -1024,17 +1105,21 @@ __device__ __forceinline__ bool tile_work(const Params& p, Shared& sm, const uns
     const float Mw = unord32(omx);
     const float sc = (m > kNegInf && mode != kModeArgmax) ? s * ex2((m - Mw) * kLog2e) : 0.0f;
     const float sw = warp_sum_f(sc);
-    if (lane == 0) p.part_ms[tslot * kWarps + warp] = make_float2(Mw, sw);
+    if (lane == 0)
+        st_tagged(&p.part_ms[tslot * kWarps + warp], tagged(ep, __float_as_uint(Mw)), tagged(ep, __float_as_uint(sw)));
+    // every lane's exchange result, gathered (a warp-wide reduction waits for all of them)
+    const uint32_t pub = __reduce_or_sync(kFull, (uint32_t)prev_pub ^ (uint32_t)(prev_pub >> 32));
     if (__any_sync(kFull, !mbar_wait(&sm.dfree[ds], (dphase >> ds) & 1u, deadline))) {  // slot read
         if (lane == 0) atomicOr(p.status, kStatusTimeout);
         return false;
     }
     if (lane == 0) {
         if (warp == 0) sm.dslot[ds] = make_int4(info.x, info.z, 0, 0);
-        // the best-key update must have returned (so it is performed at its
-        // point of coherence) before the count that follows the arrival: the
-        // store of its result cannot issue before the result is back
-        sm.wbest[warp] = prev_best;
+        // the best-key update and the exchanges must have returned (so they are
+        // performed at their point of coherence) before the count that follows
+        // the arrival: the store of their results cannot issue before the
+        // results are back
+        sm.wbest[warp] = prev_best ^ pub;
         mbar_arrive(&sm.dfull[ds]);
     }
     dphase ^= 1u << ds;
@@ -1049,7 +1134,7 @@ __device__ __forceinline__ bool tile_work(const Params& p, Shared& sm, const uns
 // natural-alternative tiles, where the 8 warp thresholds and candidates are
 // exchanged through a candidate slot (bounded mbarrier waits).
 template <int ELT, bool SCORE>
-__device__ void compute_loop(const Params& p, Shared& sm, unsigned char* stages, unsigned long long t0) {
+__device__ void compute_loop(const Params& p, Shared& sm, unsigned char* stages, unsigned long long t0, uint32_t ep) {
     constexpr int S = StageCfg<ELT>::kStages;
     constexpr int kTE = tile_elems<ELT>();
     const int tid = threadIdx.x, lane = tid & 31;
@@ -1073,10 +1158,10 @@ __device__ void compute_loop(const Params& p, Shared& sm, unsigned char* stages,
         trace(p, kTrTileStart, info.x, tile, tid == 0);
         bool ok;
         if (__builtin_expect(nv == kTE, 1)) {
-            ok = tile_work<ELT, true, SCORE>(p, sm, sp, nv, tbase, info, stage, ds, dphase, deadline);
+            ok = tile_work<ELT, true, SCORE>(p, sm, sp, nv, tbase, info, stage, ds, dphase, deadline, ep);
         } else {
             fill_partial<ELT>(stages + (size_t)stage * kTileBytes, tid, nv);
-            ok = tile_work<ELT, false, SCORE>(p, sm, sp, nv, tbase, info, stage, ds, dphase, deadline);
+            ok = tile_work<ELT, false, SCORE>(p, sm, sp, nv, tbase, info, stage, ds, dphase, deadline, ep);
         }
         if (!ok) return;
         trace(p, kTrTileEnd, info.x, tile, tid == 0);
@@ -1099,7 +1184,7 @@ __device__ void compute_loop(const Params& p, Shared& sm, unsigned char* stages,
 // requesting row is flagged for the record kernel.  Returns true, with *cur
 // advanced to the next row, when read-ahead had already counted every tile of
 // that row: the caller decides it too.
-__device__ __noinline__ bool decide_row(const Params& p, int2* cur) {
+__device__ __noinline__ bool decide_row(const Params& p, int2* cur, uint32_t ep) {
     const unsigned T = (unsigned)p.T;
     const unsigned fresh_rows = vload(&p.ctrl->fresh_rows);
     const int row = cur->x, entry = cur->y;
@@ -1135,11 +1220,13 @@ __device__ __noinline__ bool decide_row(const Params& p, int2* cur) {
             for (int jj = j + 1; jj <= k; ++jj) p.emitted[r0 + jj] = -1;
         }
     }
-    if (req) {  // the record kernel builds it
+    if (req) {  // a record task for the record kernel (or the sharded kernels)
         if (chosen >= p.V) atomicOr(p.status, kStatusBadToken);
         const unsigned i = atomicAdd(&p.ctrl->rec_count, 1u);
         const int is_amax = (k == 0 && samp >= 0) ? 0 : 1;  // the chosen logit is then the row maximum
-        p.rec_tasks[i] = make_int4(chosen, row, (d.y & 0x3FFF) | (is_amax << 14) | (d.z << 16), g);
+        const uint32_t dw = (uint32_t)((d.y & 0x3FFF) | (is_amax << 14) | (d.z << 16));
+        st_tagged(&p.rec_tasks[2 * (size_t)i], tagged(ep, (uint32_t)chosen), tagged(ep, (uint32_t)row));
+        st_tagged(&p.rec_tasks[2 * (size_t)i + 1], tagged(ep, dw), tagged(ep, (uint32_t)g));
     }
     trace(p, kTrDecision, row, accept ? 1 : 0, true);
     if (!accept) {
@@ -1163,13 +1250,14 @@ __device__ __noinline__ bool decide_row(const Params& p, int2* cur) {
 // its done-slot arrival, so the update has been performed at the key's
 // point of coherence (the L2 slice that owns it) before the count is issued,
 // and the decider reads the key with an atomic at that same point after its
-// own count returned.  The outputs of a decision and the tile partials are
-// read by the record kernel, after this grid has completed.  (An acquire-
+// own count returned.  The record kernel reads the tile partials and record
+// tasks while this grid runs: they are run-tagged, or were performed before
+// their tiles were counted (see tile_work).  (An acquire-
 // release count gives the same order through the memory model, but its fence
 // waits for the multiprocessor's outstanding memory traffic, which made the
 // helper's per-tile counts the bottleneck.)
 template <int ELT>
-__device__ __noinline__ void helper_loop(const Params& p, Shared& sm, unsigned long long deadline) {
+__device__ __noinline__ void helper_loop(const Params& p, Shared& sm, unsigned long long deadline, uint32_t ep) {
     const int lane = threadIdx.x & 31;
     int ds = 0;
     uint32_t dphase = 0;
@@ -1187,7 +1275,7 @@ __device__ __noinline__ void helper_loop(const Params& p, Shared& sm, unsigned l
             if (++ds == kDoneRing) ds = 0;
             if (lane == 0 && old == p.done_last) {
                 int2 cur = make_int2(d.x, d.y);
-                while (decide_row(p, &cur)) {
+                while (decide_row(p, &cur, ep)) {
                 }
             }
             __syncwarp();
@@ -1229,9 +1317,12 @@ __global__ void __launch_bounds__(kThreads, StageCfg<ELT>::kMinBlocks) lp_stream
     }
     __syncthreads();
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    // the record kernel may be scheduled now; it waits for this grid to complete
+    // the record kernel may be scheduled now (the prepare kernel's writes are
+    // visible): its CTAs take the multiprocessor room this grid leaves, and
+    // more as its CTAs exit, and build each record as its task appears
     asm volatile("griddepcontrol.launch_dependents;");
     if (vload(&p.ctrl->abort) != 0u) return;
+    const uint32_t ep = vload(&p.ctrl->epoch);
     const unsigned long long t0 = globaltimer();
     trace(p, kTrKernel, 0, 0, tid == 0);
     const int warp = tid >> 5;
@@ -1240,10 +1331,10 @@ __global__ void __launch_bounds__(kThreads, StageCfg<ELT>::kMinBlocks) lp_stream
         return;
     }
     if (warp == kWarps + 1) {
-        helper_loop<ELT>(p, sm, t0 + p.timeout_ns);
+        helper_loop<ELT>(p, sm, t0 + p.timeout_ns, ep);
         return;
     }
-    compute_loop<ELT, SCORE>(p, sm, stages, t0);
+    compute_loop<ELT, SCORE>(p, sm, stages, t0, ep);
     if ((tid & 31) == 0) {
         __threadfence_block();  // this warp's slot arrivals come first
         atomicAdd(&sm.sel_exit, 1);
@@ -1361,8 +1452,8 @@ __device__ __noinline__ void natural_exact(const Params& p, RecShared& sm, int r
     cbar();
 }
 
-// Up to kCachedShares warp shares per thread stay in registers between the
-// threshold and the candidate steps; further ones are loaded again.
+// The record's fast path keeps up to kCachedShares warp shares per thread in
+// registers (rows of up to 32 * kCachedShares tiles).
 constexpr int kCachedShares = 2;
 
 // Step 1 (before the record's first barrier): thread (w, lane) takes the
@@ -1371,17 +1462,12 @@ constexpr int kCachedShares = 2;
 // values is a threshold with at least 32 entries at or above it.
 constexpr int kWarpTop = 8;
 __device__ __forceinline__ void summary_top(const Params& p, RecShared& sm, long long base, const Span& sp, int warp,
-                                            int lane, unsigned long long (&cache)[kCachedShares][4]) {
+                                            int lane) {
     uint32_t top[4] = {0u, 0u, 0u, 0u};  // this thread's 4 largest entry values, descending
-    int i = 0;
-    for (int t = sp.t0 + lane; t < sp.t1; t += 32, ++i) {
+    for (int t = sp.t0 + lane; t < sp.t1; t += 32) {
         const ulonglong2* q = reinterpret_cast<const ulonglong2*>(p.part_keys + (base + t) * kKeysPerTile + warp * 4);
         const ulonglong2 a = __ldcg(q), b = __ldcg(q + 1);
         const unsigned long long e[4] = {a.x, a.y, b.x, b.y};
-        if (i < kCachedShares) {
-#pragma unroll
-            for (int r = 0; r < 4; ++r) cache[i][r] = e[r];
-        }
 #pragma unroll
         for (int r = 0; r < 4; ++r) {  // insert
             uint32_t v = (uint32_t)(e[r] >> 32);
@@ -1392,10 +1478,6 @@ __device__ __forceinline__ void summary_top(const Params& p, RecShared& sm, long
                 v = lo;
             }
         }
-    }
-    for (; i < kCachedShares; ++i) {
-#pragma unroll
-        for (int r = 0; r < 4; ++r) cache[i][r] = 0ull;
     }
     // the warp's 8 largest: knock out the largest head eight times.  A thread
     // keeps only its own 4 largest; if it held more of the warp's 8, smaller
@@ -1415,12 +1497,66 @@ __device__ __forceinline__ void summary_top(const Params& p, RecShared& sm, long
     }
 }
 
+// Steps 4-5 of a natural selection, once sm.ckeys[0, sm.n_keys) holds the
+// logprob keys of every lane >= theta (sm.theta_o, 0: every lane of the span)
+// and the block has synchronised: the best keff keys by rank into the record's
+// pairs, then the subtraction-tie check across theta.
+template <int ELT>
+__device__ __noinline__ void natural_rank(const Params& p, RecShared& sm, int row, const Span& sp, int keff, float lse) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t th = sm.theta_o;
+    const float theta = th ? unord32(th) : kNegInf;
+    if (sm.n_keys > kCandKeys) {
+        natural_exact<ELT>(p, sm, row, sp, keff, lse);
+        return;
+    }
+    // 4. the best keff keys by rank (keys are distinct: they carry the id)
+    const int nk = sm.n_keys;
+    for (int j = nk + tid; j < ((nk + 7) & ~7); j += kConsumerThreads) sm.ckeys[j] = 0ull;  // pad to 8
+    cbar();
+    for (int i = tid; i < nk; i += kConsumerThreads) {
+        const unsigned long long k = sm.ckeys[i];
+        int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+        for (int j = 0; j < nk; j += 8) {
+            const ulonglong2 a = *reinterpret_cast<const ulonglong2*>(&sm.ckeys[j]);
+            const ulonglong2 b = *reinterpret_cast<const ulonglong2*>(&sm.ckeys[j + 2]);
+            const ulonglong2 c = *reinterpret_cast<const ulonglong2*>(&sm.ckeys[j + 4]);
+            const ulonglong2 d = *reinterpret_cast<const ulonglong2*>(&sm.ckeys[j + 6]);
+            r0 += (a.x > k) + (a.y > k);
+            r1 += (b.x > k) + (b.y > k);
+            r2 += (c.x > k) + (c.y > k);
+            r3 += (d.x > k) + (d.y > k);
+        }
+        const int rank = r0 + r1 + r2 + r3;
+        if (rank < keff) {
+            sm.rec[2 + 2 * rank] = (int)key_id(k);
+            sm.rec[3 + 2 * rank] = (int)__float_as_uint(key_value(k));
+            if (rank == keff - 1) sm.lkey = k;
+        }
+    }
+    cbar();
+    // 5. lanes below theta can tie with the K-th logprob only if the float just
+    // below theta already reports it
+    const float L = key_value(sm.lkey);
+    if (th != 0u && logprob(nextafterf(theta, kNegInf), lse) == L) {
+        if (tid == 0) sm.n_thr = 0;
+        cbar();
+        int gt = 0;
+        for (int i = tid; i < nk; i += kConsumerThreads) gt += key_value(sm.ckeys[i]) > L;
+        gt = (int)__reduce_add_sync(kFull, (unsigned)gt);
+        if (lane == 0 && gt) atomicAdd(&sm.n_thr, gt);
+        cbar();
+        if (warp == 0) fill_equal_lanes<ELT>(p, sm.rec, row, sp, lse, L, sm.n_thr, keff, lane);
+        cbar();
+    }
+}
+
 // Steps 2-5, all 256 threads, after warp 0 has set sm.theta_o (0: every lane
 // is a candidate) and sm.lse: candidates, their logprob keys, the best keff by
 // rank, the subtraction-tie check.  Writes the natural pairs into sm.rec.
 template <int ELT>
 __device__ __noinline__ void natural_record(const Params& p, RecShared& sm, int row, long long base, const Span& sp,
-                                            int keff, const unsigned long long (&cache)[kCachedShares][4]) {
+                                            int keff) {
     constexpr int TE = tile_elems<ELT>(), EPV = 16 / ELT, NCH = TileLayout<ELT>::NCH;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const float lse = sm.lse;
@@ -1445,10 +1581,7 @@ __device__ __noinline__ void natural_record(const Params& p, RecShared& sm, int 
         int i = 0;
         for (int t = sp.t0 + lane; t < sp.t1; t += 32, ++i) {
             unsigned long long e[4];
-            if (i < kCachedShares) {
-#pragma unroll
-                for (int r = 0; r < 4; ++r) e[r] = cache[i][r];
-            } else {
+            {
                 const ulonglong2* q = reinterpret_cast<const ulonglong2*>(p.part_keys + (base + t) * kKeysPerTile + warp * 4);
                 const ulonglong2 a = __ldcg(q), b = __ldcg(q + 1);
                 e[0] = a.x; e[1] = a.y; e[2] = b.x; e[3] = b.y;
@@ -1531,45 +1664,7 @@ __device__ __noinline__ void natural_record(const Params& p, RecShared& sm, int 
         natural_exact<ELT>(p, sm, row, sp, keff, lse);
         return;
     }
-    // 4. the best keff keys by rank (keys are distinct: they carry the id)
-    const int nk = sm.n_keys;
-    for (int j = nk + tid; j < ((nk + 7) & ~7); j += kConsumerThreads) sm.ckeys[j] = 0ull;  // pad to 8
-    cbar();
-    for (int i = tid; i < nk; i += kConsumerThreads) {
-        const unsigned long long k = sm.ckeys[i];
-        int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
-        for (int j = 0; j < nk; j += 8) {
-            const ulonglong2 a = *reinterpret_cast<const ulonglong2*>(&sm.ckeys[j]);
-            const ulonglong2 b = *reinterpret_cast<const ulonglong2*>(&sm.ckeys[j + 2]);
-            const ulonglong2 c = *reinterpret_cast<const ulonglong2*>(&sm.ckeys[j + 4]);
-            const ulonglong2 d = *reinterpret_cast<const ulonglong2*>(&sm.ckeys[j + 6]);
-            r0 += (a.x > k) + (a.y > k);
-            r1 += (b.x > k) + (b.y > k);
-            r2 += (c.x > k) + (c.y > k);
-            r3 += (d.x > k) + (d.y > k);
-        }
-        const int rank = r0 + r1 + r2 + r3;
-        if (rank < keff) {
-            sm.rec[2 + 2 * rank] = (int)key_id(k);
-            sm.rec[3 + 2 * rank] = (int)__float_as_uint(key_value(k));
-            if (rank == keff - 1) sm.lkey = k;
-        }
-    }
-    cbar();
-    // 5. lanes below theta can tie with the K-th logprob only if the float just
-    // below theta already reports it
-    const float L = key_value(sm.lkey);
-    if (th != 0u && logprob(nextafterf(theta, kNegInf), lse) == L) {
-        if (tid == 0) sm.n_thr = 0;
-        cbar();
-        int gt = 0;
-        for (int i = tid; i < nk; i += kConsumerThreads) gt += key_value(sm.ckeys[i]) > L;
-        gt = (int)__reduce_add_sync(kFull, (unsigned)gt);
-        if (lane == 0 && gt) atomicAdd(&sm.n_thr, gt);
-        cbar();
-        if (warp == 0) fill_equal_lanes<ELT>(p, sm.rec, row, sp, lse, L, sm.n_thr, keff, lane);
-        cbar();
-    }
+    natural_rank<ELT>(p, sm, row, sp, keff, lse);
 }
 
 // Prompt scoring: the largest float X with fl32(X - lse) <= lp, where lp =
@@ -1602,13 +1697,41 @@ __device__ __forceinline__ void ms_merge(float& m, float& s, float m2, float s2)
     m = M;
 }
 
-// Record of a requested, emitted row, built by one CTA of 256 threads: lse from
-// the tile partials, the chosen pair, then the explicit-id gather or the
-// natural alternatives.  Every global load is issued before the first barrier.
+// A (max, exp-sum) tile partial of this run, by its words as loaded: it was
+// written before its tile was counted, so it has landed or is about to; waits
+// (bounded) until both words carry the run's epoch.
+__device__ __noinline__ ulonglong2 part_ms_wait(const Params& p, long long i, ulonglong2 v, uint32_t ep,
+                                                unsigned long long deadline) {
+    while (!has_epoch(v, ep)) {
+        if (globaltimer() > deadline) {
+            atomicOr(p.status, kStatusTimeout);
+            break;
+        }
+        v = ld_tagged(&p.part_ms[i]);
+    }
+    return v;
+}
+
+// Record of a requested, emitted row, built by one CTA of 256 threads.
+//
+// Every independent load is issued first (the tile partials, the summary
+// entries, the chosen logit, the explicit ids; the explicit ids' logits as
+// soon as the ids arrive).  Each warp then reduces its partials (maximum
+// first, then the rescaled sums) and, for natural rows, finds the 8 largest
+// summary entries of its warp column and starts loading those threads'
+// vectors, so the candidate gather is in flight across the block barrier.
+// After the barrier every warp derives the same lse and threshold theta from
+// the warps' results (same operations in the same order, so the same bits),
+// keeps the prefetched lanes >= theta as logprob keys and checks that its
+// column has no candidate thread outside the 8 it loaded (no other entry >=
+// theta, no warp share whose 4th entry reaches theta); if any warp finds one,
+// the block takes the general path of natural_record.
 // SCORE: the prompt-scoring record (rank, 43 words) instead of the 258-word one.
 template <int ELT, bool SCORE>
 __device__ __noinline__ void record_block(const Params& p, RecShared& sm, int row, int g, int chosen, int dy,
-                                          int kc) {
+                                          int kc, uint32_t ep, unsigned long long deadline) {
+    constexpr int TE = tile_elems<ELT>(), EPV = 16 / ELT;
+    static_assert(TileLayout<ELT>::NCH == 8, "four lanes load a thread's 8 vectors, two each");
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int mode = (dy >> 8) & 3, ids = (dy >> 12) & 1;
     const bool chosen_is_max = ((dy >> 14) & 1) != 0;  // its logit is the row maximum
@@ -1616,36 +1739,129 @@ __device__ __noinline__ void record_block(const Params& p, RecShared& sm, int ro
     const long long base = (long long)row * T;
     const bool natural = !ids && mode == kModeNatural && kc > 0;
     constexpr bool score = SCORE;
+    const unsigned char* rowp = reinterpret_cast<const unsigned char*>(p.logits) + (long long)row * p.Vp * ELT;
+    // ---- every independent load, issued together
+    int id = -1;
+    if (ids && tid < kc) id = __ldg(&p.token_ids[(long long)g * kMaxIds + tid]);
+    float xc = 0.0f;
+    if (tid == 32 && !chosen_is_max && chosen >= 0 && chosen < p.V) xc = load_logit<ELT>(p, row, chosen);
+    const int np = T * kWarps;  // one (max, exp-sum) per warp of each tile
+    ulonglong2 v[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+        if (tid + u * kConsumerThreads < np) v[u] = ld_tagged(&p.part_ms[base * kWarps + tid + u * kConsumerThreads]);
+    // summary entries of warp column `warp`: tiles lane and lane + 32
+    ulonglong2 ca[kCachedShares], cb[kCachedShares];
+#pragma unroll
+    for (int i = 0; i < kCachedShares; ++i) {
+        const int t = lane + 32 * i;
+        ca[i] = cb[i] = make_ulonglong2(0ull, 0ull);
+        if (natural && t < T) {
+            const ulonglong2* q = reinterpret_cast<const ulonglong2*>(p.part_keys + (base + t) * kKeysPerTile + warp * 4);
+            ca[i] = __ldcg(q);
+            cb[i] = __ldcg(q + 1);
+        }
+    }
+    // the explicit ids' logits, once the ids are back
+    float xi = 0.0f;
+    if (ids && tid < kc && id >= 0 && id < p.V) xi = load_logit<ELT>(p, row, id);
     for (int w = tid; w < kRecordWords; w += kConsumerThreads)
         sm.rec[w] = (w >= 2 && (w & 1) == 0) ? -1 : (int)kUnusedBits;
     if (tid == 0) {
         sm.corr = 0;
         sm.n_thr = sm.n_sh = sm.n_keys = 0;
+        sm.slow = 0;
     }
-    // loads: tile partials, the chosen logit, explicit-id logits, summary entries
+    // ---- (max, exp-sum) of the thread's partials, then of the warp's
     float m = kNegInf, s = 0.0f;
     int above = 0;  // prompt scoring: logits above the target's
-    for (int t = tid; t < T * kWarps; t += kConsumerThreads) {  // one (max, exp-sum) per warp of each tile
-        const float2 ms = __ldcg(&p.part_ms[base * kWarps + t]);
-        ms_merge(m, s, ms.x, ms.y);
-        if (score) above += __ldcg(&p.part_rank[base * kWarps + t]).x;
+    for (int t0 = tid; t0 < np; t0 += 2 * kConsumerThreads) {
+        if (t0 != tid) {  // beyond the first two per thread (more than 64 tiles)
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+                if (t0 + u * kConsumerThreads < np) v[u] = ld_tagged(&p.part_ms[base * kWarps + t0 + u * kConsumerThreads]);
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int t = t0 + u * kConsumerThreads;
+            if (t >= np) break;
+            const ulonglong2 ms = has_epoch(v[u], ep) ? v[u] : part_ms_wait(p, base * kWarps + t, v[u], ep, deadline);
+            ms_merge(m, s, __uint_as_float((uint32_t)ms.x), __uint_as_float((uint32_t)ms.y));
+            if (score) above += __ldcg(&p.part_rank[base * kWarps + t]).x;
+        }
+    }
+    {
+        // the warp's maximum first, then one rescaled sum
+        const uint32_t om = __reduce_max_sync(kFull, ord32(__fadd_rn(m, 0.0f)));
+        const float Mw = unord32(om);
+        float sc = (m > kNegInf) ? s * ex2((m - Mw) * kLog2e) : 0.0f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sc += __shfl_xor_sync(kFull, sc, o);
+        m = Mw;
+        s = sc;
     }
     if (score) above = (int)__reduce_add_sync(kFull, (unsigned)above);
-    float xc = 0.0f;
-    if (tid == 32 && !chosen_is_max && chosen >= 0 && chosen < p.V) xc = load_logit<ELT>(p, row, chosen);
-    int id = -1;
-    float xi = 0.0f;
-    if (ids && tid < kc) {
-        id = __ldg(&p.token_ids[(long long)g * kMaxIds + tid]);
-        if (id >= 0 && id < p.V) xi = load_logit<ELT>(p, row, id);
-    }
-    unsigned long long cache[kCachedShares][4];
-    const Span whole = {0, T, 0, p.V};
-    if (natural) summary_top(p, sm, base, whole, warp, lane, cache);
+    // ---- natural: the warp column's 8 largest summary entries (lane r < 8
+    // keeps entry r), and their threads' vectors, loaded now
+    unsigned long long mine = 0ull;
+    uint32_t cv[kCachedShares][4];  // the entries' values, kept for the completeness check
+    uint4 pv[2];
+    long long pv0[2];
+    if (natural) {
+        // a share's 4 entries are stored largest first; a lane with two tiles
+        // (rows of more than 32 tiles) merges them into its 4 largest
+        unsigned long long top[4] = {ca[0].x, ca[0].y, cb[0].x, cb[0].y};
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float m2 = __shfl_xor_sync(kFull, m, o), s2 = __shfl_xor_sync(kFull, s, o);
-        ms_merge(m, s, m2, s2);
+        for (int i = 0; i < kCachedShares; ++i) {
+            cv[i][0] = (uint32_t)(ca[i].x >> 32);
+            cv[i][1] = (uint32_t)(ca[i].y >> 32);
+            cv[i][2] = (uint32_t)(cb[i].x >> 32);
+            cv[i][3] = (uint32_t)(cb[i].y >> 32);
+        }
+        if (lane + 32 < T) {
+            const unsigned long long ent[4] = {ca[1].x, ca[1].y, cb[1].x, cb[1].y};
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                unsigned long long x = ent[r];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const unsigned long long hi = x > top[k] ? x : top[k], lo = x > top[k] ? top[k] : x;
+                    top[k] = hi;
+                    x = lo;
+                }
+            }
+        }
+        // knock out the largest head eight times; the winning lane writes its
+        // entry (a lane holding more than 4 of the column's 8 largest gives
+        // smaller ones instead: still 8 distinct entries, all the threshold needs)
+        uint32_t hv = (uint32_t)(top[0] >> 32);
+#pragma unroll
+        for (int r = 0; r < kWarpTop; ++r) {
+            const uint32_t vmax = __reduce_max_sync(kFull, hv);
+            const unsigned b = __ballot_sync(kFull, hv == vmax);
+            if (lane == __ffs(b) - 1) {
+                sm.wsel[warp][r] = vmax != 0u ? top[0] : 0ull;
+                sm.wtop[warp][r] = vmax;
+                top[0] = top[1];
+                top[1] = top[2];
+                top[2] = top[3];
+                top[3] = 0ull;
+                hv = (uint32_t)(top[0] >> 32);
+            }
+        }
+        __syncwarp();
+        if (lane < kWarpTop) mine = sm.wsel[warp][lane];
+        // lane l loads vectors 2*(l & 3) and 2*(l & 3) + 1 of entry l >> 2
+        const unsigned long long pe = sm.wsel[warp][lane >> 2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int c = 2 * (lane & 3) + h;
+            const uint32_t pos = (uint32_t)pe;
+            pv0[h] = (long long)(pos >> 8) * TE + (long long)(c * kConsumerThreads + (int)(pos & 0xFFu)) * EPV;
+            if (pe == 0ull || pv0[h] >= p.V) pv0[h] = p.V;
+            pv[h] = make_uint4(0u, 0u, 0u, 0u);
+            if (pv0[h] < p.V) pv[h] = __ldcs(reinterpret_cast<const uint4*>(rowp + pv0[h] * ELT));
+        }
     }
     if (lane == 0) {
         sm.red_f[warp] = m;
@@ -1655,53 +1871,132 @@ __device__ __noinline__ void record_block(const Params& p, RecShared& sm, int ro
     if (tid == 32) sm.xchosen = xc;
     cbar();
     rtrace(p, kTrRecA, row);
-    if (warp == 0) {
-        // lse = M + log(sum_t s_t exp(m_t - M)); S >= 1 holds the maximum's own
-        // term, so logf(S) is accurate to an ulp of a small number and the sum
-        // rounds once (FP64 is slow on this part and buys nothing here)
-        float M = sm.red_f[0], S = sm.red_f2[0];
+    // ---- every warp: lse from the 8 warps' partials (identical in every warp)
+    float lse, xch;
+    {
+        const float mw = lane < kWarps ? sm.red_f[lane] : kNegInf;
+        const float sw = lane < kWarps ? sm.red_f2[lane] : 0.0f;
+        const float M = unord32(__reduce_max_sync(kFull, ord32(__fadd_rn(mw, 0.0f))));
+        float t = (mw > kNegInf) ? sw * ex2((mw - M) * kLog2e) : 0.0f;
 #pragma unroll
-        for (int w = 1; w < 8; ++w) ms_merge(M, S, sm.red_f[w], sm.red_f2[w]);
-        float lse = 0.0f;
-        if (lane == 0) lse = M + logf(S);
-        lse = __shfl_sync(kFull, lse, 0);
-        if (chosen_is_max && lane == 0) sm.xchosen = M;
-        __syncwarp();
-        if (lane == 0) {
+        for (int o = 4; o > 0; o >>= 1) t += __shfl_xor_sync(kFull, t, o);
+        const float S = __shfl_sync(kFull, t, 0);
+        // lse = M + log(S); S >= 1 holds the maximum's own term, so logf(S) is
+        // accurate to an ulp of a small number and the sum rounds once
+        lse = M + logf(S);
+        xch = chosen_is_max ? M : sm.xchosen;
+        if (warp == 0 && lane == 0) {
             sm.lse = lse;
+            sm.xchosen = xch;
             sm.rec[0] = chosen;
-            sm.rec[1] = (chosen >= 0 && chosen < p.V) ? (int)__float_as_uint(logprob(sm.xchosen, lse))
-                                                      : (int)kUnusedBits;
+            sm.rec[1] = (chosen >= 0 && chosen < p.V) ? (int)__float_as_uint(logprob(xch, lse)) : (int)kUnusedBits;
             if (p.lse_out) p.lse_out[row] = lse;
         }
-        if (natural) {
-            // theta: the 32nd largest of the 8 warps' 8 largest entry values (0:
-            // fewer than 32 entries)
-            const uint32_t* wt = &sm.wtop[0][0];
-            const uint32_t a = wt[lane], b = wt[lane + 32];
-            int ra = 0, rb = 0;  // ranks by (value desc, index asc)
-#pragma unroll 8
-            for (int j = 0; j < 64; ++j) {
-                const uint32_t v = wt[j];
-                ra += v > a || (v == a && j < lane);
-                rb += v > b || (v == b && j < lane + 32);
+    }
+    if (natural) {
+        // theta: the 32nd largest of the 8 warps' 8 largest entry values (0:
+        // fewer than 32 entries), by a bitonic sort of the 64 values, element
+        // 2 * lane + h on lane `lane`, descending
+        uint32_t a0 = sm.wtop[lane >> 2][2 * (lane & 3)], a1 = sm.wtop[lane >> 2][2 * (lane & 3) + 1];
+#pragma unroll
+        for (int k = 2; k <= 64; k <<= 1) {
+#pragma unroll
+            for (int j = k >> 1; j > 0; j >>= 1) {
+                if (j == 1) {
+                    // elements 2*lane and 2*lane + 1: the lower index keeps the larger in a descending block
+                    const bool desc = ((2 * lane) & k) == 0;
+                    const uint32_t hi = a0 > a1 ? a0 : a1, lo = a0 > a1 ? a1 : a0;
+                    a0 = desc ? hi : lo;
+                    a1 = desc ? lo : hi;
+                } else {
+                    const int pl = lane ^ (j >> 1);
+                    const uint32_t b0 = __shfl_sync(kFull, a0, pl), b1 = __shfl_sync(kFull, a1, pl);
+                    const bool lower = (lane & (j >> 1)) == 0;
+                    const bool desc = ((2 * lane) & k) == 0;
+                    const bool keep_hi = lower == desc;
+                    a0 = keep_hi ? (a0 > b0 ? a0 : b0) : (a0 > b0 ? b0 : a0);
+                    a1 = keep_hi ? (a1 > b1 ? a1 : b1) : (a1 > b1 ? b1 : a1);
+                }
             }
-            if (ra == 31) sm.theta_o = a;
-            if (rb == 31) sm.theta_o = b;
         }
-        if constexpr (SCORE) {
-            const float lp = logprob(sm.xchosen, lse);
-            sm.xlim = lp == lp ? score_limit(sm.xchosen, lse, lp, lane) : sm.xchosen;  // NaN: nothing is above
+        const uint32_t th = __shfl_sync(kFull, a1, 15);  // element 31
+        const float theta = th ? unord32(th) : kNegInf;
+        if (warp == 0 && lane == 0) sm.theta_o = th;
+        // this column's candidate threads must all be among the 8 loaded
+        int cnt = 0;
+        bool full = false;
+#pragma unroll
+        for (int i = 0; i < kCachedShares; ++i) {
+#pragma unroll
+            for (int r = 0; r < 4; ++r) cnt += (cv[i][r] != 0u && cv[i][r] >= th) ? 1 : 0;
+            full |= cv[i][3] != 0u && cv[i][3] >= th;
+        }
+        const int loaded = (lane < kWarpTop && mine != 0ull && (uint32_t)(mine >> 32) >= th) ? 1 : 0;
+        const bool slow = th == 0u || T > 32 * kCachedShares ||
+                          __any_sync(kFull, full) ||
+                          __reduce_add_sync(kFull, (unsigned)cnt) != __reduce_add_sync(kFull, (unsigned)loaded);
+        if (slow) {
+            if (lane == 0) sm.slow = 1;
+        } else {
+            // the prefetched lanes >= theta, as logprob keys (warp-aggregated append)
+            int n = 0;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                if (pv0[h] < p.V) {
+#pragma unroll
+                    for (int e = 0; e < EPV; ++e) n += (pv0[h] + e < p.V && vec_elem<ELT>(pv[h], e) >= theta) ? 1 : 0;
+                }
+            }
+            int incl = n;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int q = __shfl_up_sync(kFull, incl, o);
+                if (lane >= o) incl += q;
+            }
+            int k0 = 0;
+            if (lane == 31 && incl > 0) k0 = atomicAdd(&sm.n_keys, incl);
+            int k = __shfl_sync(kFull, k0, 31) + incl - n;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                if (pv0[h] < p.V) {
+#pragma unroll
+                    for (int e = 0; e < EPV; ++e) {
+                        const float y = vec_elem<ELT>(pv[h], e);
+                        if (pv0[h] + e < p.V && y >= theta) {
+                            if (k < kCandKeys) sm.ckeys[k] = lp_key(y, lse, (uint32_t)(pv0[h] + e));
+                            ++k;
+                        }
+                    }
+                }
+            }
+        }
+    }
+    if constexpr (SCORE) {
+        if (warp == 0) {
+            const float xt = xch;
+            const float lp = logprob(xt, lse);
+            const float xl = lp == lp ? score_limit(xt, lse, lp, lane) : xt;  // NaN: nothing is above
+            if (lane == 0) sm.xlim = xl;
         }
     }
     cbar();
     rtrace(p, kTrRecB, row);
-    if (natural) natural_record<ELT>(p, sm, row, base, whole, (long long)kc < p.V ? kc : (int)p.V, cache);
+    if (natural) {
+        const int keff = (long long)kc < p.V ? kc : (int)p.V;
+        const Span whole = {0, T, 0, p.V};
+        if (sm.slow) {
+            if (tid == 0) sm.n_keys = 0;
+            cbar();
+            natural_record<ELT>(p, sm, row, base, whole, keff);
+        } else {
+            natural_rank<ELT>(p, sm, row, whole, keff, lse);
+        }
+    }
     rtrace(p, kTrRecC, row);
     if (ids && tid < kc) {
         int bits = (int)kUnusedBits;
         if (id >= 0 && id < p.V) {
-            bits = (int)__float_as_uint(logprob(xi, sm.lse));
+            bits = (int)__float_as_uint(logprob(xi, lse));
         } else {
             atomicOr(p.status, kStatusBadId);
         }
@@ -1711,7 +2006,7 @@ __device__ __noinline__ void record_block(const Params& p, RecShared& sm, int ro
     if constexpr (SCORE) {
         // logits in (xt, X]: above the target's but reported equal to it.  Only
         // a tile whose smallest logit above the target's is <= X holds any.
-        const float xt = sm.xchosen, X = sm.xlim;
+        const float xt = xch, X = sm.xlim;
         int corr = 0;
         for (int t = warp; t < T; t += kWarps) {
             const float mn = lane < kWarps ? __uint_as_float((uint32_t)__ldcg(&p.part_rank[(base + t) * kWarps + lane]).y)
@@ -1744,23 +2039,58 @@ __device__ __noinline__ void record_block(const Params& p, RecShared& sm, int ro
     cbar();
 }
 
-// Builds the records of the rows the stream kernel decided (launched after it
-// with programmatic dependent launch: it waits for the stream grid to finish).
-// The deciders append each record task to a compact list; CTA b takes tasks
-// b, b + grid, ...
+// Builds the records of the rows the stream kernel decides, while it runs.
+// Launched after it with programmatic dependent launch, the grid is scheduled
+// once every stream CTA has started: its CTAs take the multiprocessor room the
+// stream grid leaves, then the room of each stream CTA that exits.  It does not
+// wait for the stream grid to complete.  CTA b claims record tasks in order
+// through a counter, waits until the claimed task's words carry the run's epoch
+// (the decider wrote them after the row's last tile was counted), and builds
+// the record; the tile partials it reads are run-tagged, or were performed
+// before their tiles were counted.  A CTA stops once every group is decided
+// and its claim is past the last task.
 template <int ELT, bool SCORE>
 __global__ void __launch_bounds__(kConsumerThreads, 3) lp_record_kernel(Params p) {
     __shared__ RecShared rs;
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    __shared__ int4 s_task;  // the claimed task: (chosen, row, descriptor word | count << 16, group); row -1: none
     if (vload(&p.ctrl->abort) != 0u) return;
-    unsigned long long* tr = p.trace != nullptr ? p.trace + ((size_t)p.trace_ctas * 3) * p.trace_cap * 2 : nullptr;
-    if (tr != nullptr && threadIdx.x == 0) atomicMin(&tr[4], globaltimer());
-    const unsigned n = __ldcg(&p.ctrl->rec_count);
-    for (unsigned i = blockIdx.x; i < n; i += gridDim.x) {
-        // (chosen, row, descriptor word | chosen-is-argmax << 14 | count << 16, group)
-        const int4 t = __ldcg(&p.rec_tasks[i]);
+    const uint32_t ep = vload(&p.ctrl->epoch);
+    const unsigned long long deadline = globaltimer() + p.timeout_ns;
+    unsigned long long* tr = p.trace != nullptr ? p.trace + ((size_t)p.trace_ctas * kTraceRoles) * p.trace_cap * 2 : nullptr;
+    if (tr != nullptr && threadIdx.x == 0) {
+        g_trace_n[3] = 0u;
+        atomicMin(&tr[4], globaltimer());
+    }
+    for (;;) {
+        if (threadIdx.x == 0) {
+            const unsigned i = atomicAdd(&p.ctrl->rec_claim, 1u);
+            int4 t = make_int4(0, -1, 0, 0);
+            for (;;) {
+                if (i < (unsigned)p.rows) {
+                    const ulonglong2 a = ld_tagged(&p.rec_tasks[2 * (size_t)i]);
+                    const ulonglong2 b = ld_tagged(&p.rec_tasks[2 * (size_t)i + 1]);
+                    if (has_epoch(a, ep) && has_epoch(b, ep)) {
+                        t = make_int4((int)(uint32_t)a.x, (int)(uint32_t)a.y, (int)(uint32_t)b.x, (int)(uint32_t)b.y);
+                        break;
+                    }
+                }
+                // no task i once every group is decided and i is past the count:
+                // the count is read after the outstanding groups are seen to be
+                // none, and each decider appended its task before its group retired
+                if (vload(&p.ctrl->outstanding) <= 0 && i >= vload(&p.ctrl->rec_count)) break;
+                if (globaltimer() > deadline) {
+                    atomicOr(p.status, kStatusTimeout);
+                    break;
+                }
+                __nanosleep(128);
+            }
+            s_task = t;
+        }
+        __syncthreads();
+        const int4 t = s_task;
+        if (t.y < 0) break;
         rtrace(p, kTrRecStart, t.y);
-        record_block<ELT, SCORE>(p, rs, t.y, t.w, t.x, t.z & 0x7FFF, t.z >> 16);
+        record_block<ELT, SCORE>(p, rs, t.y, t.w, t.x, t.z & 0x7FFF, t.z >> 16, ep, deadline);
         rtrace(p, kTrRecEnd, t.y);
     }
     if (tr != nullptr && threadIdx.x == 0) atomicMax(&tr[6], globaltimer());
@@ -1793,6 +2123,13 @@ __global__ void lp_occupy_kernel(unsigned long long ns) {
 // x2[(i*S + s)*256]; the kernels read another shard's payload only after the
 // launch that wrote it has completed, as the all-gathers order them.
 
+// Record task i, once the stream kernel has completed: (chosen, row, descriptor
+// word | flags | count << 16, group).
+__device__ __forceinline__ int4 load_task(const Params& p, unsigned i) {
+    const ulonglong2 a = __ldcg(&p.rec_tasks[2 * (size_t)i]), b = __ldcg(&p.rec_tasks[2 * (size_t)i + 1]);
+    return make_int4((int)(uint32_t)a.x, (int)(uint32_t)a.y, (int)(uint32_t)b.x, (int)(uint32_t)b.y);
+}
+
 __device__ __forceinline__ Span shard_span(const Params& p, int s, int S) {
     Span sp;
     sp.t0 = (int)((long long)s * p.T / S);
@@ -1811,13 +2148,13 @@ __global__ void __launch_bounds__(kConsumerThreads) lp_shard_stage1_kernel(Param
     const int lane = threadIdx.x & 31, s = threadIdx.x >> 5;
     if (s >= S || vload(&p.ctrl->abort) != 0u) return;
     for (unsigned i = blockIdx.x; i < n; i += gridDim.x) {
-        const int row = __ldcg(&p.rec_tasks[i]).y;
+        const int row = load_task(p, i).y;
         const Span sp = shard_span(p, s, S);
         const long long base = (long long)row * p.T;
         float m = kNegInf, sum = 0.0f;
         for (int q = sp.t0 * kWarps + lane; q < sp.t1 * kWarps; q += 32) {
-            const float2 ms = __ldcg(&p.part_ms[base * kWarps + q]);
-            ms_merge(m, sum, ms.x, ms.y);
+            const ulonglong2 ms = __ldcg(&p.part_ms[base * kWarps + q]);
+            ms_merge(m, sum, __uint_as_float((uint32_t)ms.x), __uint_as_float((uint32_t)ms.y));
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) ms_merge(m, sum, __shfl_xor_sync(kFull, m, o), __shfl_xor_sync(kFull, sum, o));
@@ -1850,7 +2187,7 @@ __global__ void __launch_bounds__(kConsumerThreads, 3) lp_shard_stage2_kernel(Pa
     for (unsigned bi = blockIdx.x; bi < n * (unsigned)S; bi += gridDim.x) {
         const unsigned i = bi / S;
         const int s = (int)(bi % S);
-        const int4 t = __ldcg(&p.rec_tasks[i]);  // (chosen, row, descriptor word | flags | count << 16, group)
+        const int4 t = load_task(p, i);  // (chosen, row, descriptor word | flags | count << 16, group)
         const int row = t.y, chosen = t.x, g = t.w, dy = t.z & 0x7FFF, kc = t.z >> 16;
         const int mode = (dy >> 8) & 3, ids = (dy >> 12) & 1;
         const bool natural = !ids && mode == kModeNatural && kc > 0;
@@ -1875,8 +2212,7 @@ __global__ void __launch_bounds__(kConsumerThreads, 3) lp_shard_stage2_kernel(Pa
             sm.n_thr = sm.n_sh = sm.n_keys = 0;
             sm.lse = shard_lse(x1, i, S);
         }
-        unsigned long long cache[kCachedShares][4];
-        if (natural) summary_top(p, sm, base, sp, warp, lane, cache);
+        if (natural) summary_top(p, sm, base, sp, warp, lane);
         cbar();
         if (natural) {
             if (warp == 0) {
@@ -1895,7 +2231,7 @@ __global__ void __launch_bounds__(kConsumerThreads, 3) lp_shard_stage2_kernel(Pa
             for (int w = tid; w < 66; w += kConsumerThreads) sm.rec[w] = (w >= 2 && (w & 1) == 0) ? -1 : (int)kUnusedBits;
             cbar();
             const long long len = sp.v1 - sp.v0;
-            natural_record<ELT>(p, sm, row, base, sp, len < 32 ? (int)len : 32, cache);
+            natural_record<ELT>(p, sm, row, base, sp, len < 32 ? (int)len : 32);
             // the shard's best keys, from the pairs in rank order
             if (warp == 0) {
                 const int id = sm.rec[2 + 2 * lane];
@@ -1919,7 +2255,7 @@ __global__ void __launch_bounds__(kConsumerThreads) lp_shard_merge_kernel(Params
     if (vload(&p.ctrl->abort) != 0u) return;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     for (unsigned i = blockIdx.x; i < n; i += gridDim.x) {
-        const int4 t = __ldcg(&p.rec_tasks[i]);
+        const int4 t = load_task(p, i);
         const int row = t.y, chosen = t.x, dy = t.z & 0x7FFF, kc = t.z >> 16, g = t.w;
         const int mode = (dy >> 8) & 3, ids = (dy >> 12) & 1;
         const bool natural = !ids && mode == kModeNatural && kc > 0;
@@ -2039,7 +2375,8 @@ cudaError_t launch_shard_records(const Params& p, int dtype, const LaunchCfg& cf
 
 cudaError_t launch_epilogue(const Params& p_in, int dtype, const LaunchCfg& cfg, cudaStream_t stream, bool records) {
     long long work = (long long)p_in.rows * p_in.T;
-    int grid = cfg.grid;
+    // stream-CTA slots left to the record kernel from the start
+    int grid = cfg.grid - (records ? (LP_RECORD_SLOTS < cfg.grid / 2 ? LP_RECORD_SLOTS : cfg.grid / 2) : 0);
     if (work < grid) grid = work > 0 ? (int)work : 1;
     Params p = p_in;
     p.stream_grid = grid;
@@ -2063,9 +2400,10 @@ cudaError_t launch_epilogue(const Params& p_in, int dtype, const LaunchCfg& cfg,
         e = score ? cudaLaunchKernelEx(&lc, lp_stream_kernel<4, true>, p) : cudaLaunchKernelEx(&lc, lp_stream_kernel<4, false>, p);
     }
     if (e != cudaSuccess || !records) return e;
-    // records: CTA b builds tasks b, b + grid, ... of the compact task list
-    // (at most one per row); three 256-thread CTAs per SM are resident
-    int rgrid = cfg.sms * 3;
+    // records: a persistent grid, one CTA per stream-CTA slot of the device
+    // (the ones the stream grid leaves start at once, the others as stream CTAs
+    // exit), at most one per row
+    int rgrid = cfg.grid;
     if (rgrid > p.rows) rgrid = p.rows;
     if (rgrid < 1) rgrid = 1;
     cudaLaunchConfig_t rc = {};

@@ -7,6 +7,7 @@
 // the hot path.
 #include <cuda_runtime.h>
 
+#include <cstddef>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -28,8 +29,8 @@ struct lp_plan_s {
     int* done;
     unsigned long long* row_best;
     int4* gdesc;
-    int4* rec_tasks;
-    float2* part_ms;
+    ulonglong2* rec_tasks;
+    ulonglong2* part_ms;
     int2* part_rank;
     unsigned long long* part_keys;
     size_t part_ms_bytes, part_keys_bytes;
@@ -105,9 +106,9 @@ Layout layout_of(const lp_plan_desc* d) {
     L.gdesc = off;
     off = align_up(off + (size_t)d->max_groups * sizeof(int4));
     L.rec_tasks = off;
-    off = align_up(off + rows * sizeof(int4));
+    off = align_up(off + rows * 2 * sizeof(ulonglong2));
     L.part_ms = off;
-    L.part_ms_bytes = rows * T * (lp::kConsumerThreads / 32) * sizeof(float2);
+    L.part_ms_bytes = rows * T * (lp::kConsumerThreads / 32) * sizeof(ulonglong2);
     off = align_up(off + L.part_ms_bytes);
     L.part_rank = off;
     off = align_up(off + rows * T * (lp::kConsumerThreads / 32) * sizeof(int2));
@@ -280,13 +281,15 @@ int lp_plan_create(lp_plan_t* out, const lp_plan_desc* desc) {
     plan->row_best = reinterpret_cast<unsigned long long*>(plan->scratch + L.row_best);
     plan->done = reinterpret_cast<int*>(plan->scratch + L.done);
     plan->gdesc = reinterpret_cast<int4*>(plan->scratch + L.gdesc);
-    plan->rec_tasks = reinterpret_cast<int4*>(plan->scratch + L.rec_tasks);
-    plan->part_ms = reinterpret_cast<float2*>(plan->scratch + L.part_ms);
+    plan->rec_tasks = reinterpret_cast<ulonglong2*>(plan->scratch + L.rec_tasks);
+    plan->part_ms = reinterpret_cast<ulonglong2*>(plan->scratch + L.part_ms);
     plan->part_rank = reinterpret_cast<int2*>(plan->scratch + L.part_rank);
     plan->part_keys = reinterpret_cast<unsigned long long*>(plan->scratch + L.part_keys);
     plan->part_ms_bytes = L.part_ms_bytes;
     plan->part_keys_bytes = L.part_keys_bytes;
-    e = cudaMemset(plan->scratch, 0, L.part_ms);  // control block, queue, counters, descriptors
+    // all of it: the run epoch starts at 0, and no partial or record task then
+    // carries the epoch of a run (never 0)
+    e = cudaMemset(plan->scratch, 0, L.total);
     if (e == cudaSuccess && (desc->flags & LP_PLAN_HOST_STAGING)) {
         const StageLayout S = stage_layout_of(desc);
         e = cudaMalloc(&plan->staging, S.total);
@@ -316,11 +319,11 @@ int lp_plan_create(lp_plan_t* out, const lp_plan_desc* desc) {
     if (e == cudaSuccess && (desc->flags & LP_PLAN_DEBUG_TRACE)) {
         plan->trace_cap = 2048;
         plan->trace_ctas = plan->cfg.grid;
-        const size_t ev = ((size_t)plan->trace_ctas * 3 + 1) * plan->trace_cap * 2 * sizeof(unsigned long long);
+        const size_t ev = ((size_t)plan->trace_ctas * lp::kTraceRoles + 1) * plan->trace_cap * 2 * sizeof(unsigned long long);
         e = cudaMalloc(&plan->trace, ev);
-        if (e == cudaSuccess) e = cudaMalloc(&plan->trace_count, (size_t)plan->trace_ctas * 3 * sizeof(unsigned));
+        if (e == cudaSuccess) e = cudaMalloc(&plan->trace_count, (size_t)plan->trace_ctas * lp::kTraceRoles * sizeof(unsigned));
         if (e == cudaSuccess) e = cudaMemset(plan->trace, 0, ev);
-        if (e == cudaSuccess) e = cudaMemset(plan->trace_count, 0, (size_t)plan->trace_ctas * 3 * sizeof(unsigned));
+        if (e == cudaSuccess) e = cudaMemset(plan->trace_count, 0, (size_t)plan->trace_ctas * lp::kTraceRoles * sizeof(unsigned));
     }
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
@@ -576,10 +579,11 @@ int lp_debug_poison_scratch(lp_plan_t plan, void* stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaMemsetAsync(plan->part_ms, 0xFF, plan->part_ms_bytes, s);
     if (e == cudaSuccess) e = cudaMemsetAsync(plan->part_keys, 0xFF, plan->part_keys_bytes, s);
-    // the scoring partials: one int2 per warp of a tile, the size of part_ms
-    if (e == cudaSuccess) e = cudaMemsetAsync(plan->part_rank, 0xFF, plan->part_ms_bytes, s);
-    // record tasks past the run's count are never read
-    if (e == cudaSuccess) e = cudaMemsetAsync(plan->rec_tasks, 0xFF, (size_t)plan->d.max_rows * sizeof(int4), s);
+    // the scoring partials: one int2 per warp of a tile, half the size of part_ms
+    if (e == cudaSuccess) e = cudaMemsetAsync(plan->part_rank, 0xFF, plan->part_ms_bytes / 2, s);
+    // record tasks past the run's count are never read; all-ones words carry no run's epoch
+    if (e == cudaSuccess)
+        e = cudaMemsetAsync(plan->rec_tasks, 0xFF, (size_t)plan->d.max_rows * 2 * sizeof(ulonglong2), s);
     if (e != cudaSuccess) return cuda_fail(e);
     return LP_OK;
 }
@@ -600,11 +604,11 @@ int lp_debug_trace(lp_plan_t plan, uint64_t* events, uint32_t* counts, int32_t* 
     if (!events) return LP_OK;
     if (!counts) return LP_EINVAL;
     DeviceGuard guard(plan->d.device);
-    const size_t ev = ((size_t)plan->trace_ctas * 3 + 1) * plan->trace_cap * 2 * sizeof(unsigned long long);
+    const size_t ev = ((size_t)plan->trace_ctas * lp::kTraceRoles + 1) * plan->trace_cap * 2 * sizeof(unsigned long long);
     cudaError_t e = cudaStreamSynchronize(plan->last_stream);
     if (e == cudaSuccess) e = cudaMemcpy(events, plan->trace, ev, cudaMemcpyDeviceToHost);
     if (e == cudaSuccess)
-        e = cudaMemcpy(counts, plan->trace_count, (size_t)plan->trace_ctas * 3 * sizeof(unsigned),
+        e = cudaMemcpy(counts, plan->trace_count, (size_t)plan->trace_ctas * lp::kTraceRoles * sizeof(unsigned),
                        cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return cuda_fail(e);
     return LP_OK;
@@ -707,16 +711,18 @@ extern "C" int lp_run_static(const lp_plan_desc* desc, const lp_io* io, void* st
     run.row_best = reinterpret_cast<unsigned long long*>(base + L.row_best);
     run.done = reinterpret_cast<int*>(base + L.done);
     run.gdesc = reinterpret_cast<int4*>(base + L.gdesc);
-    run.rec_tasks = reinterpret_cast<int4*>(base + L.rec_tasks);
-    run.part_ms = reinterpret_cast<float2*>(base + L.part_ms);
+    run.rec_tasks = reinterpret_cast<ulonglong2*>(base + L.rec_tasks);
+    run.part_ms = reinterpret_cast<ulonglong2*>(base + L.part_ms);
     run.part_rank = reinterpret_cast<int2*>(base + L.part_rank);
     run.part_keys = reinterpret_cast<unsigned long long*>(base + L.part_keys);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // The array keeps the previous call's contents.  The control block must
     // start at zero (its never-written word is the forced-timeout test's
-    // flag); the prepare kernel resets the queue, counters and descriptors, and
-    // tile partials are written before they are read.
-    e = cudaMemsetAsync(run.ctrl, 0, sizeof(lp::Ctrl), s);
+    // flag), except the run epoch, which keeps counting across calls so that
+    // no partial or record task left by an earlier call (at any layout) carries
+    // the new run's epoch; the prepare kernel resets the queue, counters and
+    // descriptors.
+    e = cudaMemsetAsync(run.ctrl, 0, offsetof(lp::Ctrl, epoch), s);
     if (e != cudaSuccess) return cuda_fail(e);
     const lp::Params p = make_params(&run, *io);
     e = lp::launch_epilogue(p, desc->dtype, run.cfg, s);

@@ -43,11 +43,11 @@ def test_strerror(L):
 
 
 def test_scratch_bytes_of_workloads(L):
-    # tile partials dominate: per 32 KiB tile, one (max, exp-sum) and one
-    # prompt-scoring (count, minimum) per compute warp (2 x 8 x 8 bytes) and 32
-    # sort keys (256 bytes)
+    # tile partials dominate: per 32 KiB tile, one run-tagged (max, exp-sum)
+    # pair and one prompt-scoring (count, minimum) per compute warp (8 x 16 and
+    # 8 x 8 bytes) and 32 summary entries (256 bytes)
     b = lpe.scratch_bytes(max_rows=2048, max_groups=256, k_max=7, V=262_144, dtype="f32")
-    assert 2048 * 32 * 384 <= b < 2048 * 32 * 384 + (1 << 20)
+    assert 2048 * 32 * 448 <= b < 2048 * 32 * 448 + (1 << 20)
     assert lpe.scratch_bytes(max_rows=0, max_groups=1, k_max=0, V=10) == 0
     staged = lpe.scratch_bytes(max_rows=4, max_groups=1, k_max=3, V=1000, V_padded=1024, dtype="f32",
                                host_staging=True)

@@ -57,7 +57,7 @@ def _same(w, static, planned):
 def test_static_matches_plan_entry_point_two_calls():
     # Two calls in a row on different shapes and element types: the second
     # reuses the fixed array the first one left behind.
-    first = W.spec()             # 512 rows x 248,448 BF16 lanes: about 3.2 MB of scratch
+    first = W.spec()             # 512 rows x 248,448 BF16 lanes: about 3.7 MB of scratch
     second = W.large(groups=4)   # 32 rows x 262,144 FP32 lanes
     s1 = _run_static(first)
     s2 = _run_static(second)
