@@ -92,6 +92,8 @@ struct Ctrl {
     unsigned int epoch;       // run number, advanced by the prepare kernel (never 0 or all ones); the
                               // tile partials and record tasks of a run carry it
     unsigned int pad7[31];
+    unsigned int retired;     // stream CTAs that left their slot to the record kernel early
+    unsigned int pad8[31];
 };
 
 struct Params {
@@ -137,7 +139,8 @@ struct Params {
                                     // thread maxima, (ord32 << 32) | (tile << 8) | thread; 0 = none
     unsigned long long timeout_ns;
     unsigned int debug_flags;
-    int build_records;    // 1: the stream kernel builds the records (0: the sharded kernels do)
+    int build_records;    // 1: the record kernel runs beside the stream kernel (0: the sharded kernels
+                          // build the records after it)
     int read_ahead;       // 0: rows past a group's emitted prefix are never read
     // prompt scoring (targets != nullptr): group g is row g alone, k = 0, 20
     // natural alternatives, chosen token targets[g]; records go to score_records

@@ -613,6 +613,7 @@ __global__ void __launch_bounds__(1024) lp_prepare_kernel(Params p) {
             p.ctrl->outstanding = 0;
             p.ctrl->rec_count = 0u;
             p.ctrl->rec_claim = 0u;
+            p.ctrl->retired = 0u;
         }
         return;
     }
@@ -742,6 +743,7 @@ __global__ void __launch_bounds__(1024) lp_prepare_kernel(Params p) {
         p.ctrl->outstanding = s_base;
         p.ctrl->rec_count = 0u;
         p.ctrl->rec_claim = 0u;
+        p.ctrl->retired = 0u;
         p.ctrl->abort = 0u;
     }
 }
@@ -766,6 +768,16 @@ constexpr unsigned kNone = 0xFFFFFFFFu;
 // waiting chained claims cover k/4 of the next row of every outstanding group.
 #ifndef LP_SURPLUS_EXIT
 #define LP_SURPLUS_EXIT 0
+#endif
+// A producer with no claim retires its CTA when at least this many appended
+// record tasks wait unclaimed (0: never), up to 1/LP_RETIRE_SHARE of the grid:
+// the slot goes to a record CTA, so that the records keep pace with the
+// decisions instead of piling up behind the last one.
+#ifndef LP_RETIRE_BACKLOG
+#define LP_RETIRE_BACKLOG 16
+#endif
+#ifndef LP_RETIRE_SHARE
+#define LP_RETIRE_SHARE 4
 #endif
 // A producer reads ahead only after waiting this long for a chained item.
 #ifndef LP_READ_AHEAD_IDLE_NS
@@ -807,6 +819,17 @@ __device__ __noinline__ void producer_loop(const Params& p, Shared& sm, unsigned
         if (LP_SURPLUS_EXIT && surplus && fresh_done && !p.read_ahead) {
             chains_over = true;
             return;
+        }
+        // record pressure: record tasks wait with no record CTA to take them;
+        // a producer without a claim leaves its slot to the record kernel
+        // (at most a share of the grid does)
+        if (LP_RETIRE_BACKLOG > 0 && fresh_done && p.build_records && !p.read_ahead) {
+            const int backlog = (int)(vload(&ctrl->rec_count) - vload(&ctrl->rec_claim));
+            if (backlog >= LP_RETIRE_BACKLOG &&
+                atomicAdd(&ctrl->retired, 1u) < (unsigned)(p.stream_grid / LP_RETIRE_SHARE)) {
+                chains_over = true;
+                return;
+            }
         }
         chain_claim = atomicAdd(&ctrl->chain_next, 1u);
         if (chain_claim / T >= CM) {
@@ -2061,6 +2084,7 @@ __global__ void __launch_bounds__(kConsumerThreads, 3) lp_record_kernel(Params p
         g_trace_n[3] = 0u;
         atomicMin(&tr[4], globaltimer());
     }
+    rtrace(p, kTrKernel, 0);
     for (;;) {
         if (threadIdx.x == 0) {
             const unsigned i = atomicAdd(&p.ctrl->rec_claim, 1u);
@@ -2380,6 +2404,7 @@ cudaError_t launch_epilogue(const Params& p_in, int dtype, const LaunchCfg& cfg,
     if (work < grid) grid = work > 0 ? (int)work : 1;
     Params p = p_in;
     p.stream_grid = grid;
+    p.build_records = records ? 1 : 0;
     lp_prepare_kernel<<<1, 1024, 0, stream>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
