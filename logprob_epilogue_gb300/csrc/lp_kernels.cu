@@ -2076,7 +2076,10 @@ template <int ELT, bool SCORE>
 __global__ void __launch_bounds__(kConsumerThreads, 3) lp_record_kernel(Params p) {
     __shared__ RecShared rs;
     __shared__ int4 s_task;  // the claimed task: (chosen, row, descriptor word | count << 16, group); row -1: none
-    if (vload(&p.ctrl->abort) != 0u) return;
+    if (vload(&p.ctrl->abort) != 0u) {
+        if (threadIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");  // completes after the stream grid
+        return;
+    }
     const uint32_t ep = vload(&p.ctrl->epoch);
     const unsigned long long deadline = globaltimer() + p.timeout_ns;
     unsigned long long* tr = p.trace != nullptr ? p.trace + ((size_t)p.trace_ctas * kTraceRoles) * p.trace_cap * 2 : nullptr;
@@ -2118,6 +2121,10 @@ __global__ void __launch_bounds__(kConsumerThreads, 3) lp_record_kernel(Params p
         rtrace(p, kTrRecEnd, t.y);
     }
     if (tr != nullptr && threadIdx.x == 0) atomicMax(&tr[6], globaltimer());
+    // this grid completes after the stream grid (it never waited for it):
+    // whatever follows in the stream, the next run's prepare kernel included,
+    // finds every kernel of the run done
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // Test hook: each CTA holds `smem` bytes of shared memory (so no stream CTA
