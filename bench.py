@@ -407,6 +407,12 @@ def run_e2e(args, w, plan, stream, dev, pg, local, world, accepted):
                 emitted_tokens=pin(np.zeros(w.rows, np.int32)), lse_out=pin(np.zeros(w.rows, np.float32)),
                 status=pin(np.zeros(1, np.int32)))
     h2d, d2h = plan.host_bytes(harr)
+    # pinned logits are read in place: what crosses the link is the rows the
+    # run reads and the gathered logits, not the whole block
+    in_place = h2d < w.rows * w.Vp * w.elt
+    if in_place:
+        ab = algorithmic_bytes(w, accepted)
+        h2d += ab["logit_bytes"] + ab["gathers"] * 32
     for _ in range(3):
         plan.run_host(harr, stream)
     torch.cuda.synchronize(dev)
@@ -420,7 +426,9 @@ def run_e2e(args, w, plan, stream, dev, pg, local, world, accepted):
     e2e_ok = np.array_equal(harr["accepted"].numpy(), accepted)
     del harr
     return {"value": world * w.rows / e2e_t, "unit": "rows/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": e2e_t * 1e3, "matches_device_run": bool(e2e_ok)}
+            "d2h_bytes_per_step": d2h, "ms_per_step": e2e_t * 1e3, "matches_device_run": bool(e2e_ok),
+            "logits": "read in place from pinned host memory (the rows the run reads)" if in_place
+                      else "copied to device staging"}
 
 
 
@@ -516,7 +524,7 @@ def main():
                      "kernel": "lp_stream_kernel (timed with lp_prepare_kernel: one lp_run)",
                      "algorithmic_bytes_per_launch": ab["total"], "peak_source": peak_kind},
         "e2e": e2e,
-        "gpu_launches": 2 * args.steps,  # lp_prepare_kernel and lp_stream_kernel per lp_run
+        "gpu_launches": 3 * args.steps,  # lp_prepare_kernel, lp_stream_kernel and lp_record_kernel per lp_run
         "clocks": clocks,
         "status": status,
         "median_launch_us": statistics.median(durs) * 1e6,

@@ -210,13 +210,19 @@ int lp_run(lp_plan_t plan, void* stream);
  * inputs and the output buffers (so that rows the run does not write keep the
  * caller's contents) to plan-owned device staging, runs, and copies records,
  * accepted, emitted_tokens, lse_out (if non-NULL) and status back, all on
- * `stream`.
+ * `stream`.  When the logit block is pinned host memory mapped into the
+ * device's address space (cudaHostAlloc'd or registered; 16-byte aligned), it
+ * is not copied: the kernels read it in place, so only the rows the run reads
+ * (and the gathered logits) cross the host link.
  * Returns after enqueueing; synchronise the stream before reading outputs.
  * Needs a plan created with LP_PLAN_HOST_STAGING (else LP_ESTATE).
- * Host buffers must stay valid until the stream reaches the end of the copies. */
+ * Host buffers must stay valid until the stream reaches the end of the copies
+ * (and, for logits read in place, until the run has completed). */
 int lp_run_host(lp_plan_t plan, const lp_io* host_io, void* stream);
 
-/* Bytes lp_run_host copies host->device and device->host for host_io. */
+/* Bytes lp_run_host copies host->device and device->host for host_io.  Logits
+ * read in place are not included: the run reads rows_read * V * element size
+ * of them (rows_read from the accepted counts). */
 int lp_run_host_bytes(lp_plan_t plan, const lp_io* host_io, int64_t* h2d, int64_t* d2h);
 
 /* ---- Prompt scoring ("logprobs-design.md", the prompt-logprobs paragraphs)

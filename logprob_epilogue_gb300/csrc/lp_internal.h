@@ -139,6 +139,8 @@ struct Params {
                                     // thread maxima, (ord32 << 32) | (tile << 8) | thread; 0 = none
     unsigned long long timeout_ns;
     unsigned int debug_flags;
+    int host_logits;      // 1: logits is pinned host memory mapped into the device's address space;
+                          // tiles are copied with cp.async (16-byte copies) instead of TMA bulk copies
     int build_records;    // 1: the record kernel runs beside the stream kernel (0: the sharded kernels
                           // build the records after it)
     int read_ahead;       // 0: rows past a group's emitted prefix are never read

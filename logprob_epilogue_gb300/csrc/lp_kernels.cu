@@ -961,8 +961,18 @@ __device__ __noinline__ void producer_loop(const Params& p, Shared& sm, unsigned
         const uint32_t bytes = (static_cast<uint32_t>(nv * ELT) + 15u) & ~15u;
         const unsigned char* src =
             reinterpret_cast<const unsigned char*>(p.logits) + ((long long)item.x * p.Vp + tbase) * ELT;
-        mbar_arrive_expect_tx(&sm.full[stage], bytes);
-        bulk_load(stages + (size_t)stage * kTileBytes, src, bytes, &sm.full[stage], item.w == kModeNatural ? npolicy : policy);
+        if (p.host_logits) {
+            // logits in mapped host memory: 16-byte asynchronous copies, the
+            // stage's barrier completing when they have all landed
+            unsigned char* dst = stages + (size_t)stage * kTileBytes;
+            for (uint32_t o = 0; o < bytes; o += 16)
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst + o)), "l"(src + o) : "memory");
+            asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(&sm.full[stage])) : "memory");
+        } else {
+            mbar_arrive_expect_tx(&sm.full[stage], bytes);
+            bulk_load(stages + (size_t)stage * kTileBytes, src, bytes, &sm.full[stage],
+                      item.w == kModeNatural ? npolicy : policy);
+        }
         trace(p, kTrIssue, item.x, item.y, true);
         if (++stage == S) {
             stage = 0;

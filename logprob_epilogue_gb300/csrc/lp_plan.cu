@@ -409,10 +409,28 @@ int lp_run(lp_plan_t plan, void* stream) {
     return LP_OK;
 }
 
+namespace {
+// The device address of a pinned host block mapped into the device's address
+// space (16-byte aligned, as the tile copies need), or nullptr.
+const void* mapped_host_logits(const void* h) {
+    if (h == nullptr || (reinterpret_cast<uintptr_t>(h) & 15u) != 0) return nullptr;
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, h) != cudaSuccess) {
+        cudaGetLastError();  // an unregistered pointer is not an error here
+        return nullptr;
+    }
+    if (a.type != cudaMemoryTypeHost || a.devicePointer == nullptr) return nullptr;
+    if ((reinterpret_cast<uintptr_t>(a.devicePointer) & 15u) != 0) return nullptr;
+    return a.devicePointer;
+}
+}  // namespace
+
 int lp_run_host_bytes(lp_plan_t plan, const lp_io* io, int64_t* h2d, int64_t* d2h) {
     if (!plan || !io || !h2d || !d2h) return LP_EINVAL;
     const int64_t rows = io->rows, G = io->groups;
-    *h2d = rows * plan->d.V_padded * plan->elt + (G + 1) * 4 + rows * 4 + G * 4 * 4 + G * LP_MAX_IDS * 4 +
+    // mapped pinned logits are read in place (the rows the run reads, counted by the caller)
+    const int64_t logit_bytes = mapped_host_logits(io->logits) ? 0 : rows * plan->d.V_padded * plan->elt;
+    *h2d = logit_bytes + (G + 1) * 4 + rows * 4 + G * 4 * 4 + G * LP_MAX_IDS * 4 +
            rows * LP_RECORD_WORDS * 4 + G * 4 + rows * 4 + (io->lse_out ? rows * 4 : 0);
     *d2h = rows * LP_RECORD_WORDS * 4 + G * 4 + rows * 4 + (io->lse_out ? rows * 4 : 0) + 4;
     return LP_OK;
@@ -435,8 +453,10 @@ int lp_run_host(lp_plan_t plan, const lp_io* h, void* stream) {
         size_t n;
         cudaMemcpyKind k;
     };
+    // pinned, mapped logits are read in place: only the rows the run reads cross the link
+    const void* mapped = mapped_host_logits(h->logits);
     const Cp in[] = {
-        {(void*)d.logits, h->logits, rows * (size_t)plan->d.V_padded * plan->elt, H2D},
+        {(void*)d.logits, h->logits, mapped ? 0 : rows * (size_t)plan->d.V_padded * plan->elt, H2D},
         {(void*)d.group_indptr, h->group_indptr, (G + 1) * 4, H2D},
         {(void*)d.draft_tokens, h->draft_tokens, rows * 4, H2D},
         {(void*)d.sampled_tokens, h->sampled_tokens, G * 4, H2D},
@@ -466,7 +486,9 @@ int lp_run_host(lp_plan_t plan, const lp_io* h, void* stream) {
     run_io.rows = h->rows;
     run_io.groups = h->groups;
     if (!h->lse_out) run_io.lse_out = nullptr;
-    const lp::Params p = make_params(plan, run_io);
+    if (mapped) run_io.logits = mapped;
+    lp::Params p = make_params(plan, run_io);
+    p.host_logits = mapped ? 1 : 0;
     cudaError_t e = lp::launch_epilogue(p, plan->d.dtype, plan->cfg, s);
     if (e != cudaSuccess) return cuda_fail(e);
     const Cp out[] = {

@@ -355,6 +355,32 @@ def test_host_buffers_match_device_run():
                   records=pin(np.full((w.rows, 258), PT.SENTINEL, np.int32)),
                   accepted=pin(np.zeros(w.groups, np.int32)), emitted_tokens=pin(np.zeros(w.rows, np.int32)),
                   lse_out=pin(np.full(w.rows, PT.LSE_SENTINEL, np.float32)), status=pin(np.zeros(1, np.int32)))
+    h2d, _ = plan.host_bytes(arrays)
+    assert h2d < w.logits.nbytes // 2, "pinned logits are read in place, not copied"
+    plan.run_host(arrays)
+    torch.cuda.synchronize()
+    assert np.array_equal(arrays["records"].numpy(), ref["records"])
+    assert np.array_equal(arrays["accepted"].numpy(), ref["accepted"])
+    assert np.array_equal(arrays["emitted_tokens"].numpy(), ref["emitted_tokens"])
+    plan.close()
+
+
+def test_host_buffers_pageable_logits_are_staged():
+    # A logit block in ordinary (pageable) host memory is copied to device
+    # staging; pinned blocks are read in place (the test above).  Same results.
+    import torch
+    w = W.large(groups=4)
+    ref, _ = PT.run_gpu(w)
+    plan = PT.make_plan(w, host_staging=True)
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+    arrays = dict(logits=np.ascontiguousarray(w.logits), group_indptr=pin(w.group_indptr),
+                  draft_tokens=pin(w.draft_tokens), sampled_tokens=pin(w.sampled_tokens),
+                  requested=pin(w.requested), top_k=pin(w.top_k), token_ids=pin(w.token_ids),
+                  id_counts=pin(w.id_counts), records=pin(np.full((w.rows, 258), PT.SENTINEL, np.int32)),
+                  accepted=pin(np.zeros(w.groups, np.int32)), emitted_tokens=pin(np.zeros(w.rows, np.int32)),
+                  lse_out=pin(np.full(w.rows, PT.LSE_SENTINEL, np.float32)), status=pin(np.zeros(1, np.int32)))
+    h2d, _ = plan.host_bytes(arrays)
+    assert h2d >= w.logits.nbytes, "pageable logits are copied whole"
     plan.run_host(arrays)
     torch.cuda.synchronize()
     assert np.array_equal(arrays["records"].numpy(), ref["records"])
