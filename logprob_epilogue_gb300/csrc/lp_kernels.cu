@@ -285,6 +285,11 @@ static_assert(StageCfg<2>::kStages <= kMaxStages && StageCfg<4>::kStages <= kMax
 // Tiles handed from the compute warps to the helper warp, in order.
 constexpr int kDoneRing = 4;
 
+#ifndef LP_STAGE_ALIGN
+#define LP_STAGE_ALIGN 128
+#endif
+constexpr uint32_t kStageAlign = LP_STAGE_ALIGN < 16 ? 16u : (uint32_t)LP_STAGE_ALIGN;
+
 struct Shared {
     uint64_t full[kMaxStages];       // stage filled (producer + TMA)
     uint64_t empty[kMaxStages];      // stage released (8 compute warps)
@@ -551,7 +556,10 @@ __device__ __forceinline__ GroupIn load_group(const Params& p, int g) {
     return x;
 }
 
-__global__ void __launch_bounds__(1024) lp_prepare_kernel(Params p) {
+#ifndef LP_PREP_THREADS
+#define LP_PREP_THREADS 1024
+#endif
+__global__ void __launch_bounds__(LP_PREP_THREADS) lp_prepare_kernel(Params p) {
     asm volatile("griddepcontrol.launch_dependents;");
     if (p.trace != nullptr && threadIdx.x == 0) {
         unsigned long long* e = p.trace + ((size_t)p.trace_ctas * kTraceRoles) * p.trace_cap * 2;
@@ -785,8 +793,44 @@ constexpr unsigned kNone = 0xFFFFFFFFu;
 #endif
 constexpr unsigned long long kReadAheadIdleNs = LP_READ_AHEAD_IDLE_NS;
 
+// The producer warp's lanes load the first queue entries beside the producer
+// lane's first claim (LP_QUEUE_WINDOW): a run's first items come from the
+// first rows of the queue, so the claim's entry is then known one round trip
+// sooner.
+#ifndef LP_QUEUE_WINDOW
+#define LP_QUEUE_WINDOW 1
+#endif
+
+// First claim of a producer: its fresh ticket, the run's fresh-row and
+// chained-row counts, and the ticket's queue entry when the window held it
+// (else all ones: to be loaded).
+struct FirstClaim {
+    unsigned ticket, F, CM;
+    unsigned long long entry;
+};
+
+__device__ __forceinline__ FirstClaim first_claim(const Params& p) {
+    const int lane = threadIdx.x & 31;
+    Ctrl* ctrl = p.ctrl;
+    FirstClaim f = {0u, 0u, 0u, ~0ull};
+    unsigned long long qe = ~0ull;
+    if (LP_QUEUE_WINDOW && lane < p.rows) qe = vload(&p.queue[lane]);
+    if (lane == 0) {
+        f.ticket = atomicAdd(&ctrl->fresh_next, 1u);
+        f.F = vload(&ctrl->fresh_rows);
+        f.CM = vload(&ctrl->chain_max);
+    }
+    f.ticket = __shfl_sync(kFull, f.ticket, 0);
+    f.F = __shfl_sync(kFull, f.F, 0);
+    const unsigned pos = f.ticket / (unsigned)p.T;
+    const unsigned long long e = __shfl_sync(kFull, qe, (int)(pos & 31u));
+    if (LP_QUEUE_WINDOW && pos < 32u && pos < f.F) f.entry = e;
+    return f;
+}
+
 template <int ELT>
-__device__ __noinline__ void producer_loop(const Params& p, Shared& sm, unsigned char* stages, unsigned long long t0) {
+__device__ __noinline__ void producer_loop(const Params& p, Shared& sm, unsigned char* stages, unsigned long long t0,
+                                           FirstClaim first) {
     constexpr int S = StageCfg<ELT>::kStages;
     constexpr int kTE = tile_elems<ELT>();
     const unsigned long long deadline = t0 + p.timeout_ns;
@@ -801,9 +845,9 @@ __device__ __noinline__ void producer_loop(const Params& p, Shared& sm, unsigned
     unsigned chain_claim = kNone;
     unsigned long long ra_e = ~0ull;  // read-ahead candidate: entry of the successor of the last row streamed
     unsigned long long idle_t0 = 0;   // start of the current wait for a chained item (0: not waiting)
-    unsigned fresh_ahead = atomicAdd(&ctrl->fresh_next, 1u);
-    const unsigned F = vload(&ctrl->fresh_rows);
-    const unsigned CM = vload(&ctrl->chain_max);
+    unsigned fresh_ahead = first.ticket;
+    const unsigned F = first.F;
+    const unsigned CM = first.CM;
     const unsigned fresh_items = F * T;
     // A chained claim at or past CM rows can never be taken (no more rows can
     // be appended): once this producer holds one it has no work left, and
@@ -837,7 +881,8 @@ __device__ __noinline__ void producer_loop(const Params& p, Shared& sm, unsigned
             chains_over = true;
         }
     };
-    unsigned long long fresh_entry = fresh_done ? ~0ull : vload(&p.queue[fresh_ahead / T]);
+    unsigned long long fresh_entry =
+        fresh_done ? ~0ull : ((long long)first.entry >= 0 ? first.entry : vload(&p.queue[fresh_ahead / T]));
     int stage = 0;
     uint32_t phase = 0;
     bool timed_out = false;
@@ -962,12 +1007,9 @@ __device__ __noinline__ void producer_loop(const Params& p, Shared& sm, unsigned
         const unsigned char* src =
             reinterpret_cast<const unsigned char*>(p.logits) + ((long long)item.x * p.Vp + tbase) * ELT;
         if (p.host_logits) {
-            // logits in mapped host memory: 16-byte asynchronous copies, the
-            // stage's barrier completing when they have all landed
-            unsigned char* dst = stages + (size_t)stage * kTileBytes;
-            for (uint32_t o = 0; o < bytes; o += 16)
-                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst + o)), "l"(src + o) : "memory");
-            asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(&sm.full[stage])) : "memory");
+            // logits in mapped host memory: the compute warps copy the tile
+            // themselves (host_tile_copy); the item is posted now
+            mbar_arrive(&sm.full[stage]);
         } else {
             mbar_arrive_expect_tx(&sm.full[stage], bytes);
             bulk_load(stages + (size_t)stage * kTileBytes, src, bytes, &sm.full[stage],
@@ -1166,6 +1208,25 @@ __device__ __forceinline__ bool tile_work(const Params& p, Shared& sm, const uns
 // its partial results itself: the warps never wait for one another, except on
 // natural-alternative tiles, where the 8 warp thresholds and candidates are
 // exchanged through a candidate slot (bounded mbarrier waits).
+// Logits in pinned host memory mapped into the device's address space (TMA
+// bulk copies are kept for device memory): each compute thread copies its own
+// 16-byte vectors of the tile, the only ones it reads, so a warp moves 512
+// contiguous bytes per instruction and no block barrier is needed before the
+// reads.
+template <int ELT>
+__device__ __noinline__ void host_tile_copy(const Params& p, unsigned char* sp, int row, int tbase, int nv) {
+    const int tid = threadIdx.x;
+    const uint32_t bytes = (static_cast<uint32_t>(nv * ELT) + 15u) & ~15u;
+    const unsigned char* src = reinterpret_cast<const unsigned char*>(p.logits) + ((long long)row * p.Vp + tbase) * ELT;
+#pragma unroll
+    for (int c = 0; c < TileLayout<ELT>::NCH; ++c) {
+        const uint32_t o = static_cast<uint32_t>(c * kConsumerThreads + tid) * 16u;
+        if (o < bytes)
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(sp + o)), "l"(src + o) : "memory");
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 template <int ELT, bool SCORE>
 __device__ void compute_loop(const Params& p, Shared& sm, unsigned char* stages, unsigned long long t0, uint32_t ep) {
     constexpr int S = StageCfg<ELT>::kStages;
@@ -1188,6 +1249,7 @@ __device__ void compute_loop(const Params& p, Shared& sm, unsigned char* stages,
         const int tbase = tile * kTE;
         const int rem = V - tbase;
         const int nv = rem < kTE ? (rem > 0 ? rem : 0) : kTE;
+        if (p.host_logits) host_tile_copy<ELT>(p, stages + (size_t)stage * kTileBytes, info.x, tbase, nv);
         trace(p, kTrTileStart, info.x, tile, tid == 0);
         bool ok;
         if (__builtin_expect(nv == kTE, 1)) {
@@ -1330,8 +1392,11 @@ template <int ELT, bool SCORE>
 __global__ void __launch_bounds__(kThreads, StageCfg<ELT>::kMinBlocks) lp_stream_kernel(Params p) {
     constexpr int S = StageCfg<ELT>::kStages;
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    unsigned char* stages = smem_raw;
-    Shared& sm = *reinterpret_cast<Shared*>(smem_raw + (size_t)S * kTileBytes);
+    // the stages start on a 128-byte boundary (the static event counters come
+    // first).  At a 16-byte offset, every 32-byte sector of the 16-byte
+    // per-thread copies was fetched twice, and the bulk copies ran slower.
+    unsigned char* stages = smem_raw + ((kStageAlign - (smem_u32(smem_raw) & (kStageAlign - 1u))) & (kStageAlign - 1u));
+    Shared& sm = *reinterpret_cast<Shared*>(stages + (size_t)S * kTileBytes);
     const int tid = threadIdx.x;
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
@@ -1360,7 +1425,8 @@ __global__ void __launch_bounds__(kThreads, StageCfg<ELT>::kMinBlocks) lp_stream
     trace(p, kTrKernel, 0, 0, tid == 0);
     const int warp = tid >> 5;
     if (warp == kWarps) {
-        if (tid == kConsumerThreads) producer_loop<ELT>(p, sm, stages, t0);
+        const FirstClaim first = first_claim(p);
+        if (tid == kConsumerThreads) producer_loop<ELT>(p, sm, stages, t0, first);
         return;
     }
     if (warp == kWarps + 1) {
@@ -2352,7 +2418,7 @@ __global__ void __launch_bounds__(kConsumerThreads) lp_shard_merge_kernel(Params
 
 template <int ELT>
 constexpr int stream_smem_bytes() {
-    return StageCfg<ELT>::kStages * kTileBytes + (int)sizeof(Shared);
+    return StageCfg<ELT>::kStages * kTileBytes + (int)sizeof(Shared) + (int)kStageAlign;
 }
 
 }  // namespace
@@ -2422,7 +2488,7 @@ cudaError_t launch_epilogue(const Params& p_in, int dtype, const LaunchCfg& cfg,
     Params p = p_in;
     p.stream_grid = grid;
     p.build_records = records ? 1 : 0;
-    lp_prepare_kernel<<<1, 1024, 0, stream>>>(p);
+    lp_prepare_kernel<<<1, LP_PREP_THREADS, 0, stream>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];
