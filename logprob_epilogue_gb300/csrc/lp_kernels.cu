@@ -556,6 +556,11 @@ __device__ __forceinline__ GroupIn load_group(const Params& p, int g) {
     return x;
 }
 
+// Waves of first claims whose tiles the stream kernel brings into L2 before
+// its dependent-launch wait (0: none).
+#ifndef LP_EARLY_PREFETCH
+#define LP_EARLY_PREFETCH 1
+#endif
 #ifndef LP_PREP_THREADS
 #define LP_PREP_THREADS 1024
 #endif
@@ -724,8 +729,8 @@ __global__ void __launch_bounds__(LP_PREP_THREADS) lp_prepare_kernel(Params p) {
         }
         __syncthreads();
         if (need) {
-            p.queue[s_base + s_warp[warp] + pos_in_warp] =
-                queue_entry(g << 4, row0, mode0) | (k0 >= 1 ? kEntryNext : 0ull);
+            const int qpos = s_base + s_warp[warp] + pos_in_warp;
+            p.queue[qpos] = queue_entry(g << 4, row0, mode0) | (k0 >= 1 ? kEntryNext : 0ull);
             p.done[row0] = parent_bias;
             if (k0 > 0) atomicAdd(&s_chain, (unsigned)k0);
         }
@@ -1414,6 +1419,28 @@ __global__ void __launch_bounds__(kThreads, StageCfg<ELT>::kMinBlocks) lp_stream
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     __syncthreads();
+    // While the prepare kernel runs, each CTA brings into L2 the tiles of the
+    // first claims it stands for: ticket blockIdx.x + w * gridDim.x (w <
+    // LP_EARLY_PREFETCH), tile ticket % T of queue position ticket / T, taken
+    // to be group ticket / T's first row (every group read).  The inputs are
+    // the caller's, complete before the prepare kernel started; a guess that
+    // misses only costs its read.
+    if (LP_EARLY_PREFETCH > 0 && tid == kConsumerThreads && !p.host_logits) {
+        const long long T = p.T;
+        const long long row_bytes = ((long long)p.V * ELT + 15) & ~15ll;
+        for (int w = 0; w < LP_EARLY_PREFETCH; ++w) {
+            const long long t = (long long)blockIdx.x + (long long)w * gridDim.x;
+            const long long q = t / T;
+            if (q >= p.G) break;
+            const int row = p.targets != nullptr ? (int)q : __ldg(&p.indptr[q]);
+            if (row < 0 || row >= p.rows) continue;
+            const long long off = (t % T) * (long long)kTileBytes;
+            if (off >= row_bytes) continue;
+            const uint32_t sz = (uint32_t)min((long long)kTileBytes, row_bytes - off);
+            const unsigned char* a = reinterpret_cast<const unsigned char*>(p.logits) + (long long)row * p.Vp * ELT + off;
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a), "r"(sz) : "memory");
+        }
+    }
     asm volatile("griddepcontrol.wait;" ::: "memory");
     // the record kernel may be scheduled now (the prepare kernel's writes are
     // visible): its CTAs take the multiprocessor room this grid leaves, and
