@@ -377,7 +377,7 @@ int lp_plan_tiles_per_row(lp_plan_t plan);
 
 /* ---- Run without any device allocation ----
  *
- * No counterpart in the paper.  Some callers cannot call cudaMalloc: a serving
+ * No counterpart in the design pages.  Some callers cannot call cudaMalloc: a serving
  * process whose framework reserved the whole device for its own caching
  * allocator (a raw allocation then fails or splits its pool), code called back
  * from inside such an allocator (allocating there can deadlock on its lock),
